@@ -1,0 +1,34 @@
+"""Build the CPU oracle shared library (plain C, gcc, OpenMP over heads/queries).
+
+Test infrastructure only: the oracle is compiled so the tests, the smoke check
+and the benchmark's CPU-baseline leg can call it.  The product path never
+loads it.
+"""
+import os
+import platform
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "vcattn_oracle.c")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(OUT_DIR, "libvcattn_oracle.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle/vcattn_oracle.c into oracle/_build/libvcattn_oracle.so."""
+    os.makedirs(OUT_DIR, exist_ok=True)
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+        return LIB
+    flags = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared"]
+    if platform.machine() in ("x86_64", "AMD64"):
+        # Lets fmaf() compile to the FMA instruction instead of a libm call;
+        # results are the same either way (fmaf is correctly rounded).
+        flags.append("-mfma")
+    tmp = LIB + ".tmp%d" % os.getpid()
+    subprocess.check_call(["gcc", *flags, "-o", tmp, SRC, "-lm"])
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force=True))

@@ -1,0 +1,588 @@
+/*
+ * vcattn_oracle.c -- plain, slow CPU oracle for the smoothed FP8 attention
+ * forward (K centring + V-Smooth + ExpCast-FP8).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and
+ * the CPU-baseline leg of the benchmark load this library.  It shares no
+ * code, header, table or constant generator with the CUDA path.
+ *
+ * Sources (page titles; the pages give prose, not formulas):
+ *  [P1] "Feat: Attention Smoothing to Improve Generation Quality"
+ *       (TeleFuser PR #40), sections Summary and Changes: K centred by its
+ *       FP32 sequence mean before E4M3 quantisation; V centred and its mean
+ *       restored after attention.
+ *  [P2] "[perf] Add opt-in SM120 sparse attention forward kernel for
+ *       MiniMax-H3" (FastVideo PR #2048), section Changes / Test Results:
+ *       64x64 block-sparse forward with partial tiles and empty selections,
+ *       output O plus the log2-LSE.
+ *  [P3] "VC-Attention: Value Smoothing and Softmax Casting for Low-bit
+ *       Attention", Key Contributions 1-4 and Methodology: online k-means on
+ *       V, stable label sort applied jointly to K and V, per-block mean
+ *       subtraction with only the residual quantised, rank-one restoration
+ *       from the row sums, ExpCast-FP8 (affine log2 -> E4M3 byte with a
+ *       minimax centring constant, clip to normal codes, underflow to 0),
+ *       Proposition 3.1 (row TV bound 3.64% plus the underflow tail).
+ *
+ * Where the pages leave a step open, the reading taken is stated next to the
+ * code (R-numbers match the list of readings kept with the design notes).
+ *
+ * Floating point: compiled with -ffp-contract=off; every fused multiply-add
+ * is an explicit fmaf().  FP32 work that must agree bit for bit with the
+ * GPU follows the order written here; everything else is FP64.
+ *
+ * Parity pins: every function here is pinned by a -m "not gpu" test against
+ * a library routine, a closed form, an invariant or brute force.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_D 128
+#define ORC_BLK 64        /* quantisation / mean block (tokens)            */
+#define ORC_TILE 128      /* KV tile of the online-softmax recurrence      */
+#define ORC_UPD_CHUNK 512 /* token chunk of the centroid-sum order (R4)    */
+
+/* ------------------------------------------------------------------ */
+/* E4M3 (OCP FP8 E4M3FN): 1 sign, 4 exponent (bias 7), 3 mantissa bits,   */
+/* no infinities, 0x7F/0xFF are NaN, largest finite 448 = 0x7E.          */
+/* ------------------------------------------------------------------ */
+
+double orc_e4m3_decode(uint8_t c) {
+  int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);                /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* Round-to-nearest-even encode with saturation to +-448 (the behaviour of a
+ * saturating finite conversion).  The input is FP32; all steps below are
+ * exact in double except the single rint(). */
+uint8_t orc_e4m3_encode(float xf) {
+  double x = (double)xf;
+  if (isnan(x)) return 0x7F;
+  uint8_t s = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (a >= 448.0) return s | 0x7E;
+  if (a < ldexp(1.0, -6)) {               /* subnormal range, step 2^-9 */
+    double q = rint(a * 512.0);           /* RNE (default rounding mode) */
+    if (q >= 8.0) return s | 0x08;        /* rounds up to the min normal */
+    return s | (uint8_t)q;
+  }
+  int e;
+  frexp(a, &e);                           /* a = f * 2^e, f in [0.5, 1) */
+  e -= 1;                                 /* a = (1 + mant) * 2^e        */
+  double mant = ldexp(a, -e) - 1.0;       /* exact */
+  double r = rint(mant * 8.0);            /* RNE */
+  if (r >= 8.0) { r = 0.0; e += 1; }
+  int code = ((e + 7) << 3) | (int)r;
+  if (code > 0x7E) code = 0x7E;
+  return s | (uint8_t)code;
+}
+
+/* 1 when fp32 x lies exactly halfway between two adjacent E4M3 values
+ * (a rounding tie, counted by the parity tests). */
+int orc_e4m3_is_tie(float xf) {
+  double a = fabs((double)xf);
+  if (a >= 448.0 || a == 0.0) return 0;
+  if (a < ldexp(1.0, -6)) { double q = a * 512.0; return q - floor(q) == 0.5; }
+  int e; frexp(a, &e); e -= 1;
+  double q = (ldexp(a, -e) - 1.0) * 8.0;
+  return q - floor(q) == 0.5;
+}
+
+void orc_e4m3_encode_n(const float* x, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(x[i]);
+}
+void orc_e4m3_decode_n(const uint8_t* c, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
+}
+
+static float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* ------------------------------------------------------------------ */
+/* ExpCast-FP8 [P3 Key Contribution 2, Methodology, Proposition 3.1]     */
+/* ------------------------------------------------------------------ */
+/* An E4M3 byte (E<<3|M) encodes 2^(E-7)(1+M/8), so byte ~ 8*log2(value)+56
+ * up to the residual delta(M) = log2(1+M/8) - M/8, which lies in
+ * [0, 2c*] over the eight mantissa codes with c* = (log2(1.5) - 1/2)/2.
+ * Centring that residual (minimax) gives
+ *     byte = rint(8*y + 56 - 8c*)   for a value 2^y,
+ * and the byte is reinterpreted, not converted.  With the score already in
+ * code units (z = 8*log2(e)*sm_scale*logit, m = running max) and the byte
+ * encoding 2^off * p:
+ *     t = fmaf(x, A, B),  B = C - m,  C = 56 + 8*off - 8c*,
+ *     k = rint(t) (half to even),  code = k < 8 ? 0 : min(k, 126).
+ * Codes below 8 would be subnormal: they are the underflow tail and map to 0
+ * (R7).  The clip at 126 keeps the byte a finite normal (R7, R8). */
+double orc_expcast_cstar(void) { return (log2(1.5) - 0.5) / 2.0; }
+
+uint8_t orc_expcast_byte(float x, float A, float B) {
+  float t = fmaf(x, A, B);
+  float k = rintf(t);             /* half to even */
+  if (!(k >= 8.0f)) return 0;     /* underflow tail (also -inf / NaN) */
+  if (k > 126.0f) k = 126.0f;
+  return (uint8_t)k;
+}
+
+void orc_expcast_n(const float* x, float A, float B, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_expcast_byte(x[i], A, B);
+}
+
+/* ------------------------------------------------------------------ */
+/* Pairwise tree sum (R6): adjacent pairing,                             */
+/*   TREE(x[0..n)) = TREE(x[0..n/2)) + TREE(x[n/2..n)),  n a power of 2,  */
+/* in FP32.  Callers pad with +0 to a power of two.                      */
+/* ------------------------------------------------------------------ */
+static float tree_sum_f32(const float* x, int64_t n) {
+  if (n == 1) return x[0];
+  int64_t h = n / 2;
+  float a = tree_sum_f32(x, h);
+  float b = tree_sum_f32(x + h, h);
+  return a + b;
+}
+float orc_tree_sum(const float* x, int64_t n) { return tree_sum_f32(x, n); }
+
+static int64_t next_pow2(int64_t n) {
+  int64_t p = 1;
+  while (p < n) p *= 2;
+  return p;
+}
+
+/* ------------------------------------------------------------------ */
+/* V-Smooth grouping: online k-means on V [P3 Key Contribution 1]         */
+/* ------------------------------------------------------------------ */
+/* Readings (R2-R4): plain Lloyd iterations on the current V ("online" =
+ * at inference time, no calibration).  Init c_c = v[floor(c*N/k)].  One
+ * iteration = assign then update; the returned labels come from the last
+ * assign, the centroids from the last update.
+ *   assign: h_c = 0.5f * fmaf-chain_d(c_c[d]*c_c[d]);
+ *           dot = fmaf-chain over d = 0..127 ascending, starting at +0;
+ *           score = dot - h_c; label = lowest c with the largest score.
+ *   update: count_c; per chunk of 512 consecutive tokens, each member is
+ *           added in ascending token order to a +0 partial; the chunk
+ *           partials are added in ascending chunk order to a +0 total;
+ *           c_c = total / (float)count_c; an empty cluster keeps c_c. */
+static void kmeans_assign_one(const float* v, int64_t N, const float* cent, int k,
+                              int32_t* labels) {
+  float h[64];
+  for (int c = 0; c < k; ++c) {
+    float acc = 0.0f;
+    for (int d = 0; d < ORC_D; ++d) acc = fmaf(cent[c * ORC_D + d], cent[c * ORC_D + d], acc);
+    h[c] = 0.5f * acc;
+  }
+  for (int64_t j = 0; j < N; ++j) {
+    const float* vj = v + j * ORC_D;
+    float dot[64];
+    for (int c = 0; c < k; ++c) dot[c] = 0.0f;
+    /* c innermost so the k chains run side by side; each chain still
+     * visits d in ascending order. */
+    for (int d = 0; d < ORC_D; ++d)
+      for (int c = 0; c < k; ++c) dot[c] = fmaf(vj[d], cent[c * ORC_D + d], dot[c]);
+    int best = 0;
+    float bs = dot[0] - h[0];
+    for (int c = 1; c < k; ++c) {
+      float sc = dot[c] - h[c];
+      if (sc > bs) { bs = sc; best = c; }
+    }
+    labels[j] = best;
+  }
+}
+
+static void kmeans_update_one(const float* v, int64_t N, const int32_t* labels, int k,
+                              float* cent) {
+  float* total = (float*)calloc((size_t)k * ORC_D, sizeof(float));
+  float* part = (float*)malloc((size_t)k * ORC_D * sizeof(float));
+  int64_t count[64] = {0};
+  for (int64_t g0 = 0; g0 < N; g0 += ORC_UPD_CHUNK) {
+    int64_t g1 = g0 + ORC_UPD_CHUNK < N ? g0 + ORC_UPD_CHUNK : N;
+    memset(part, 0, (size_t)k * ORC_D * sizeof(float));
+    for (int64_t j = g0; j < g1; ++j) {
+      int c = labels[j];
+      count[c]++;
+      for (int d = 0; d < ORC_D; ++d) part[c * ORC_D + d] = part[c * ORC_D + d] + v[j * ORC_D + d];
+    }
+    for (int i = 0; i < k * ORC_D; ++i) total[i] = total[i] + part[i];
+  }
+  for (int c = 0; c < k; ++c) {
+    if (count[c] == 0) continue;
+    float n = (float)count[c];
+    for (int d = 0; d < ORC_D; ++d) cent[c * ORC_D + d] = total[c * ORC_D + d] / n;
+  }
+  free(part);
+  free(total);
+}
+
+/* V: [BH, N, 128] bf16 bits.  labels [BH, N]; centroids [BH, k, 128]. */
+int orc_kmeans(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
+               int32_t* labels, float* centroids) {
+  if (k < 1 || k > 64 || iters < 1 || N < 1) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bh = 0; bh < BH; ++bh) {
+    float* v = (float*)malloc((size_t)N * ORC_D * sizeof(float));
+    const uint16_t* src = V + bh * N * ORC_D;
+    for (int64_t i = 0; i < N * ORC_D; ++i) v[i] = bf16_to_f32(src[i]);
+    float* cent = centroids + bh * (int64_t)k * ORC_D;
+    for (int c = 0; c < k; ++c) {
+      int64_t j = ((int64_t)c * N) / k;
+      memcpy(cent + c * ORC_D, v + j * ORC_D, ORC_D * sizeof(float));
+    }
+    int32_t* lab = labels + bh * N;
+    for (int it = 0; it < iters; ++it) {
+      kmeans_assign_one(v, N, cent, k, lab);
+      kmeans_update_one(v, N, lab, k, cent);
+    }
+    free(v);
+  }
+  return 0;
+}
+
+/* Scores of the assign step for tie counting: score[j*k + c]. */
+int orc_kmeans_scores(const uint16_t* V, int64_t N, const float* cent, int k, float* score) {
+  float h[64];
+  for (int c = 0; c < k; ++c) {
+    float acc = 0.0f;
+    for (int d = 0; d < ORC_D; ++d) acc = fmaf(cent[c * ORC_D + d], cent[c * ORC_D + d], acc);
+    h[c] = 0.5f * acc;
+  }
+  for (int64_t j = 0; j < N; ++j)
+    for (int c = 0; c < k; ++c) {
+      float acc = 0.0f;
+      for (int d = 0; d < ORC_D; ++d)
+        acc = fmaf(bf16_to_f32(V[j * ORC_D + d]), cent[c * ORC_D + d], acc);
+      score[j * k + c] = acc - h[c];
+    }
+  return 0;
+}
+
+/* Stable sort of the labels (R5): perm[i] = index of the token at sorted
+ * position i, ordered by (label, index).  Written as a counting sort. */
+int orc_stable_sort(const int32_t* labels, int64_t BH, int64_t N, int k, int32_t* perm) {
+  for (int64_t bh = 0; bh < BH; ++bh) {
+    const int32_t* lab = labels + bh * N;
+    int32_t* p = perm + bh * N;
+    int64_t start[65] = {0};
+    for (int64_t j = 0; j < N; ++j) {
+      if (lab[j] < 0 || lab[j] >= k) return 1;
+      start[lab[j] + 1]++;
+    }
+    for (int c = 0; c < k; ++c) start[c + 1] += start[c];
+    for (int64_t j = 0; j < N; ++j) p[start[lab[j]]++] = (int32_t)j;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Preprocessing: K mean, gather, V block demean, quantisers             */
+/* [P1 Changes; P3 Key Contributions 1 and 3]                            */
+/* ------------------------------------------------------------------ */
+/* Readings (R6): one scale per 64-token block for Q (original order) and
+ * for centred, permuted K; one scale per channel for the V residual over
+ * the whole sequence.  amax = max|x| (FP32); amax below 2^-100 counts as
+ * 0 (bytes 0, scale 1); inv = fl(448/amax); byte = E4M3(fl(x*inv));
+ * scale = fl(amax/448).  Means are the adjacent-pairing tree over the 64
+ * tokens of a block (pad +0) and, for mu_K, over the blocks (pad +0 to a
+ * power of two), divided by the count of valid tokens.
+ *
+ * Layout: Npad = 128*ceil(N/128) rows; nbp = Npad/64 metadata blocks;
+ * rows >= N are 0x00, blocks >= ceil(N/64) have scale 1 and mean 0.
+ * r8t is the V residual transposed per head: [D, Npad]. */
+#define AMAX_FLOOR 7.888609052210118e-31f /* 2^-100 */
+
+static void quant_block(const float* x, int64_t rows, int64_t stride, int64_t cols,
+                        uint8_t* out, int64_t ostride, float* scale) {
+  float amax = 0.0f;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      float a = fabsf(x[r * stride + c]);
+      if (a > amax) amax = a;
+    }
+  if (!(amax >= AMAX_FLOOR)) {
+    for (int64_t r = 0; r < rows; ++r) memset(out + r * ostride, 0, (size_t)cols);
+    *scale = 1.0f;
+    return;
+  }
+  float inv = 448.0f / amax;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) out[r * ostride + c] = orc_e4m3_encode(x[r * stride + c] * inv);
+  *scale = amax / 448.0f;
+}
+
+int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+             int64_t BH, int64_t N,
+             uint8_t* q8, uint8_t* k8, uint8_t* r8t,
+             float* q_scale, float* k_scale, float* v_scale,
+             float* k_mean, float* v_mean, float* qmu) {
+  if (N < 1) return 1;
+  const int64_t Npad = ((N + ORC_TILE - 1) / ORC_TILE) * ORC_TILE;
+  const int64_t nbp = Npad / ORC_BLK;
+  const int64_t nb = (N + ORC_BLK - 1) / ORC_BLK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bh = 0; bh < BH; ++bh) {
+    const uint16_t* q = Q + bh * N * ORC_D;
+    const uint16_t* kk = K + bh * N * ORC_D;
+    const uint16_t* vv = V + bh * N * ORC_D;
+    const int32_t* p = perm ? perm + bh * N : NULL;
+    float* xf = (float*)malloc((size_t)Npad * ORC_D * sizeof(float));
+    float* tmp = (float*)malloc((size_t)next_pow2(nb) * sizeof(float));
+    float col[ORC_BLK];
+    uint8_t* Q8 = q8 + bh * Npad * ORC_D;
+    uint8_t* K8 = k8 + bh * Npad * ORC_D;
+    uint8_t* R8t = r8t + bh * Npad * ORC_D;
+    float* qs = q_scale + bh * nbp;
+    float* ks = k_scale + bh * nbp;
+    float* vs = v_scale + bh * ORC_D;
+    float* km = k_mean + bh * ORC_D;
+    float* vm = v_mean + bh * nbp * ORC_D;
+    memset(Q8, 0, (size_t)Npad * ORC_D);
+    memset(K8, 0, (size_t)Npad * ORC_D);
+    memset(R8t, 0, (size_t)Npad * ORC_D);
+    for (int64_t b = 0; b < nbp; ++b) { qs[b] = 1.0f; ks[b] = 1.0f; }
+    memset(vm, 0, (size_t)nbp * ORC_D * sizeof(float));
+
+    /* K mean over the original order: tree over each block, then over the
+     * blocks, divided by N. */
+    int64_t P = next_pow2(nb);
+    for (int d = 0; d < ORC_D; ++d) {
+      for (int64_t b = 0; b < P; ++b) {
+        if (b >= nb) { tmp[b] = 0.0f; continue; }
+        for (int i = 0; i < ORC_BLK; ++i) {
+          int64_t j = b * ORC_BLK + i;
+          col[i] = j < N ? bf16_to_f32(kk[j * ORC_D + d]) : 0.0f;
+        }
+        tmp[b] = tree_sum_f32(col, ORC_BLK);
+      }
+      km[d] = tree_sum_f32(tmp, P) / (float)N;
+    }
+
+    /* Q: per 64-query block, original order. */
+    for (int64_t j = 0; j < N; ++j)
+      for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] = bf16_to_f32(q[j * ORC_D + d]);
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
+      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, Q8 + r0 * ORC_D, ORC_D, &qs[b]);
+    }
+    /* qmu_i = q_i . mu_K, fmaf chain over d ascending (used for the LSE). */
+    for (int64_t j = 0; j < N; ++j) {
+      float acc = 0.0f;
+      for (int d = 0; d < ORC_D; ++d) acc = fmaf(xf[j * ORC_D + d], km[d], acc);
+      qmu[bh * N + j] = acc;
+    }
+
+    /* K: gathered by perm, centred, per-block scale. */
+    for (int64_t j = 0; j < N; ++j) {
+      int64_t src = p ? p[j] : j;
+      for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] = bf16_to_f32(kk[src * ORC_D + d]) - km[d];
+    }
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
+      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, K8 + r0 * ORC_D, ORC_D, &ks[b]);
+    }
+
+    /* V: gathered by perm; block means; residual; per-channel scale. */
+    for (int64_t j = 0; j < N; ++j) {
+      int64_t src = p ? p[j] : j;
+      for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] = bf16_to_f32(vv[src * ORC_D + d]);
+    }
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
+      for (int d = 0; d < ORC_D; ++d) {
+        for (int i = 0; i < ORC_BLK; ++i) col[i] = i < rows ? xf[(r0 + i) * ORC_D + d] : 0.0f;
+        vm[b * ORC_D + d] = tree_sum_f32(col, ORC_BLK) / (float)rows;
+      }
+    }
+    for (int64_t j = 0; j < N; ++j)
+      for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] = xf[j * ORC_D + d] - vm[(j / ORC_BLK) * ORC_D + d];
+    for (int d = 0; d < ORC_D; ++d) {
+      float amax = 0.0f;
+      for (int64_t j = 0; j < N; ++j) {
+        float a = fabsf(xf[j * ORC_D + d]);
+        if (a > amax) amax = a;
+      }
+      if (!(amax >= AMAX_FLOOR)) { vs[d] = 1.0f; continue; }  /* bytes stay 0 */
+      float inv = 448.0f / amax;
+      for (int64_t j = 0; j < N; ++j) R8t[d * Npad + j] = orc_e4m3_encode(xf[j * ORC_D + d] * inv);
+      vs[d] = amax / 448.0f;
+    }
+    free(tmp);
+    free(xf);
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* O2: the E4M3-emulating attention forward                              */
+/* [P3 Key Contributions 1-2; P2 Changes (partial tiles, empty           */
+/* selections, log2-LSE)]                                                */
+/* ------------------------------------------------------------------ */
+/* Per head, for each requested query i (original order), KV tiles of 128
+ * permuted keys (two 64-blocks) in ascending order, kept ones only:
+ *   x_ij  = sum_d dec(q8_id) dec(k8_jd), exact then rounded to FP32;
+ *   a_i   = fl(c0 * q_scale[i/64]),  c0 = fl(8 log2(e) sm_scale);
+ *   A_h   = fl(a_i * k_scale[2t+h]),  h = half of the tile;
+ *   m_tile= max_h fl(A_h * max_{valid j in h} x_ij);
+ *   rescale when m_tile > fl(m_run + tau8): m_run = m_tile and the running
+ *   sums are multiplied by 2^((m_old - m_tile)/8) (R9);
+ *   code  = ExpCast(x_ij, A_h, fl(C - m_run)), p = dec(code) (R7);
+ *   l_h   = sum of p over the half (R10);
+ *   acc  += sum_j p * (v_scale . dec(r8_j))  +  sum_h l_h mu_{2t+h}
+ *           (the rank-one mean restoration);   l += l_0 + l_1.
+ *   O_i   = acc / l;  lse2_i = m_run/8 - off + log2(l) + qmu_i sm_scale log2(e)
+ *   (R11); a row with no kept key gets O = 0, lse2 = -inf.
+ * Accumulation is FP64.  Switches (for the pins):
+ *   flags & 1: replace ExpCast by the exact 2^off * 2^((z - m)/8) in FP64,
+ *              z = 8 log2(e) sm_scale q_scale k_scale x_ij in FP64 (no byte,
+ *              no clip, no underflow);
+ *   flags & 2: use the dequantised V (v_scale*dec(r8) + mu_b) directly with
+ *              no separate mean term (the rank-one restoration pin).
+ * mask: [nq64, nbp] bytes (query 64-tile in original order, KV 64-block in
+ * permuted order), NULL = dense.  Keys j >= N are never valid. */
+int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
+                  const float* q_scale, const float* k_scale, const float* v_scale,
+                  const float* v_mean, const float* qmu, int64_t N,
+                  float sm_scale, int off, float tau8, const uint8_t* mask,
+                  const int64_t* qidx, int64_t nq, int flags,
+                  double* O, double* lse2) {
+  const int64_t Npad = ((N + ORC_TILE - 1) / ORC_TILE) * ORC_TILE;
+  const int64_t nbp = Npad / ORC_BLK;
+  const int64_t ntile = Npad / ORC_TILE;
+  const float c0 = (float)(8.0 * 1.4426950408889634 * (double)sm_scale);
+  const float C = (float)(56.0 + 8.0 * off - 8.0 * orc_expcast_cstar());
+  double dk[256];
+  for (int i = 0; i < 256; ++i) dk[i] = orc_e4m3_decode((uint8_t)i);
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t qi = 0; qi < nq; ++qi) {
+    const int64_t i = qidx[qi];
+    double acc[ORC_D], xs[ORC_TILE], xs64[ORC_TILE];
+    uint8_t valid[ORC_TILE];
+    for (int d = 0; d < ORC_D; ++d) acc[d] = 0.0;
+    double l = 0.0;
+    float m_run = -INFINITY;
+    const float a_i = c0 * q_scale[i / ORC_BLK];
+    for (int64_t t = 0; t < ntile; ++t) {
+      int kept[2];
+      for (int h = 0; h < 2; ++h)
+        kept[h] = mask ? mask[(i / ORC_BLK) * nbp + 2 * t + h] != 0 : 1;
+      if (!kept[0] && !kept[1]) continue;
+      float A[2], mx[2] = {-INFINITY, -INFINITY};
+      for (int h = 0; h < 2; ++h) A[h] = a_i * k_scale[2 * t + h];
+      for (int jj = 0; jj < ORC_TILE; ++jj) {
+        int64_t j = t * ORC_TILE + jj;
+        int h = jj / ORC_BLK;
+        valid[jj] = (j < N) && kept[h];
+        if (!valid[jj]) continue;
+        double s = 0.0;
+        for (int d = 0; d < ORC_D; ++d) s += dk[q8[i * ORC_D + d]] * dk[k8[j * ORC_D + d]];
+        xs64[jj] = s;                         /* exact */
+        xs[jj] = (double)(float)s;            /* FP32, as accumulated in hardware */
+        if ((float)s > mx[h]) mx[h] = (float)s;
+      }
+      float m_tile = fmaxf(A[0] * mx[0], A[1] * mx[1]);
+      if (m_tile == -INFINITY) continue;                 /* nothing valid */
+      if (m_tile > m_run + tau8) {
+        double alpha = m_run == -INFINITY ? 0.0 : exp2(((double)m_run - (double)m_tile) / 8.0);
+        for (int d = 0; d < ORC_D; ++d) acc[d] *= alpha;
+        l *= alpha;
+        m_run = m_tile;
+      }
+      const float B = C - m_run;
+      double lh[2] = {0.0, 0.0};
+      for (int jj = 0; jj < ORC_TILE; ++jj) {
+        if (!valid[jj]) continue;
+        int64_t j = t * ORC_TILE + jj;
+        int h = jj / ORC_BLK;
+        double pv;
+        if (flags & 1) {
+          /* exact score: FP64 coefficient, no FP32 rounding of A */
+          double z = 8.0 * 1.4426950408889634 * (double)sm_scale * (double)q_scale[i / ORC_BLK] *
+                     (double)k_scale[2 * t + h] * xs64[jj];
+          pv = exp2((double)off + (z - (double)m_run) / 8.0);
+        } else {
+          pv = dk[orc_expcast_byte((float)xs[jj], A[h], B)];
+        }
+        if (pv == 0.0) continue;
+        lh[h] += pv;
+        const float* mu = v_mean + (j / ORC_BLK) * ORC_D;
+        for (int d = 0; d < ORC_D; ++d) {
+          double r = (double)v_scale[d] * dk[r8t[d * Npad + j]];
+          if (flags & 2) r += (double)mu[d];
+          acc[d] += pv * r;
+        }
+      }
+      if (!(flags & 2))
+        for (int h = 0; h < 2; ++h) {
+          const float* mu = v_mean + (2 * t + h) * ORC_D;
+          for (int d = 0; d < ORC_D; ++d) acc[d] += lh[h] * (double)mu[d];
+        }
+      l += lh[0] + lh[1];
+    }
+    if (l > 0.0) {
+      for (int d = 0; d < ORC_D; ++d) O[qi * ORC_D + d] = acc[d] / l;
+      lse2[qi] = (double)m_run / 8.0 - off + log2(l) + (double)qmu[i] * (double)sm_scale * 1.4426950408889634;
+    } else {
+      for (int d = 0; d < ORC_D; ++d) O[qi * ORC_D + d] = 0.0;
+      lse2[qi] = -INFINITY;
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* O1: exact FP64 dense attention from the bf16 inputs.                  */
+/* With a mask, query i sees the original keys perm[p] for p in the kept */
+/* permuted 64-blocks of its query 64-tile.                              */
+/* ------------------------------------------------------------------ */
+int orc_attn_dense(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t N,
+                   float sm_scale, const uint8_t* mask, const int32_t* perm,
+                   const int64_t* qidx, int64_t nq, double* O, double* lse2) {
+  const int64_t Npad = ((N + ORC_TILE - 1) / ORC_TILE) * ORC_TILE;
+  const int64_t nbp = Npad / ORC_BLK;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t qi = 0; qi < nq; ++qi) {
+    const int64_t i = qidx[qi];
+    double* s = (double*)malloc((size_t)N * sizeof(double));
+    uint8_t* use = (uint8_t*)malloc((size_t)N);
+    double qv[ORC_D];
+    for (int d = 0; d < ORC_D; ++d) qv[d] = bf16_to_f32(Q[i * ORC_D + d]);
+    double mx = -INFINITY;
+    for (int64_t p = 0; p < N; ++p) {
+      int64_t j = perm ? perm[p] : p;
+      use[j] = mask ? mask[(i / ORC_BLK) * nbp + p / ORC_BLK] != 0 : 1;
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      if (!use[j]) continue;
+      double dot = 0.0;
+      for (int d = 0; d < ORC_D; ++d) dot += qv[d] * (double)bf16_to_f32(K[j * ORC_D + d]);
+      s[j] = dot * (double)sm_scale;
+      if (s[j] > mx) mx = s[j];
+    }
+    double l = 0.0, acc[ORC_D];
+    for (int d = 0; d < ORC_D; ++d) acc[d] = 0.0;
+    if (mx != -INFINITY)
+      for (int64_t j = 0; j < N; ++j) {
+        if (!use[j]) continue;
+        double w = exp(s[j] - mx);
+        l += w;
+        for (int d = 0; d < ORC_D; ++d) acc[d] += w * (double)bf16_to_f32(V[j * ORC_D + d]);
+      }
+    if (l > 0.0) {
+      for (int d = 0; d < ORC_D; ++d) O[qi * ORC_D + d] = acc[d] / l;
+      lse2[qi] = (mx + log(l)) * 1.4426950408889634;
+    } else {
+      for (int d = 0; d < ORC_D; ++d) O[qi * ORC_D + d] = 0.0;
+      lse2[qi] = -INFINITY;
+    }
+    free(use);
+    free(s);
+  }
+  return 0;
+}
