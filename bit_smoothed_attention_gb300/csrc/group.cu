@@ -1,0 +1,308 @@
+// V-Smooth grouping ("VC-Attention: Value Smoothing and Softmax Casting for
+// Low-bit Attention", Key Contribution 1 and Methodology): online k-means over
+// the value tokens of each (batch, head), then a stable sort of the labels
+// into the permutation applied jointly to K and V.
+//
+// Every FP32 result is produced in one fixed order so that labels, centroids
+// and the permutation are bit-for-bit reproducible:
+//   assign : h_c = 0.5f * (fmaf chain over d of c_c[d]^2); dot = one fmaf
+//            chain over d = 0..127 ascending; score = dot - h_c; the lowest
+//            cluster with the largest score wins.
+//   update : per 512-token chunk, the members of each cluster are added in
+//            token order to a +0 partial; partials are added in chunk order
+//            to a +0 total; centroid = total / (float)count (IEEE division);
+//            an empty cluster keeps its centroid.
+// This file is compiled with --fmad=false: only the explicit __fmaf_rn calls
+// fuse.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace vc {
+namespace {
+
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Init: c_c = v[floor(c*N/k)].  grid (BH), block D.
+__global__ void km_init(const uint16_t* __restrict__ V, int64_t N, int k, float* __restrict__ cent) {
+  const int64_t bh = blockIdx.x;
+  const int d = threadIdx.x;
+  for (int c = 0; c < k; ++c) {
+    const int64_t j = (static_cast<int64_t>(c) * N) / k;
+    cent[(bh * k + c) * D + d] = bf16f(V[(bh * N + j) * D + d]);
+  }
+}
+
+// Assign: each thread scores TT tokens against all clusters, accumulators in
+// registers; centroids live in shared memory transposed [d][c] so one 16-byte
+// broadcast load feeds 4 x TT FMAs.  Clusters c >= k get h = +inf and never
+// win.  grid (ceil(N / (256*TT)), BH), block 256.
+template <int KC, int TT>
+__global__ void __launch_bounds__(256) km_assign(const uint16_t* __restrict__ V, int64_t N, int k,
+                                                 const float* __restrict__ cent,
+                                                 int32_t* __restrict__ labels) {
+  __shared__ __align__(16) float cT[D][KC];
+  __shared__ float hs[KC];
+  const int64_t bh = blockIdx.y;
+  const float* cb = cent + bh * k * D;
+  for (int i = threadIdx.x; i < D * KC; i += blockDim.x) {
+    const int d = i / KC, c = i % KC;
+    cT[d][c] = c < k ? cb[c * D + d] : 0.0f;
+  }
+  __syncthreads();
+  if (threadIdx.x < KC) {
+    const int c = threadIdx.x;
+    if (c < k) {
+      float acc = 0.0f;
+      for (int d = 0; d < D; ++d) acc = __fmaf_rn(cT[d][c], cT[d][c], acc);
+      hs[c] = 0.5f * acc;
+    } else {
+      hs[c] = __int_as_float(0x7f800000);  // +inf
+    }
+  }
+  __syncthreads();
+
+  const uint16_t* vb = V + bh * N * D;
+  int64_t j[TT];
+  bool ok[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    j[t] = static_cast<int64_t>(blockIdx.x) * (256 * TT) + t * 256 + threadIdx.x;
+    ok[t] = j[t] < N;
+  }
+  float acc[TT][KC];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int c = 0; c < KC; ++c) acc[t][c] = 0.0f;
+
+#pragma unroll 1
+  for (int d0 = 0; d0 < D; d0 += 8) {
+    float vv[TT][8];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      if (ok[t]) {
+        unpack8(*reinterpret_cast<const uint4*>(vb + j[t] * D + d0), vv[t]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vv[t][e] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int dd = 0; dd < 8; ++dd) {
+#pragma unroll
+      for (int c4 = 0; c4 < KC / 4; ++c4) {
+        const float4 cc = *reinterpret_cast<const float4*>(&cT[d0 + dd][4 * c4]);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          acc[t][4 * c4 + 0] = __fmaf_rn(vv[t][dd], cc.x, acc[t][4 * c4 + 0]);
+          acc[t][4 * c4 + 1] = __fmaf_rn(vv[t][dd], cc.y, acc[t][4 * c4 + 1]);
+          acc[t][4 * c4 + 2] = __fmaf_rn(vv[t][dd], cc.z, acc[t][4 * c4 + 2]);
+          acc[t][4 * c4 + 3] = __fmaf_rn(vv[t][dd], cc.w, acc[t][4 * c4 + 3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    if (!ok[t]) continue;
+    int best = 0;
+    float bs = acc[t][0] - hs[0];
+#pragma unroll
+    for (int c = 1; c < KC; ++c) {
+      const float sc = acc[t][c] - hs[c];
+      if (sc > bs) {
+        bs = sc;
+        best = c;
+      }
+    }
+    labels[bh * N + j[t]] = best;
+  }
+}
+
+// Chunk partial sums: thread d owns channel d of every cluster's partial.
+// grid (nchunk, BH), block D.
+__global__ void __launch_bounds__(D) km_partial(const uint16_t* __restrict__ V,
+                                                const int32_t* __restrict__ labels, int64_t N,
+                                                int k, int nchunk, float* __restrict__ part,
+                                                int32_t* __restrict__ cnt, uint32_t* err) {
+  __shared__ float ps[KMAX][D];
+  __shared__ int cs[KMAX];
+  const int64_t bh = blockIdx.y;
+  const int g = blockIdx.x;
+  const int d = threadIdx.x;
+  for (int c = 0; c < k; ++c) ps[c][d] = 0.0f;
+  if (d < KMAX) cs[d] = 0;
+  __syncthreads();
+  const int64_t j0 = static_cast<int64_t>(g) * UPD_CHUNK;
+  const int64_t j1 = j0 + UPD_CHUNK < N ? j0 + UPD_CHUNK : N;
+  const uint16_t* vb = V + bh * N * D;
+  const int32_t* lb = labels + bh * N;
+  bool bad = false;
+  for (int64_t j = j0; j < j1; j += 8) {
+    int cl[8];
+    float vv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (j + u < j1) {
+        cl[u] = lb[j + u];
+        vv[u] = bf16f(vb[(j + u) * D + d]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (j + u < j1) {
+        const int c = cl[u];
+        if (static_cast<unsigned>(c) >= static_cast<unsigned>(k)) {
+          bad = true;
+          continue;
+        }
+        ps[c][d] = ps[c][d] + vv[u];
+        if (d == 0) cs[c] += 1;
+      }
+    }
+  }
+  if (bad && d == 0) atomicOr(err, ERR_BAD_LABEL);
+  __syncthreads();
+  float* pg = part + (bh * nchunk + g) * static_cast<int64_t>(k) * D;
+  for (int c = 0; c < k; ++c) pg[c * D + d] = ps[c][d];
+  if (d < k) cnt[(bh * nchunk + g) * k + d] = cs[d];
+}
+
+// Centroid = (partials added in chunk order) / count.  grid (k, BH), block D.
+__global__ void __launch_bounds__(D) km_finalize(const float* __restrict__ part,
+                                                 const int32_t* __restrict__ cnt, int nchunk,
+                                                 int k, float* __restrict__ cent) {
+  const int64_t bh = blockIdx.y;
+  const int c = blockIdx.x;
+  const int d = threadIdx.x;
+  float total = 0.0f;
+  int count = 0;
+  for (int g = 0; g < nchunk; ++g) {
+    const int64_t o = (bh * nchunk + g) * k + c;
+    total = total + part[o * D + d];
+    count += cnt[o];
+  }
+  if (count > 0) cent[(bh * k + c) * D + d] = total / static_cast<float>(count);
+}
+
+// Output offsets of the stable counting sort: offs[g][c] = (tokens with a
+// smaller label) + (tokens with label c in earlier chunks).  grid (BH),
+// block KMAX.
+__global__ void sort_offsets(const int32_t* __restrict__ cnt, int nchunk, int k,
+                             int32_t* __restrict__ offs) {
+  __shared__ int tot[KMAX];
+  const int64_t bh = blockIdx.x;
+  const int c = threadIdx.x;
+  int t = 0;
+  if (c < k)
+    for (int g = 0; g < nchunk; ++g) t += cnt[(bh * nchunk + g) * k + c];
+  tot[c] = t;
+  __syncthreads();
+  if (c < k) {
+    int run = 0;
+    for (int c2 = 0; c2 < c; ++c2) run += tot[c2];
+    for (int g = 0; g < nchunk; ++g) {
+      const int64_t o = (bh * nchunk + g) * k + c;
+      offs[o] = run;
+      run += cnt[o];
+    }
+  }
+}
+
+// Stable scatter of one 512-token chunk: rank among equal labels within a
+// warp from __match_any_sync, then an exclusive prefix over the chunk's
+// warps.  grid (nchunk, BH), block 512.
+__global__ void __launch_bounds__(UPD_CHUNK) sort_scatter(const int32_t* __restrict__ labels,
+                                                          const int32_t* __restrict__ offs,
+                                                          int64_t N, int k, int nchunk,
+                                                          int32_t* __restrict__ perm) {
+  constexpr int NW = UPD_CHUNK / 32;
+  __shared__ int wc[NW][KMAX];
+  const int64_t bh = blockIdx.y;
+  const int g = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < NW * KMAX; i += UPD_CHUNK) wc[i / KMAX][i % KMAX] = 0;
+  __syncthreads();
+  const int64_t j = static_cast<int64_t>(g) * UPD_CHUNK + tid;
+  const bool valid = j < N;
+  int c = valid ? labels[bh * N + j] : -1;
+  if (valid && static_cast<unsigned>(c) >= static_cast<unsigned>(k)) c = -1;  // reported by km_partial
+  const unsigned same = __match_any_sync(0xffffffffu, c);
+  const int rank = __popc(same & ((1u << lane) - 1u));
+  if (c >= 0 && rank == 0) wc[warp][c] = __popc(same);
+  __syncthreads();
+  if (tid < k) {
+    int run = 0;
+    for (int w = 0; w < NW; ++w) {
+      const int t = wc[w][tid];
+      wc[w][tid] = run;
+      run += t;
+    }
+  }
+  __syncthreads();
+  if (c >= 0) perm[bh * N + offs[(bh * nchunk + g) * k + c] + wc[warp][c] + rank] = static_cast<int32_t>(j);
+}
+
+template <int KC, int TT>
+cudaError_t assign(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
+                   int32_t* labels, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(N, 256 * TT)), static_cast<unsigned>(BH));
+  km_assign<KC, TT><<<grid, 256, 0, s>>>(V, N, k, cent, labels);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws) {
+  const int64_t nchunk = ceil_div(N, UPD_CHUNK);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return base ? static_cast<char*>(base) + o : nullptr;
+  };
+  GroupWs w{};
+  w.cent = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * k * D * 4));
+  w.part = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * nchunk * k * D * 4));
+  w.cnt = reinterpret_cast<int32_t*>(take(static_cast<size_t>(BH) * nchunk * k * 4));
+  w.offs = reinterpret_cast<int32_t*>(take(static_cast<size_t>(BH) * nchunk * k * 4));
+  if (ws) *ws = w;
+  return off;
+}
+
+cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
+                         int32_t* labels, int32_t* perm, float* centroids_out, const GroupWs& ws,
+                         uint32_t* err, cudaStream_t s) {
+  const int nchunk = static_cast<int>(ceil_div(N, UPD_CHUNK));
+  float* cent = centroids_out ? centroids_out : ws.cent;
+  km_init<<<static_cast<unsigned>(BH), D, 0, s>>>(V, N, k, cent);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const dim3 gchunk(nchunk, static_cast<unsigned>(BH));
+  for (int it = 0; it < iters; ++it) {
+    if (k <= 8) e = assign<8, 8>(V, BH, N, k, cent, labels, s);
+    else if (k <= 16) e = assign<16, 8>(V, BH, N, k, cent, labels, s);
+    else if (k <= 32) e = assign<32, 4>(V, BH, N, k, cent, labels, s);
+    else e = assign<64, 2>(V, BH, N, k, cent, labels, s);
+    if (e != cudaSuccess) return e;
+    km_partial<<<gchunk, D, 0, s>>>(V, labels, N, k, nchunk, ws.part, ws.cnt, err);
+    km_finalize<<<dim3(k, static_cast<unsigned>(BH)), D, 0, s>>>(ws.part, ws.cnt, nchunk, k, cent);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  sort_offsets<<<static_cast<unsigned>(BH), KMAX, 0, s>>>(ws.cnt, nchunk, k, ws.offs);
+  sort_scatter<<<gchunk, UPD_CHUNK, 0, s>>>(labels, ws.offs, N, k, nchunk, perm);
+  return cudaGetLastError();
+}
+
+}  // namespace vc

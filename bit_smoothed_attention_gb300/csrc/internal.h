@@ -1,0 +1,66 @@
+// Internal declarations shared by the translation units of libvcattn.so.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace vc {
+
+constexpr int D = 128;          // head dimension
+constexpr int BLK = 64;         // quantisation / mean block (tokens)
+constexpr int TILE = 128;       // KV tile and padding granule
+constexpr int UPD_CHUNK = 512;  // token chunk of the centroid sums
+constexpr int KMAX = 64;        // largest k-means k
+constexpr float AMAX_FLOOR = 7.888609052210118e-31f;  // 2^-100
+
+// Device error word codes (bit flags, OR-ed by kernels).
+constexpr uint32_t ERR_TIMEOUT = 1u;
+constexpr uint32_t ERR_BAD_LABEL = 2u;
+
+__host__ __device__ inline int64_t npad(int64_t n) { return ((n + TILE - 1) / TILE) * TILE; }
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// ---- grouping (group.cu) ----
+struct GroupWs {
+  float* cent;    // [BH, k, D]
+  float* part;    // [BH, nchunk, k, D]
+  int32_t* cnt;   // [BH, nchunk, k]
+  int32_t* offs;  // [BH, nchunk, k]
+};
+size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws);
+cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
+                         int32_t* labels, int32_t* perm, float* centroids_out, const GroupWs& ws,
+                         uint32_t* err, cudaStream_t s);
+
+// ---- preprocessing (prep.cu) ----
+struct PrepOut {
+  uint8_t *q8, *k8, *r8t;
+  float *q_scale, *k_scale, *v_scale, *k_mean, *v_mean, *qmu, *vmu_op;
+};
+struct PrepWs {
+  float* kbs;       // [BH, nbp, D] K block sums (original order)
+  uint32_t* vamax;  // [BH, D] V residual amax (float bits)
+};
+size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws);
+cudaError_t launch_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+                        int64_t BH, int64_t N, const PrepOut& out, const PrepWs& ws, cudaStream_t s);
+
+// ---- attention (attn.cu) ----
+struct AttnArgs {
+  const uint8_t *q8, *k8, *r8t;
+  const float *q_scale, *k_scale, *v_scale, *qmu, *vmu_op;
+  const uint8_t* mask;  // nullable
+  void* O;              // bf16, or f32 when out_f32
+  int out_f32;
+  float* lse2;          // nullable
+  int64_t BH, N;
+  float sm_scale;
+  int off;
+  float tau8;
+  uint32_t* err;
+  int debug_flags;  // test hook: bit 0 = the TMA producer issues nothing
+};
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+
+}  // namespace vc

@@ -1,0 +1,343 @@
+// Fused preprocessing of the smoothed FP8 attention forward:
+//  - K centring ("Feat: Attention Smoothing to Improve Generation Quality",
+//    Changes: K centred by its FP32 sequence mean before E4M3 quantisation);
+//  - V-Smooth ("VC-Attention: Value Smoothing and Softmax Casting for Low-bit
+//    Attention", Key Contributions 1 and 3): K and V gathered by the grouping
+//    permutation, each 64-token block of V demeaned, only the residual
+//    quantised; the gather happens on the fly so the permuted bf16 tensors
+//    never make an HBM round trip.
+//
+// Thread mapping of the block kernels (256 threads, one 64-token block):
+// lane bits 0..3 pick a group of 4 consecutive tokens, lane bit 4 and the
+// warp pick a chunk of 8 channels; each thread loads 4 x 16 bytes.  Block
+// sums are the adjacent-pairing tree: the 4 tokens of a thread first, then a
+// shuffle butterfly over the token-group lanes (xor 1, 2, 4, 8).
+// Quantiser: amax = max|x|; amax < 2^-100 -> bytes 0, scale 1; inv =
+// fl(448/amax); byte = E4M3_rne_satfinite(fl(x*inv)); scale = fl(amax/448).
+// Compiled with --fmad=false: only explicit __fmaf_rn calls fuse.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace vc {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Two FP32 values -> two E4M3 bytes (round to nearest even, saturating to
+// +-448), `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint2 e4m3x8(const float (&x)[8]) {
+  uint2 o;
+  o.x = e4m3x2(x[0], x[1]) | (e4m3x2(x[2], x[3]) << 16);
+  o.y = e4m3x2(x[4], x[5]) | (e4m3x2(x[6], x[7]) << 16);
+  return o;
+}
+
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+struct Map {
+  int warp, lane, g, cc;
+};
+__device__ __forceinline__ Map thread_map() {
+  Map m;
+  m.warp = threadIdx.x >> 5;
+  m.lane = threadIdx.x & 31;
+  m.g = m.lane & 15;                     // token group (4 tokens)
+  m.cc = 2 * m.warp + (m.lane >> 4);     // channel chunk (8 channels)
+  return m;
+}
+
+// Load 4 rows x 8 channels; rows past N are zero.  `perm` maps a sorted
+// position to its source token (nullptr = identity).
+__device__ __forceinline__ void load_block(const uint16_t* base, const int32_t* perm, int64_t r0,
+                                           int64_t N, int cc, float (&x)[4][8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t r = r0 + i;
+    if (r < N) {
+      const int64_t src = perm ? perm[r] : r;
+      unpack8(*reinterpret_cast<const uint4*>(base + src * D + 8 * cc), x[i]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) x[i][c] = 0.0f;
+    }
+  }
+}
+
+// Adjacent-pairing tree over the 64 tokens of the block (per channel).
+__device__ __forceinline__ void block_tree(const float (&x)[4][8], float (&s)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) s[c] = (x[0][c] + x[1][c]) + (x[2][c] + x[3][c]);
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) s[c] = s[c] + __shfl_xor_sync(0xffffffffu, s[c], m);
+}
+
+__device__ __forceinline__ float max16(float a) {
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  return a;
+}
+
+// Block max over all 256 threads.
+__device__ __forceinline__ float block_max(float a, float* red) {
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+// Stats: K block sums (original order), mean of each permuted V block, and
+// the per-channel amax of the V residual.  grid (nb, BH), block 256.
+__global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K,
+                                                  const uint16_t* __restrict__ V,
+                                                  const int32_t* __restrict__ perm, int64_t N,
+                                                  int nbp, float* __restrict__ kbs,
+                                                  float* __restrict__ v_mean,
+                                                  uint32_t* __restrict__ vamax) {
+  const Map m = thread_map();
+  const int64_t b = blockIdx.x, bh = blockIdx.y;
+  const int64_t r0 = b * BLK + 4 * m.g;
+  const int32_t* ph = perm ? perm + bh * N : nullptr;
+  float kx[4][8], vx[4][8];
+  load_block(K + bh * N * D, nullptr, r0, N, m.cc, kx);
+  load_block(V + bh * N * D, ph, r0, N, m.cc, vx);
+  float ks[8], vs[8], mu[8];
+  block_tree(kx, ks);
+  block_tree(vx, vs);
+  const int64_t nvalid = N - b * BLK < BLK ? N - b * BLK : BLK;
+  const float fn = static_cast<float>(nvalid);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) mu[c] = vs[c] / fn;
+  float am[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (r0 + i < N) a = fmaxf(a, fabsf(vx[i][c] - mu[c]));
+    am[c] = max16(a);
+  }
+  if (m.g == 0) {
+    const int64_t o = (bh * nbp + b) * D + 8 * m.cc;
+    *reinterpret_cast<float4*>(kbs + o) = make_float4(ks[0], ks[1], ks[2], ks[3]);
+    *reinterpret_cast<float4*>(kbs + o + 4) = make_float4(ks[4], ks[5], ks[6], ks[7]);
+    *reinterpret_cast<float4*>(v_mean + o) = make_float4(mu[0], mu[1], mu[2], mu[3]);
+    *reinterpret_cast<float4*>(v_mean + o + 4) = make_float4(mu[4], mu[5], mu[6], mu[7]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) atomicMax(vamax + bh * D + 8 * m.cc + c, __float_as_uint(am[c]));
+  }
+}
+
+// mu_K = (adjacent-pairing tree over the block sums, padded with +0 to a
+// power of two) / N; v_scale from the residual amax.  grid (BH), block D.
+__global__ void __launch_bounds__(D) prep_kmean(const float* __restrict__ kbs,
+                                                const uint32_t* __restrict__ vamax, int64_t N,
+                                                int nb, int nbp, float* __restrict__ k_mean,
+                                                float* __restrict__ v_scale) {
+  const int64_t bh = blockIdx.x;
+  const int d = threadIdx.x;
+  int64_t P = 1;
+  while (P < nb) P *= 2;
+  float st[40];
+  int top = 0;
+  for (int64_t b = 0; b < P; ++b) {
+    float v = b < nb ? kbs[(bh * nbp + b) * D + d] : 0.0f;
+    for (int64_t t = b; t & 1; t >>= 1) v = st[--top] + v;
+    st[top++] = v;
+  }
+  k_mean[bh * D + d] = st[0] / static_cast<float>(N);
+  const float a = __uint_as_float(vamax[bh * D + d]);
+  v_scale[bh * D + d] = a >= AMAX_FLOOR ? a / 448.0f : 1.0f;
+}
+
+// Quantisers.  grid (nbp, BH), block 256.
+__global__ void __launch_bounds__(256) prep_quant(
+    const uint16_t* __restrict__ Q, const uint16_t* __restrict__ K, const uint16_t* __restrict__ V,
+    const int32_t* __restrict__ perm, int64_t N, int64_t Npad, int nbp,
+    const uint32_t* __restrict__ vamax, const float* __restrict__ k_mean,
+    const float* __restrict__ v_scale, float* __restrict__ v_mean, uint8_t* __restrict__ q8,
+    uint8_t* __restrict__ k8, uint8_t* __restrict__ r8t, float* __restrict__ q_scale,
+    float* __restrict__ k_scale, float* __restrict__ qmu, float* __restrict__ vmu_op) {
+  __shared__ float qs[BLK][D + 1];
+  __shared__ float kmu[D];
+  __shared__ __align__(16) uint8_t tb[D][BLK + 16];
+  __shared__ float red[8];
+  const Map m = thread_map();
+  const int64_t b = blockIdx.x, bh = blockIdx.y;
+  const int64_t r0 = b * BLK + 4 * m.g;
+  const int64_t nb = ceil_div(N, BLK);
+  const bool pad_block = b >= nb;
+  const int32_t* ph = perm ? perm + bh * N : nullptr;
+  if (threadIdx.x < D) kmu[threadIdx.x] = k_mean[bh * D + threadIdx.x];
+
+  // ---- Q: per 64-query block, original order ----
+  float x[4][8];
+  load_block(Q + bh * N * D, nullptr, r0, N, m.cc, x);
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      a = fmaxf(a, fabsf(x[i][c]));
+      qs[4 * m.g + i][8 * m.cc + c] = x[i][c];
+    }
+  float amax = block_max(a, red);  // contains a __syncthreads (qs, kmu visible)
+  bool live = amax >= AMAX_FLOOR;
+  float inv = live ? 448.0f / amax : 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float y[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) y[c] = (live && r0 + i < N) ? x[i][c] * inv : 0.0f;
+    *reinterpret_cast<uint2*>(q8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
+  }
+  if (threadIdx.x == 0) q_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
+  if (threadIdx.x < BLK) {
+    const int64_t r = b * BLK + threadIdx.x;
+    if (r < N) {
+      float acc = 0.0f;
+      for (int d = 0; d < D; ++d) acc = __fmaf_rn(qs[threadIdx.x][d], kmu[d], acc);
+      qmu[bh * N + r] = acc;
+    }
+  }
+
+  // ---- K: gathered, centred, per 64-key block ----
+  load_block(K + bh * N * D, ph, r0, N, m.cc, x);
+  a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      x[i][c] = (r0 + i < N) ? x[i][c] - kmu[8 * m.cc + c] : 0.0f;
+      a = fmaxf(a, fabsf(x[i][c]));
+    }
+  amax = block_max(a, red);
+  live = amax >= AMAX_FLOOR;
+  inv = live ? 448.0f / amax : 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float y[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) y[c] = live ? x[i][c] * inv : 0.0f;
+    *reinterpret_cast<uint2*>(k8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
+  }
+  if (threadIdx.x == 0) k_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
+
+  // ---- V: gathered, block-demeaned residual, per-channel scale, transposed ----
+  load_block(V + bh * N * D, ph, r0, N, m.cc, x);
+  const int64_t mo = (bh * nbp + b) * D + 8 * m.cc;
+  float mu[8], vinv[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    mu[c] = pad_block ? 0.0f : v_mean[mo + c];
+    const float am = __uint_as_float(vamax[bh * D + 8 * m.cc + c]);
+    vinv[c] = am >= AMAX_FLOOR ? 448.0f / am : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float y[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) y[c] = (r0 + i < N) ? (x[i][c] - mu[c]) * vinv[c] : 0.0f;
+    const uint2 by = e4m3x8(y);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w = c < 4 ? by.x : by.y;
+      tb[8 * m.cc + c][4 * m.g + i] = static_cast<uint8_t>(w >> (8 * (c & 3)));
+    }
+  }
+  if (pad_block && m.g == 0) {
+    *reinterpret_cast<float4*>(v_mean + mo) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(v_mean + mo + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __syncthreads();
+  {
+    const int d = threadIdx.x >> 1, h = threadIdx.x & 1;
+    const uint4* src = reinterpret_cast<const uint4*>(&tb[d][32 * h]);
+    uint4* dst = reinterpret_cast<uint4*>(r8t + (bh * D + d) * Npad + b * BLK + 32 * h);
+    dst[0] = src[0];
+    dst[1] = src[1];
+  }
+  // ---- mean operand of the rank-one restoration MMA ----
+  // B[k][n = d] of a [K = 8] x [N = 128] tf32 operand, K-major, no swizzle:
+  // k = 3h, 3h+1, 3h+2 hold (hi, hi, lo) of mu_b[d] / v_scale[d] for the
+  // block's half h of its 128-key tile; k = 6, 7 are zero.
+  if (threadIdx.x < D) {
+    const int d = threadIdx.x;
+    const float mud = pad_block ? 0.0f : v_mean[(bh * nbp + b) * D + d];
+    const float u = mud / v_scale[bh * D + d];
+    const float hi = to_tf32(u);
+    const float lo = to_tf32(u - hi);
+    const int h = static_cast<int>(b & 1);
+    float* tile = vmu_op + (bh * (Npad / TILE) + (b >> 1)) * 1024;
+    auto at = [&](int kk) -> float& {
+      return tile[((d >> 3) * 256 + (kk >> 2) * 128 + (d & 7) * 16 + (kk & 3) * 4) / 4];
+    };
+    at(3 * h) = hi;
+    at(3 * h + 1) = hi;
+    at(3 * h + 2) = lo;
+    if (h == 1) {
+      at(6) = 0.0f;
+      at(7) = 0.0f;
+    }
+  }
+}
+
+}  // namespace
+
+size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws) {
+  const int64_t nbp = npad(N) / BLK;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return base ? static_cast<char*>(base) + o : nullptr;
+  };
+  PrepWs w{};
+  w.kbs = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * nbp * D * 4));
+  w.vamax = reinterpret_cast<uint32_t*>(take(static_cast<size_t>(BH) * D * 4));
+  if (ws) *ws = w;
+  return off;
+}
+
+cudaError_t launch_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+                        int64_t BH, int64_t N, const PrepOut& o, const PrepWs& ws, cudaStream_t s) {
+  const int64_t Np = npad(N);
+  const int nbp = static_cast<int>(Np / BLK);
+  const int nb = static_cast<int>(ceil_div(N, BLK));
+  cudaError_t e = cudaMemsetAsync(ws.vamax, 0, static_cast<size_t>(BH) * D * 4, s);
+  if (e != cudaSuccess) return e;
+  prep_stats<<<dim3(nb, static_cast<unsigned>(BH)), 256, 0, s>>>(K, V, perm, N, nbp, ws.kbs,
+                                                                 o.v_mean, ws.vamax);
+  prep_kmean<<<static_cast<unsigned>(BH), D, 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp, o.k_mean,
+                                                     o.v_scale);
+  prep_quant<<<dim3(nbp, static_cast<unsigned>(BH)), 256, 0, s>>>(
+      Q, K, V, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
+      o.q_scale, o.k_scale, o.qmu, o.vmu_op);
+  return cudaGetLastError();
+}
+
+}  // namespace vc

@@ -1,0 +1,233 @@
+"""Python binding of libvcattn.so (ctypes; argument marshalling only).
+
+Every step of the path runs in the library's CUDA kernels; this module only
+allocates the caller-side buffers with PyTorch, passes pointers and the
+current CUDA stream, and turns status codes into exceptions.  There is no
+fallback: if the library is missing or the device is not sm_103a, calls fail.
+
+Names follow the C ABI in include/vcattn.h: ``group``, ``prep``, ``attn``,
+``fwd``, ``last_device_error``.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = _build.LIB
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(6)
+
+
+class VcattnError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, _lib().vcattn_status_string(status).decode(), status))
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("D", ctypes.c_int64)]
+
+
+class PreppedStruct(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("q8", "k8", "r8t", "q_scale", "k_scale", "v_scale", "k_mean", "v_mean", "qmu",
+                 "vmu_op")]
+
+
+_L = None
+
+
+def _lib():
+    global _L
+    if _L is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libvcattn.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        P, SP, sz, st = ctypes.c_void_p, ctypes.POINTER(Shape), ctypes.c_size_t, ctypes.c_int
+        PP = ctypes.POINTER(PreppedStruct)
+        lib.vcattn_npad.restype = ctypes.c_int64
+        lib.vcattn_npad.argtypes = [ctypes.c_int64]
+        lib.vcattn_group_workspace_bytes.restype = sz
+        lib.vcattn_group_workspace_bytes.argtypes = [SP, ctypes.c_int]
+        lib.vcattn_group.restype = st
+        lib.vcattn_group.argtypes = [SP, P, ctypes.c_int, ctypes.c_int, P, P, P, P, sz, P]
+        lib.vcattn_prepped_bytes.restype = sz
+        lib.vcattn_prepped_bytes.argtypes = [SP]
+        lib.vcattn_prepped_carve.restype = st
+        lib.vcattn_prepped_carve.argtypes = [SP, P, sz, PP]
+        lib.vcattn_prep_workspace_bytes.restype = sz
+        lib.vcattn_prep_workspace_bytes.argtypes = [SP]
+        lib.vcattn_prep.restype = st
+        lib.vcattn_prep.argtypes = [SP, P, P, P, P, PP, P, sz, P]
+        lib.vcattn_attn.restype = st
+        lib.vcattn_attn.argtypes = [SP, PP, ctypes.c_float, P, P, P, P]
+        lib.vcattn_attn_ex.restype = st
+        lib.vcattn_attn_ex.argtypes = [SP, PP, ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                       P, P, P, P]
+        lib.vcattn_fwd_workspace_bytes.restype = sz
+        lib.vcattn_fwd_workspace_bytes.argtypes = [SP]
+        lib.vcattn_fwd.restype = st
+        lib.vcattn_fwd.argtypes = [SP, P, P, P, P, ctypes.c_float, P, P, P, P, sz, P]
+        lib.vcattn_last_device_error.restype = st
+        lib.vcattn_last_device_error.argtypes = [P]
+        lib.vcattn_status_string.restype = ctypes.c_char_p
+        lib.vcattn_status_string.argtypes = [st]
+        _L = lib
+    return _L
+
+
+def lib():
+    """The loaded ctypes library (raw C ABI)."""
+    return _lib()
+
+
+def _check(status, what):
+    if status != OK:
+        raise VcattnError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _shape(x):
+    B, H, N, D = x.shape
+    return Shape(B, H, N, D)
+
+
+def _req(x, dtype, name):
+    if not (x.is_cuda and x.dtype == dtype and x.is_contiguous()):
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+
+
+def npad(N):
+    return int(_lib().vcattn_npad(N))
+
+
+def group(V, k, iters=5, centroids=False, stream=None):
+    """k-means labels and the stable-sort permutation of V [B,H,N,128] bf16.
+    Returns (labels, perm[, centroids]) as int32 [B,H,N] (and f32 [B,H,k,128])."""
+    _req(V, torch.bfloat16, "V")
+    s = _shape(V)
+    B, H, N, _ = V.shape
+    labels = torch.empty(B, H, N, dtype=torch.int32, device=V.device)
+    perm = torch.empty_like(labels)
+    cent = torch.empty(B, H, k, 128, dtype=torch.float32, device=V.device) if centroids else None
+    nbytes = _lib().vcattn_group_workspace_bytes(ctypes.byref(s), k)
+    if nbytes == 0:
+        raise ValueError("unsupported grouping shape or k")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=V.device)
+    _check(_lib().vcattn_group(ctypes.byref(s), _ptr(V), k, iters, _ptr(labels), _ptr(perm),
+                               _ptr(cent), _ptr(ws), nbytes, _stream(stream)), "vcattn_group")
+    return (labels, perm, cent) if centroids else (labels, perm)
+
+
+class Prepped:
+    """Owner of the prepped buffer (one torch allocation) plus views of its parts."""
+
+    def __init__(self, shape_tuple, device):
+        B, H, N, D = shape_tuple
+        self.shape = Shape(B, H, N, D)
+        self.nbytes = _lib().vcattn_prepped_bytes(ctypes.byref(self.shape))
+        if self.nbytes == 0:
+            raise ValueError("unsupported shape")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.struct = PreppedStruct()
+        _check(_lib().vcattn_prepped_carve(ctypes.byref(self.shape), _ptr(self.buf), self.nbytes,
+                                           ctypes.byref(self.struct)), "vcattn_prepped_carve")
+
+    def views(self):
+        """Torch views of the prepped tensors (for tests)."""
+        B, H, N = self.shape.B, self.shape.H, self.shape.N
+        Np = npad(N)
+        nbp = Np // 64
+        base = self.buf.data_ptr()
+
+        def v(name, shape, dtype):
+            off = getattr(self.struct, name) - base
+            n = 1
+            for d in shape:
+                n *= d
+            esz = torch.empty((), dtype=dtype).element_size()
+            return self.buf[off:off + n * esz].view(dtype).view(*shape)
+
+        return dict(
+            q8=v("q8", (B * H, Np, 128), torch.uint8), k8=v("k8", (B * H, Np, 128), torch.uint8),
+            r8t=v("r8t", (B * H, 128, Np), torch.uint8),
+            q_scale=v("q_scale", (B * H, nbp), torch.float32),
+            k_scale=v("k_scale", (B * H, nbp), torch.float32),
+            v_scale=v("v_scale", (B * H, 128), torch.float32),
+            k_mean=v("k_mean", (B * H, 128), torch.float32),
+            v_mean=v("v_mean", (B * H, nbp, 128), torch.float32),
+            qmu=v("qmu", (B * H, N), torch.float32),
+            vmu_op=v("vmu_op", (B * H, Np // 128, 1024), torch.float32))
+
+
+def prep(Q, K, V, perm=None, out=None, stream=None):
+    """Fused K mean, gather by perm, V block demean and Q/K/V quantisers."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _req(t, torch.bfloat16, n)
+    if perm is not None:
+        _req(perm, torch.int32, "perm")
+    pp = out if out is not None else Prepped(tuple(Q.shape), Q.device)
+    s = _shape(Q)
+    nbytes = _lib().vcattn_prep_workspace_bytes(ctypes.byref(s))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
+    _check(_lib().vcattn_prep(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(perm),
+                              ctypes.byref(pp.struct), _ptr(ws), nbytes, _stream(stream)),
+           "vcattn_prep")
+    return pp
+
+
+def attn(pp, sm_scale, mask=None, off=8, tau8=0.0, out_f32=False, O=None, lse2=None, want_lse=True,
+         stream=None):
+    """Attention forward from prepped tensors.  Returns (O [B,H,N,128] bf16, or f32 with
+    out_f32, and lse2 f32 [B,H,N])."""
+    B, H, N = pp.shape.B, pp.shape.H, pp.shape.N
+    dev = pp.buf.device
+    if O is None:
+        O = torch.empty(B, H, N, 128, dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
+    if lse2 is None and want_lse:
+        lse2 = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    if mask is not None:
+        _req(mask, torch.uint8, "mask")
+    _check(_lib().vcattn_attn_ex(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale),
+                                 int(off), float(tau8), int(bool(out_f32)), _ptr(mask), _ptr(O),
+                                 _ptr(lse2),
+                                 _stream(stream)), "vcattn_attn")
+    return O, lse2
+
+
+def fwd(Q, K, V, perm, sm_scale, mask=None, O=None, lse2=None, ws=None, stream=None):
+    """vcattn_fwd: prep into a workspace + attention, one call."""
+    s = _shape(Q)
+    nbytes = _lib().vcattn_fwd_workspace_bytes(ctypes.byref(s))
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
+    if O is None:
+        O = torch.empty_like(Q)
+    if lse2 is None:
+        lse2 = torch.empty(Q.shape[:3], dtype=torch.float32, device=Q.device)
+    _check(_lib().vcattn_fwd(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(perm), float(sm_scale),
+                             _ptr(mask), _ptr(O), _ptr(lse2), _ptr(ws), ws.numel(), _stream(stream)),
+           "vcattn_fwd")
+    return O, lse2
+
+
+def fwd_workspace_bytes(shape_tuple):
+    s = Shape(*shape_tuple)
+    return int(_lib().vcattn_fwd_workspace_bytes(ctypes.byref(s)))
+
+
+def last_device_error(stream=None):
+    """Synchronise and return (and clear) the device error status."""
+    return _lib().vcattn_last_device_error(_stream(stream))

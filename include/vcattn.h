@@ -1,0 +1,178 @@
+/*
+ * vcattn.h -- C ABI of libvcattn.so: the FP8 (E4M3) smoothed attention
+ * forward for GB300 (sm_103a).
+ *
+ * The operation, as described by the pages it comes from:
+ *  - "Feat: Attention Smoothing to Improve Generation Quality" (TeleFuser
+ *    PR #40), Summary and Changes: K is centred by its FP32 sequence mean
+ *    before E4M3 quantisation (exact under softmax); V is centred and the
+ *    mean restored.
+ *  - "VC-Attention: Value Smoothing and Softmax Casting for Low-bit
+ *    Attention", Key Contributions 1-3 and Methodology: V-Smooth (online
+ *    k-means over value tokens, a stable sort of the labels into a
+ *    permutation applied jointly to K and V, per-block mean subtraction with
+ *    only the residual quantised, the means restored inside the online
+ *    softmax from the per-block row sums) and ExpCast-FP8 (the probability's
+ *    E4M3 byte written from the max-subtracted log2 score with one FMA and
+ *    one integer rounding).
+ *  - "[perf] Add opt-in SM120 sparse attention forward kernel for
+ *    MiniMax-H3" (FastVideo PR #2048), Changes and Test Results: a 64x64
+ *    block-sparse forward that handles partial tiles and empty selections
+ *    and returns O plus the log2-LSE.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are contiguous.  Q, K, V, O are bf16 [B, H, N, D] with D = 128.
+ *  - The caller owns and allocates every device buffer, including the
+ *    workspaces sized by the *_workspace_bytes queries.  The library never
+ *    allocates, never frees and never synchronises (except
+ *    vcattn_last_device_error).  All pointers are device pointers unless
+ *    stated otherwise; every device pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream); all work
+ *    is enqueued on it in order.
+ *  - Argument errors return at once and enqueue nothing.  A failed launch
+ *    returns VCATTN_ERR_CUDA.  Errors found on the device (a bounded wait
+ *    that ran out, a bad label) are recorded in a per-device error word and
+ *    reported by the next vcattn_last_device_error().
+ *  - Calls on different streams with different buffers are independent.
+ */
+#ifndef VCATTN_H
+#define VCATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VCATTN_OK = 0,
+  VCATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, small workspace */
+  VCATTN_ERR_UNSUPPORTED = 2, /* D != 128, k outside [1, 64], no sm_103a device        */
+  VCATTN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed                */
+  VCATTN_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out (device error word) */
+  VCATTN_ERR_DEVICE = 5       /* another device-side check failed (device error word)   */
+} vcattn_status;
+
+/* Problem shape.  D must be 128; N >= 1; B, H >= 1. */
+typedef struct {
+  int64_t B, H, N, D;
+} vcattn_shape;
+
+/* Output of vcattn_prep, input of vcattn_attn.  With Npad = 128*ceil(N/128)
+ * rows and nbp = Npad/64 metadata blocks per head (blocks at or past
+ * ceil(N/64) are padding: scale 1, mean 0; rows at or past N are 0x00):
+ *   q8      [B,H,Npad,D]  u8  E4M3 Q, original token order
+ *   k8      [B,H,Npad,D]  u8  E4M3 centred K, permuted order
+ *   r8t     [B,H,D,Npad]  u8  E4M3 V residual, permuted order, transposed
+ *   q_scale [B,H,nbp]     f32 one scale per 64-query block
+ *   k_scale [B,H,nbp]     f32 one scale per 64-key block
+ *   v_scale [B,H,D]       f32 one scale per channel
+ *   k_mean  [B,H,D]       f32 mu_K, the FP32 sequence mean of K
+ *   v_mean  [B,H,nbp,D]   f32 mu_b, the FP32 mean of each permuted 64-block of V
+ *   qmu     [B,H,N]       f32 q . mu_K (restores the true LSE)
+ *   vmu_op  [B,H,Npad/128,1024] f32 the block means divided by v_scale,
+ *           split into tf32 high and low parts, laid out as the B operand of
+ *           the mean-restoration MMA (one 4 KiB tile per 128 keys).
+ * vcattn_prepped_carve() fills this struct from one buffer of
+ * vcattn_prepped_bytes() bytes. */
+typedef struct {
+  uint8_t *q8, *k8, *r8t;
+  float *q_scale, *k_scale, *v_scale, *k_mean, *v_mean, *qmu, *vmu_op;
+} vcattn_prepped;
+
+/* Padded row count 128*ceil(N/128) of the FP8 tensors. */
+int64_t vcattn_npad(int64_t N);
+
+/* ---------------------------------------------------------------- grouping */
+/* V-Smooth grouping (VC-Attention, Key Contribution 1 and Methodology):
+ * `iters` Lloyd iterations of k-means over the value tokens of each (b, h),
+ * then a stable sort of the labels.  Init c_c = v[floor(c*N/k)]; one
+ * iteration assigns every token to the cluster with the largest
+ * v.c - |c|^2/2 (FP32, one fmaf chain over d ascending; ties to the lowest
+ * cluster) and recomputes each centroid as the mean of its members (sums over
+ * 512-token chunks in token order, chunks in order; empty clusters keep
+ * their centroid).
+ *   V         bf16 [B,H,N,D] (device)
+ *   labels    i32  [B,H,N]   out: cluster of each token (last assignment)
+ *   perm      i32  [B,H,N]   out: perm[i] = token at sorted position i,
+ *                             sorted by (label, token index)
+ *   centroids f32  [B,H,k,D] out, nullable: centroids after the last update
+ *   ws        device scratch of at least vcattn_group_workspace_bytes(shape, k)
+ * k in [1, 64], iters >= 1.  Results are bit-for-bit deterministic. */
+size_t vcattn_group_workspace_bytes(const vcattn_shape* shape, int k);
+vcattn_status vcattn_group(const vcattn_shape* shape, const void* V, int k, int iters,
+                           int32_t* labels, int32_t* perm, float* centroids,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------- preprocessing */
+/* Fused preprocessing (TeleFuser PR #40 Changes; VC-Attention Key
+ * Contributions 1 and 3): mu_K over the original order; K gathered by perm,
+ * centred and quantised per 64-key block; V gathered by perm, each 64-block
+ * demeaned and only the residual quantised with one scale per channel; Q
+ * quantised per 64-query block in the original order.  Quantiser: amax =
+ * max|x| (amax < 2^-100 gives bytes 0 and scale 1), byte =
+ * E4M3_rne_satfinite(x * fl(448/amax)), scale = fl(amax/448).  Means are
+ * adjacent-pairing FP32 tree sums divided by the valid count.
+ *   Q, K, V  bf16 [B,H,N,D] (device)
+ *   perm     i32  [B,H,N] (device), nullable = identity; must be a
+ *            permutation of [0, N) per head (not validated on the device)
+ *   out      the prepped buffers (device pointers inside a host struct)
+ *   ws       device scratch of at least vcattn_prep_workspace_bytes(shape) */
+size_t vcattn_prepped_bytes(const vcattn_shape* shape);
+vcattn_status vcattn_prepped_carve(const vcattn_shape* shape, void* base, size_t bytes,
+                                   vcattn_prepped* out);
+size_t vcattn_prep_workspace_bytes(const vcattn_shape* shape);
+vcattn_status vcattn_prep(const vcattn_shape* shape, const void* Q, const void* K, const void* V,
+                          const int32_t* perm, const vcattn_prepped* out,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------- attention */
+/* FP8 attention forward with ExpCast-FP8 and the rank-one mean restoration
+ * (VC-Attention Key Contributions 1-2; FastVideo PR #2048 for the mask,
+ * partial tiles, empty selections and the log2-LSE).  Per query i (original
+ * order) over KV tiles of 128 permuted keys:
+ *   x = q8_i . k8_j (FP8 tensor cores, FP32 accumulate);
+ *   A = fl(fl(c0*q_scale)*k_scale), c0 = fl(8*log2(e)*sm_scale);
+ *   running max m (code units) rescales when the tile max exceeds
+ *   m + tau8 (tau8 = 0: exact running max);
+ *   byte = ExpCast(x) = clip(rint(fmaf(x, A, C - m))), C = 56 + 8*off - 8c*,
+ *   c* = (log2 1.5 - 1/2)/2, bytes below 8 flush to 0, above 126 clip;
+ *   O_i = v_scale . (P8 R8 + sum_b l_ib mu_b / v_scale) / l_i  (bf16),
+ *   lse2_i = m/8 - off + log2(l_i) + qmu_i * sm_scale * log2(e).
+ *   in        prepped tensors from vcattn_prep
+ *   sm_scale  softmax scale (> 0)
+ *   tile_mask u8 [B,H,ceil(N/64),Npad/64] (device), nullable = dense:
+ *             nonzero keeps (query 64-tile in original order, key 64-block
+ *             in permuted order); a row with no kept key gets O = 0 and
+ *             lse2 = -inf
+ *   O         bf16 [B,H,N,D] (device) out
+ *   lse2      f32 [B,H,N] (device) out, nullable
+ * vcattn_attn uses off = 8, tau8 = 0 and writes bf16 O; vcattn_attn_ex takes
+ * off and tau8 (0 <= off <= 8, 0 <= tau8 <= 8*(8.75 - off) so codes stay
+ * <= 126) and, with out_f32 = 1, writes O as f32 [B,H,N,D] instead of bf16
+ * (the value before the final bf16 rounding). */
+vcattn_status vcattn_attn(const vcattn_shape* shape, const vcattn_prepped* in, float sm_scale,
+                          const uint8_t* tile_mask, void* O, float* lse2, void* stream);
+vcattn_status vcattn_attn_ex(const vcattn_shape* shape, const vcattn_prepped* in, float sm_scale,
+                             int off, float tau8, int out_f32, const uint8_t* tile_mask, void* O,
+                             float* lse2, void* stream);
+
+/* One call = vcattn_prep into `ws` followed by vcattn_attn.  perm is the
+ * output of vcattn_group (or of an earlier step, or NULL = identity). */
+size_t vcattn_fwd_workspace_bytes(const vcattn_shape* shape);
+vcattn_status vcattn_fwd(const vcattn_shape* shape, const void* Q, const void* K, const void* V,
+                         const int32_t* perm, float sm_scale, const uint8_t* tile_mask,
+                         void* O, float* lse2, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ errors */
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: VCATTN_OK, VCATTN_ERR_TIMEOUT or VCATTN_ERR_DEVICE (or
+ * VCATTN_ERR_CUDA when the synchronisation itself fails). */
+vcattn_status vcattn_last_device_error(void* stream);
+const char* vcattn_status_string(vcattn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VCATTN_H */

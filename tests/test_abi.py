@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads and exports every symbol its headers declare;
+host-side argument validation works without a GPU (no compute calls)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_smoothed_attention_gb300 import build, vcattn
+    build.build()
+    return vcattn.lib()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(vcattn_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"vcattn_group", "vcattn_prep", "vcattn_attn", "vcattn_fwd",
+            "vcattn_last_device_error"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def _shape(B=1, H=2, N=1000, D=128):
+    from bit_smoothed_attention_gb300.vcattn import Shape
+    return Shape(B, H, N, D)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.vcattn_status_string(s)
+
+
+def test_workspace_queries(lib):
+    s = _shape()
+    g = lib.vcattn_group_workspace_bytes(ctypes.byref(s), 8)
+    p = lib.vcattn_prep_workspace_bytes(ctypes.byref(s))
+    pb = lib.vcattn_prepped_bytes(ctypes.byref(s))
+    f = lib.vcattn_fwd_workspace_bytes(ctypes.byref(s))
+    assert g > 0 and p > 0 and pb > 0 and f >= pb + p
+    assert lib.vcattn_group_workspace_bytes(ctypes.byref(s), 0) == 0
+    assert lib.vcattn_group_workspace_bytes(ctypes.byref(s), 65) == 0
+    bad = _shape(D=64)
+    assert lib.vcattn_prepped_bytes(ctypes.byref(bad)) == 0
+    big = _shape(N=4096)
+    assert lib.vcattn_prepped_bytes(ctypes.byref(big)) > pb
+    assert lib.vcattn_npad(1) == 128 and lib.vcattn_npad(128) == 128 and lib.vcattn_npad(129) == 256
+
+
+def test_prepped_carve_layout(lib):
+    from bit_smoothed_attention_gb300.vcattn import PreppedStruct
+    s = _shape(N=777)
+    nb = lib.vcattn_prepped_bytes(ctypes.byref(s))
+    base = 1 << 20   # carving only computes addresses; nothing is touched
+    out = PreppedStruct()
+    assert lib.vcattn_prepped_carve(ctypes.byref(s), ctypes.c_void_p(base), nb, ctypes.byref(out)) == 0
+    addrs = sorted((getattr(out, f), f) for f, _ in PreppedStruct._fields_)
+    assert all(a % 256 == 0 for a, _ in addrs)
+    assert addrs[0][0] == base and addrs[-1][0] < base + nb
+    assert lib.vcattn_prepped_carve(ctypes.byref(s), ctypes.c_void_p(base), nb - 1,
+                                    ctypes.byref(out)) == 1
+    assert lib.vcattn_prepped_carve(ctypes.byref(s), ctypes.c_void_p(base + 8), nb,
+                                    ctypes.byref(out)) == 1
+
+
+def test_argument_validation_without_gpu(lib):
+    """Invalid arguments are rejected before any CUDA call."""
+    P = ctypes.c_void_p
+    s = _shape()
+    fake = P(1 << 20)
+    # D != 128
+    bad = _shape(D=64)
+    assert lib.vcattn_group(ctypes.byref(bad), fake, 8, 5, fake, fake, None, fake, 1 << 30, None) == 2
+    # k outside [1, 64]
+    assert lib.vcattn_group(ctypes.byref(s), fake, 0, 5, fake, fake, None, fake, 1 << 30, None) == 2
+    assert lib.vcattn_group(ctypes.byref(s), fake, 65, 5, fake, fake, None, fake, 1 << 30, None) == 2
+    # null pointers, zero iterations, misalignment, short workspace
+    assert lib.vcattn_group(ctypes.byref(s), None, 8, 5, fake, fake, None, fake, 1 << 30, None) == 1
+    assert lib.vcattn_group(ctypes.byref(s), fake, 8, 0, fake, fake, None, fake, 1 << 30, None) == 1
+    assert lib.vcattn_group(ctypes.byref(s), P((1 << 20) + 4), 8, 5, fake, fake, None, fake,
+                            1 << 30, None) == 1
+    assert lib.vcattn_group(ctypes.byref(s), fake, 8, 5, fake, fake, None, fake, 16, None) == 1
+    # shape errors
+    for B, H, N in ((0, 1, 10), (1, 0, 10), (1, 1, 0)):
+        z = _shape(B, H, N)
+        assert lib.vcattn_prepped_bytes(ctypes.byref(z)) == 0
+    from bit_smoothed_attention_gb300.vcattn import PreppedStruct
+    pp = PreppedStruct()
+    assert lib.vcattn_prep(ctypes.byref(s), fake, fake, fake, None, ctypes.byref(pp), fake, 1 << 30,
+                           None) == 1
+    assert lib.vcattn_attn(ctypes.byref(s), ctypes.byref(pp), ctypes.c_float(0.1), None, fake, None,
+                           None) == 1
+    assert lib.vcattn_fwd(ctypes.byref(s), fake, fake, fake, None, ctypes.c_float(0.1), None, fake,
+                          None, fake, 16, None) == 1
