@@ -25,6 +25,7 @@ UNITS = {
     "group.cu": ["--fmad=false"],
     "prep.cu": ["--fmad=false"],
     "attn.cu": [],
+    "prep_noalloc.cu": [],
 }
 HEADERS = ["internal.h", "ptx.cuh"]
 

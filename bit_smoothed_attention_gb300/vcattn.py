@@ -231,3 +231,20 @@ def fwd_workspace_bytes(shape_tuple):
 def last_device_error(stream=None):
     """Synchronise and return (and clear) the device error status."""
     return _lib().vcattn_last_device_error(_stream(stream))
+
+
+def prep_noalloc(Q, K, V, perm=None, out=None, stream=None):
+    """vcattn_prep without a caller workspace: for callers that cannot
+    allocate device memory at call time.  The scratch is a 16 MiB array owned
+    by the library (shared by all calls on a device; overlapping calls race)."""
+    f = _lib().vcattn_prep_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(Shape), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.POINTER(PreppedStruct), ctypes.c_void_p]
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _req(t, torch.bfloat16, n)
+    pp = out if out is not None else Prepped(tuple(Q.shape), Q.device)
+    s = _shape(Q)
+    _check(f(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(perm), ctypes.byref(pp.struct),
+             _stream(stream)), "vcattn_prep_noalloc")
+    return pp

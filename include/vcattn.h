@@ -127,6 +127,28 @@ vcattn_status vcattn_prep(const vcattn_shape* shape, const void* Q, const void* 
                           const int32_t* perm, const vcattn_prepped* out,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* Preprocessing without a caller-provided workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory when they call the preprocessing, such as a plugin
+ * that receives only its input and output tensors from a host framework, or
+ * a program that forbids device allocation after start-up.  It computes
+ * exactly what vcattn_prep computes (same kernels, same outputs) but keeps
+ * its scratch in a 16 MiB device array owned by the library, held on every
+ * GPU that loads the library until the process exits.
+ *   - Problems needing more than 16 MiB of scratch (256-byte-rounded
+ *     B*H*(Npad/64)*512 + B*H*512 bytes; the 56-head, 32,626-token workload
+ *     needs 14.7 MB) return VCATTN_ERR_UNSUPPORTED with nothing enqueued.
+ *   - The first call on a device looks up the array's device address; make
+ *     it before any stream capture begins.
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents; each call clears what must start at zero on its own stream.
+ *     Calls that overlap on the GPU race on the array: order them on one
+ *     stream.
+ *   - It allocates and frees nothing. */
+vcattn_status vcattn_prep_noalloc(const vcattn_shape* shape, const void* Q, const void* K,
+                                  const void* V, const int32_t* perm, const vcattn_prepped* out,
+                                  void* stream);
+
 /* --------------------------------------------------------------- attention */
 /* FP8 attention forward with ExpCast-FP8 and the rank-one mean restoration
  * (VC-Attention Key Contributions 1-2; FastVideo PR #2048 for the mask,
