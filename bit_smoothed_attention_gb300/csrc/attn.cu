@@ -6,19 +6,36 @@
 // partial tiles, empty selections and log2-LSE from "[perf] Add opt-in SM120
 // sparse attention forward kernel for MiniMax-H3", Changes):
 //   S = Q8 K8^T (E4M3 x E4M3 -> FP32 in TMEM);
-//   the softmax warps turn S into E4M3 probability bytes with ExpCast:
-//     t = fmaf(x, A, C - m), byte = clip(rint(t)) (no exp2, no cvt);
-//   O += P8 R8 (E4M3 x E4M3) and, in the same TMEM accumulator, the block
-//   means restored as sum_b l_b mu_b / v_scale by one tf32 MMA whose A operand
-//   is the per-64-key-block row sums of the decoded bytes (split hi/lo) and
-//   whose B operand is the prepared mean tile (split hi/lo).
+//   the softmax warps turn S into E4M3 probability bytes with ExpCast
+//   (byte = rint(fmaf(x, A, C - m)), bytes below 8 flush to 0) on the FMA
+//   pipe: no exp2, no conversion instruction;
+//   the bytes P8 go back to TMEM and feed, as the A operand,
+//   [O | l] += P8 [R8 ; 1_b0 ; 1_b1] (E4M3, N = 144): the 128 output
+//   channels plus the per-64-key-block row sums of the decoded bytes, from
+//   the same MMA;
+//   the block means are restored in the same accumulator as
+//   sum_b l_b mu_b / v_scale by one tf32 MMA whose A operand is the row sums
+//   split into tf32 high and low parts and whose B operand is the prepared
+//   mean tile.
 //
 // CTA = 256 query rows (two 128-row slots) of one (b, h).  Warps 0-3 run the
 // softmax of slot 0 (thread = row = TMEM lane), warps 4-7 slot 1, warp 8
-// issues TMA loads, warp 9 allocates TMEM and issues the MMAs from one lane.
-// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512) columns.
-// The MMA issue order QK0 QK1 PV0 PV1 lets slot 0's softmax overlap QK1 and
-// slot 1's softmax overlap PV0 and the next QK0.
+// issues TMA loads, warp 9 allocates TMEM and issues every MMA from one lane.
+// TMEM columns: S [0,128) shared by the slots, P0 [128,160), P1 [160,192),
+// O0 [192,336), O1 [352,496); columns 128 and 129 of O_s hold the tile's row
+// sums, which the softmax reads and clears after each PV.
+//
+// Per KV tile t the MMA lane issues, slot 0 then slot 1,
+//   PV_s(t) | QK_s(t+1) | MEAN_s(t)
+// and the softmax of slot s does
+//   wait S(t), load it, release S -> max, ExpCast -> P(t), rescale O ->
+//   wait PV(t) -> read and clear the row sums, l += ..., write the mean
+//   operand.
+// The two slots overlap: while one computes, the tensor core runs the other
+// slot's MMAs, and QK(t+1) starts as soon as PV(t) is queued, in parallel
+// with the row-sum read-back.  tcgen05 operations of one thread complete in issue order,
+// so "PV(t+1) done" implies MEAN(t) done; a softmax that must rescale O waits
+// for MEAN(t) explicitly first.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -32,19 +49,25 @@
 namespace vc {
 namespace {
 
-constexpr int NS = 3;          // K/V/mean pipeline stages
+constexpr int NS = 4;          // K/V/mean pipeline stages
 constexpr int NTHREADS = 320;  // 8 softmax warps + TMA warp + MMA warp
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int CTA_ROWS = 256;
 
-constexpr uint32_t TILE_BYTES = 16384;  // 128 x 128 E4M3
-constexpr uint32_t MU_BYTES = 4096;     // 128 x 8 tf32
+// TMEM columns
+constexpr uint32_t COL_S = 0;
+constexpr uint32_t COL_P = 128;    // + 32 * slot
+constexpr uint32_t COL_O = 192;    // + 160 * slot; 144 columns each
+constexpr uint32_t COL_L = 128;    // row sums inside O_s
+
+constexpr uint32_t TILE_BYTES = 16384;    // 128 x 128 E4M3
+constexpr uint32_t V_STAGE = 18432;       // V tile + 16 indicator rows
+constexpr uint32_t MU_BYTES = 4096;       // 128 x 8 tf32
 constexpr uint32_t SM_Q = 0;
 constexpr uint32_t SM_K = SM_Q + 2 * TILE_BYTES;
 constexpr uint32_t SM_V = SM_K + NS * TILE_BYTES;
-constexpr uint32_t SM_P = SM_V + NS * TILE_BYTES;
-constexpr uint32_t SM_MU = SM_P + 2 * TILE_BYTES;
+constexpr uint32_t SM_MU = SM_V + NS * V_STAGE;
 constexpr uint32_t SM_L = SM_MU + NS * MU_BYTES;
 constexpr uint32_t SM_BAR = SM_L + 2 * MU_BYTES;
 enum {
@@ -52,10 +75,12 @@ enum {
   B_KVFULL = 1,
   B_KVEMPTY = B_KVFULL + NS,
   B_SFULL = B_KVEMPTY + NS,
-  B_SFREE = B_SFULL + 2,
-  B_PFULL = B_SFREE + 2,
+  B_STAKEN = B_SFULL + 2,
+  B_PFULL = B_STAKEN + 2,
   B_ODONE = B_PFULL + 2,
-  B_FIN = B_ODONE + 2,
+  B_LFULL = B_ODONE + 2,
+  B_MDONE = B_LFULL + 2,
+  B_FIN = B_MDONE + 2,
   NBAR = B_FIN + 1
 };
 constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
@@ -63,7 +88,8 @@ constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
 constexpr uint32_t SM_END = SM_ABORT + 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;  // slack for 1024-byte alignment
 
-constexpr uint32_t IDESC_F8 = idesc(FMT_E4M3, FMT_E4M3, 128, 128);
+constexpr uint32_t IDESC_QK = idesc(FMT_E4M3, FMT_E4M3, 128, 128);
+constexpr uint32_t IDESC_PV = idesc(FMT_E4M3, FMT_E4M3, 128, 144);
 constexpr uint32_t IDESC_TF32 = idesc(FMT_TF32, FMT_TF32, 128, 128);
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s per wait
 
@@ -106,6 +132,47 @@ __device__ __forceinline__ void record_timeout(const Params& p, volatile int* ab
   atomicOr(p.err, ERR_TIMEOUT);
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// ExpCast of four scores sharing A' = A/256 and B' = (C - m)/256, packed into
+// one little-endian word of E4M3 bytes:
+//   t' = fma(x, A', B')              = t/256 exactly, t = fmaf(x, A, C - m);
+//   u  = sat(t' 2^29 + 1 - 7.5 2^21) = 1 iff t >= 7.5 (iff rint(t) >= 8),
+//        else 0 (t' 2^29 is an integer whenever t is near 7.5);
+//   f  = fma(t', u, 49152)           = 49152 + rint(t)/256 (ulp 2^-8, ties
+//        to even) or 49152 when u = 0, so the low byte of f's bits is the
+//        code.
+// The clip at 126 never binds: t <= C + tau8 <= 125.66 by construction.
+__device__ __forceinline__ uint32_t expcast4(float x0, float x1, float x2, float x3, float A,
+                                             float B) {
+  constexpr float S29 = 536870912.0f;  // 2^29
+  constexpr float K29 = -15728639.0f;  // 1 - 7.5 * 2^21
+  const float2 A2 = make_float2(A, A), B2 = make_float2(B, B);
+  const float2 t01 = __ffma2_rn(make_float2(x0, x1), A2, B2);
+  const float2 t23 = __ffma2_rn(make_float2(x2, x3), A2, B2);
+  const float2 u01 = make_float2(fma_sat(t01.x, S29, K29), fma_sat(t01.y, S29, K29));
+  const float2 u23 = make_float2(fma_sat(t23.x, S29, K29), fma_sat(t23.y, S29, K29));
+  const float2 M = make_float2(49152.0f, 49152.0f);
+  const float2 f01 = __ffma2_rn(t01, u01, M);
+  const float2 f23 = __ffma2_rn(t23, u23, M);
+  return prmt(prmt(__float_as_uint(f01.x), __float_as_uint(f01.y), 0x0040u),
+              prmt(__float_as_uint(f23.x), __float_as_uint(f23.y), 0x0040u), 0x5410u);
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ Params p) {
@@ -128,14 +195,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SFREE + s), 4);
+      mbar_init(bar(B_STAKEN + s), 4);
       mbar_init(bar(B_PFULL + s), 4);
       mbar_init(bar(B_ODONE + s), 1);
+      mbar_init(bar(B_LFULL + s), 4);
+      mbar_init(bar(B_MDONE + s), 1);
     }
     mbar_init(bar(B_FIN), 1);
     *abort = 0;
     mbar_fence_init();
   }
+  // Indicator rows 128..143 of every V stage (B operand rows of the PV MMA,
+  // 128B-swizzled K-major): row 128 = 1.0 on keys 0..63, row 129 = 1.0 on
+  // keys 64..127, rows 130..143 = 0.  TMA writes only rows 0..127.
+  for (int c = threadIdx.x; c < NS * 16 * 8; c += NTHREADS) {
+    const int st = c >> 7, n = (c >> 3) & 15, k = c & 7;  // stage, row, 16-key chunk
+    const uint32_t one4 = 0x38383838u;                    // four E4M3 1.0 bytes
+    const uint32_t v = ((n == 0 && k < 4) || (n == 1 && k >= 4)) ? one4 : 0u;
+    *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + TILE_BYTES + n * 128 + ((k ^ (n & 7)) * 16)) =
+        make_uint4(v, v, v, v);
+  }
+  fence_proxy_async_smem();
   if (warp == WARP_MMA) tmem_alloc(sb + SM_TSLOT, 512);
   tc_fence_before();
   __syncthreads();
@@ -143,8 +223,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TSLOT);
 
   // Number of KV tiles this CTA processes (the same in every role).
-  int ntiles = 0;
-  for (int t = 0; t < p.ntile; ++t) ntiles += tile_kept(p, bh, qt0, t) ? 1 : 0;
+  int ntiles = p.ntile;
+  if (p.mask) {
+    ntiles = 0;
+    for (int t = 0; t < p.ntile; ++t) ntiles += tile_kept(p, bh, qt0, t) ? 1 : 0;
+  }
 
   if (warp == WARP_TMA) {
     // ------------------------------------------------------------ producer
@@ -163,7 +246,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive_expect_tx(bar(B_KVFULL + st), 2 * TILE_BYTES + MU_BYTES);
         tma_load_3d(sb + SM_K + st * TILE_BYTES, &tmk, 0, t * TILE, static_cast<int>(bh),
                     bar(B_KVFULL + st));
-        tma_load_3d(sb + SM_V + st * TILE_BYTES, &tmv, t * TILE, 0, static_cast<int>(bh),
+        tma_load_3d(sb + SM_V + st * V_STAGE, &tmv, t * TILE, 0, static_cast<int>(bh),
                     bar(B_KVFULL + st));
         bulk_load(sb + SM_MU + st * MU_BYTES, p.vmu_op + (bh * p.ntile + t) * 1024, MU_BYTES,
                   bar(B_KVFULL + st));
@@ -174,42 +257,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ----------------------------------------------------------- MMA issue
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(bar(B_QFULL), 0, abort, WAIT_NS);
-      if (!ok) record_timeout(p, abort);
       tc_fence_after();
-      int i = 0;
-      for (int t = 0; t < p.ntile && ok; ++t) {
-        if (!tile_kept(p, bh, qt0, t)) continue;
-        const int st = i % NS;
-        if (!(ok = mbar_wait(bar(B_KVFULL + st), (i / NS) & 1, abort, WAIT_NS))) break;
+      auto next_tile = [&](int t) {
+        for (int u = t + 1; u < p.ntile; ++u)
+          if (tile_kept(p, bh, qt0, u)) return u;
+        return -1;
+      };
+      // Descriptors are built once; a byte offset o advances them by o >> 4
+      // in the start-address field (all of shared memory is below 256 KiB).
+      const uint64_t dQ = sdesc_sw128(sb + SM_Q), dK = sdesc_sw128(sb + SM_K);
+      const uint64_t dV = sdesc_sw128(sb + SM_V);
+      const uint64_t dL = sdesc_k8_tf32(sb + SM_L), dMu = sdesc_k8_tf32(sb + SM_MU);
+      auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+      auto qk = [&](int s, int st) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8(tmem + COL_S, adv(dQ, s * TILE_BYTES + 32 * kk), adv(dK, st * TILE_BYTES + 32 * kk),
+                 IDESC_QK, kk > 0);
+        mma_commit(bar(B_SFULL + s));
+      };
+      auto wt = [&](int b, uint32_t par) {
+        if (!ok) return;
+        ok = mbar_wait(bar(b), par, abort, WAIT_NS);
         tc_fence_after();
-        const uint32_t kb = sb + SM_K + st * TILE_BYTES;
-        const uint32_t vb = sb + SM_V + st * TILE_BYTES;
-        const uint32_t mb = sb + SM_MU + st * MU_BYTES;
+      };
+      int t = next_tile(-1);
+      wt(B_KVFULL + 0, 0);
+      if (ok) qk(0, 0);
+      wt(B_STAKEN + 0, 0);  // slot 0 has S(0) in registers: S is free
+      if (ok) qk(1, 0);
+      for (int i = 0; ok && t >= 0; ++i) {
+        const int st = i % NS;
+        const int tn = next_tile(t);
+        const int stn = (i + 1) % NS;
         for (int s = 0; s < 2 && ok; ++s) {
-          if (i > 0 && !(ok = mbar_wait(bar(B_SFREE + s), (i - 1) & 1, abort, WAIT_NS))) break;
-          tc_fence_after();
-          const uint32_t qb = sb + SM_Q + s * TILE_BYTES;
+          const uint32_t dO = tmem + COL_O + 160 * s;
+          wt(B_PFULL + s, i & 1);
+          if (!ok) break;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8(tmem + 128 * s, sdesc_sw128(qb + 32 * kk), sdesc_sw128(kb + 32 * kk), IDESC_F8,
-                   kk > 0);
-          mma_commit(bar(B_SFULL + s));
-        }
-        for (int s = 0; s < 2 && ok; ++s) {
-          if (!(ok = mbar_wait(bar(B_PFULL + s), i & 1, abort, WAIT_NS))) break;
-          tc_fence_after();
-          const uint32_t pb = sb + SM_P + s * TILE_BYTES;
-          const uint32_t dO = tmem + 256 + 128 * s;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8(dO, sdesc_sw128(pb + 32 * kk), sdesc_sw128(vb + 32 * kk), IDESC_F8,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-          mma_tf32(dO, sdesc_k8_tf32(sb + SM_L + s * MU_BYTES), sdesc_k8_tf32(mb), IDESC_TF32, 1);
+            mma_f8_tmem_a(dO, tmem + COL_P + 32 * s + 8 * kk, adv(dV, st * V_STAGE + 32 * kk), IDESC_PV,
+                          (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(B_ODONE + s));
+          if (tn >= 0) {
+            // S is free once the other slot holds its S(t) (slot 0) or slot 0
+            // holds S(t+1) (slot 1).
+            wt(s == 0 ? B_STAKEN + 1 : B_STAKEN + 0, s == 0 ? (i & 1) : ((i + 1) & 1));
+            if (s == 0) wt(B_KVFULL + stn, ((i + 1) / NS) & 1);
+            if (!ok) break;
+            qk(s, stn);
+          }
+          // The softmax has read and cleared the row sums and written the
+          // mean operand: restore the block means of tile t.
+          wt(B_LFULL + s, i & 1);
+          if (!ok) break;
+          mma_tf32(dO, adv(dL, s * MU_BYTES), adv(dMu, st * MU_BYTES), IDESC_TF32, 1);
+          mma_commit(bar(B_MDONE + s));
         }
         if (!ok) break;
-        mma_commit(bar(B_KVEMPTY + st));
-        ++i;
+        mma_commit(bar(B_KVEMPTY + st));  // tile t fully consumed
+        t = tn;
       }
       if (!ok) record_timeout(p, abort);
       // Drain: every issued MMA has completed before TMEM is released.
@@ -225,36 +332,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool row_ok = row < p.N;
     const int qt = static_cast<int>(row >> 6);
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + 128 * slot;
-    const uint32_t tO = tmem + lane_addr + 256 + 128 * slot;
+    const uint32_t tS = tmem + lane_addr + COL_S;
+    const uint32_t tP = tmem + lane_addr + COL_P + 32 * slot;
+    const uint32_t tO = tmem + lane_addr + COL_O + 160 * slot;
     const float qsc = p.q_scale[bh * p.nbp + (qt < p.nbp ? qt : p.nbp - 1)];
     const float a_i = p.c0 * qsc;
     const uint8_t* mrow = (p.mask && qt < p.nq64) ? p.mask + (bh * p.nq64 + qt) * p.nbp : nullptr;
-    uint8_t* Prow = sm + SM_P + slot * TILE_BYTES + r * 128;
     uint8_t* Lrow = sm + SM_L + slot * MU_BYTES + (r >> 3) * 256 + (r & 7) * 16;
-    float m_run = -__int_as_float(0x7f800000);
+    const float* ksc = p.k_scale + bh * p.nbp;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    float m_run = NEG_INF;
     float l = 0.0f;
     bool ok = true;
     int i = 0;
     for (int t = 0; t < p.ntile; ++t) {
-      if (!tile_kept(p, bh, qt0, t)) continue;
+      if (p.mask && !tile_kept(p, bh, qt0, t)) continue;
       bool keep0 = row_ok, keep1 = row_ok;
       if (p.mask) {
         keep0 = keep0 && mrow && mrow[2 * t] != 0;
         keep1 = keep1 && mrow && mrow[2 * t + 1] != 0;
       }
       const int64_t kv_lim = p.N - static_cast<int64_t>(t) * TILE;  // valid keys in the tile
-      const float A0 = a_i * p.k_scale[bh * p.nbp + 2 * t];
-      const float A1 = a_i * p.k_scale[bh * p.nbp + 2 * t + 1];
+      const float2 ks = *reinterpret_cast<const float2*>(ksc + 2 * t);
+      const float A0 = a_i * ks.x;
+      const float A1 = a_i * ks.y;
+      // Warp-uniform: does any lane need per-key masking in this tile?
+      const bool full = keep0 && keep1 && kv_lim >= TILE;
+      const bool masked = !__all_sync(0xffffffffu, full);
 
       if (!(ok = mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS))) break;
       tc_fence_after();
-      uint32_t xr[128];
+      float x[128];
       {
-        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[0]);
-        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[32]);
-        uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[64]);
-        uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&xr[96]);
+        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
+        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
+        uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
+        uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
         tmem_ld32(tS + 0, c0);
         tmem_ld32(tS + 32, c1);
         tmem_ld32(tS + 64, c2);
@@ -263,56 +376,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SFREE + slot));
-
-      const float NEG_INF = -__int_as_float(0x7f800000);
-      float x[128];
+      if (lane == 0) mbar_arrive(bar(B_STAKEN + slot));  // S may be overwritten
+      if (masked) {
+        // masked keys and keys past N never contribute: -inf for the max
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        const bool valid = (j < 64 ? keep0 : keep1) && j < kv_lim;
-        x[j] = valid ? __uint_as_float(xr[j]) : NEG_INF;
+        for (int j = 0; j < 128; ++j) {
+          const bool valid = (j < 64 ? keep0 : keep1) && j < kv_lim;
+          x[j] = valid ? x[j] : NEG_INF;
+        }
       }
-      float mx0 = NEG_INF, mx1 = NEG_INF;
+      // four independent max chains (two per 64-key half)
+      float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
+      float mc = fmax3(x[64], x[65], x[66]), md = fmax3(x[96], x[97], x[98]);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) mx0 = fmaxf(mx0, x[j]);
-#pragma unroll
-      for (int j = 64; j < 128; ++j) mx1 = fmaxf(mx1, x[j]);
+      for (int j = 3; j < 31; j += 2) {
+        ma = fmax3(ma, x[j], x[j + 1]);
+        mb = fmax3(mb, x[32 + j], x[33 + j]);
+        mc = fmax3(mc, x[64 + j], x[65 + j]);
+        md = fmax3(md, x[96 + j], x[97 + j]);
+      }
+      const float mx0 = fmax3(ma, mb, fmaxf(x[31], x[63]));
+      const float mx1 = fmax3(mc, md, fmaxf(x[95], x[127]));
       const float m_tile = fmaxf(A0 * mx0, A1 * mx1);
       const bool need = m_tile > m_run + p.tau8;
       const float m_new = need ? m_tile : m_run;
       const bool live = m_new != NEG_INF;
-      const float B = p.C - m_new;
-
-      // ExpCast: byte = clip(rint(fmaf(x, A, C - m))); codes below 8 -> 0.
-      uint32_t w[32];
-      float l0 = 0.0f, l1 = 0.0f;
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * q + e;
-          const float A = j < 64 ? A0 : A1;
-          float tt = fmaxf(__fmaf_rn(x[j], A, B), 0.0f);
-          const int k = __float_as_int(__fadd_rn(tt, 12582912.0f)) - 0x4B400000;  // rint(tt)
-          int code = k < 8 ? 0 : (k > 126 ? 126 : k);
-          code = live ? code : 0;
-          const float dec = code ? __int_as_float((code << 20) + 0x3C000000) : 0.0f;
-          if (j < 64) l0 += dec; else l1 += dec;
-          word |= static_cast<uint32_t>(code) << (8 * e);
-        }
-        w[q] = word;
-      }
-
-      // O and the P / L buffers are free once the previous PV has completed.
-      if (i > 0) {
-        if (!(ok = mbar_wait(bar(B_ODONE + slot), (i - 1) & 1, abort, WAIT_NS))) break;
-        tc_fence_after();
-      }
       const bool resc = need && m_run != NEG_INF;
-      float alpha = 1.0f;
-      if (resc) alpha = exp2f((m_run - m_new) * 0.125f);
+      const float alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
+      m_run = m_new;
+
+      // ExpCast -> 32 words of E4M3 bytes.  In a masked tile the -inf scores
+      // are replaced by 0 (keeping the cast finite) and the bytes of masked
+      // keys, or of a row with no key kept so far, are cleared afterwards.
+      if (masked) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
+      }
+      const float Bq = live ? (p.C - m_new) * 0.00390625f : 0.0f;
+      const float A0q = A0 * 0.00390625f, A1q = A1 * 0.00390625f;
+      // Bytes of masked keys (or of a row with no key kept so far) are
+      // cleared after the cast.
+      const int64_t lim0 = !masked ? 64 : (live && keep0) ? (kv_lim < 64 ? kv_lim : 64) : 0;
+      const int64_t lim1 = !masked ? 128 : (live && keep1) ? (kv_lim < 128 ? kv_lim : 128) : 64;
+      uint32_t w[32];  // the row's 128 E4M3 bytes
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q, Bq);
+      if (masked) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          uint32_t keep = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (4 * q + e < (q < 16 ? lim0 : lim1)) keep |= 0xFFu << (8 * e);
+          w[q] &= keep;
+        }
+      }
+      tmem_st32(tP, w);  // row r of P_s: 128 bytes in 32 columns
+      // Rescale O (PV(t-1) done; MEAN(t-1) waited for above; PV(t) is issued
+      // only after p_full below).
       if (i > 0 && __any_sync(0xffffffffu, resc)) {
+        // O must hold MEAN(t-1) before it is scaled
+        if (!(ok = mbar_wait(bar(B_MDONE + slot), (i - 1) & 1, abort, WAIT_NS))) break;
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -322,28 +448,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(tO + 32 * c, o);
         }
-        tmem_wait_st();
       }
-      l = l * alpha + (l0 + l1);
-      m_run = m_new;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
 
-      // P row: 128 bytes in the 128B-swizzled K-major layout.
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int pc = c ^ (r & 7);
-        *reinterpret_cast<uint4*>(Prow + 16 * pc) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-      }
-      // Row sums as the tf32 A operand: [hi0, lo0, hi0, hi1 | lo1, hi1, 0, 0].
+      // Row sums of the decoded bytes (columns 128, 129 of the PV result),
+      // the running l, and the tf32 A operand of the mean restoration:
+      // [hi0, lo0, hi0, hi1 | lo1, hi1, 0, 0].  The two columns are cleared
+      // so that the next PV accumulates the next tile's sums alone.
+      if (!(ok = mbar_wait(bar(B_ODONE + slot), i & 1, abort, WAIT_NS))) break;
+      tc_fence_after();
+      uint32_t ls0, ls1;
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                   : "=r"(ls0), "=r"(ls1)
+                   : "r"(tO + COL_L));
+      tmem_wait_ld();
+      asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tO + COL_L), "r"(0u),
+                   "r"(0u)
+                   : "memory");
+      const float l0 = __uint_as_float(ls0), l1 = __uint_as_float(ls1);
+      l = l * alpha + (l0 + l1);
       {
         const float h0 = to_tf32(l0), h1 = to_tf32(l1);
         const float g0 = to_tf32(l0 - h0), g1 = to_tf32(l1 - h1);
         *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, h1);
         *reinterpret_cast<float4*>(Lrow + 128) = make_float4(g1, h1, 0.0f, 0.0f);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
+      if (lane == 0) mbar_arrive(bar(B_LFULL + slot));
       ++i;
     }
     if (!ok) record_timeout(p, abort);
@@ -351,13 +488,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------ epilogue
     bool have = ok && ntiles > 0;
     if (have) {
-      if (!mbar_wait(bar(B_ODONE + slot), (ntiles - 1) & 1, abort, WAIT_NS)) {
+      // the last mean restoration
+      if (!mbar_wait(bar(B_MDONE + slot), (ntiles - 1) & 1, abort, WAIT_NS)) {
         record_timeout(p, abort);
         have = false;
       }
       tc_fence_after();
     }
-    if (__any_sync(0xffffffffu, have) && __all_sync(0xffffffffu, have)) {
+    if (__all_sync(0xffffffffu, have)) {
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {

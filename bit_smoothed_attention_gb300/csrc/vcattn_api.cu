@@ -192,7 +192,7 @@ vcattn_status vcattn_attn_ex(const vcattn_shape* s, const vcattn_prepped* in, fl
 
 vcattn_status vcattn_attn(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
                           const uint8_t* tile_mask, void* O, float* lse2, void* stream) {
-  return vcattn_attn_ex(s, in, sm_scale, 8, 0.0f, 0, tile_mask, O, lse2, stream);
+  return vcattn_attn_ex(s, in, sm_scale, 8, 6.0f, 0, tile_mask, O, lse2, stream);
 }
 
 size_t vcattn_fwd_workspace_bytes(const vcattn_shape* s) {

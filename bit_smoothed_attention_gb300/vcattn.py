@@ -188,7 +188,7 @@ def prep(Q, K, V, perm=None, out=None, stream=None):
     return pp
 
 
-def attn(pp, sm_scale, mask=None, off=8, tau8=0.0, out_f32=False, O=None, lse2=None, want_lse=True,
+def attn(pp, sm_scale, mask=None, off=8, tau8=6.0, out_f32=False, O=None, lse2=None, want_lse=True,
          stream=None):
     """Attention forward from prepped tensors.  Returns (O [B,H,N,128] bf16, or f32 with
     out_f32, and lse2 f32 [B,H,N])."""

@@ -170,10 +170,13 @@ vcattn_status vcattn_prep_noalloc(const vcattn_shape* shape, const void* Q, cons
  *             lse2 = -inf
  *   O         bf16 [B,H,N,D] (device) out
  *   lse2      f32 [B,H,N] (device) out, nullable
- * vcattn_attn uses off = 8, tau8 = 0 and writes bf16 O; vcattn_attn_ex takes
- * off and tau8 (0 <= off <= 8, 0 <= tau8 <= 8*(8.75 - off) so codes stay
- * <= 126) and, with out_f32 = 1, writes O as f32 [B,H,N,D] instead of bf16
- * (the value before the final bf16 rounding). */
+ * vcattn_attn uses off = 8, tau8 = 6 (the largest lazy-rescale threshold that
+ * keeps every code <= 126 at off = 8: the running max, and with it O and l,
+ * is rescaled only when a tile raises it by more than 6 code units = 0.75 in
+ * log2 units) and writes bf16 O; vcattn_attn_ex takes off and tau8
+ * (0 <= off <= 8, 0 <= tau8 <= 8*(8.75 - off); tau8 = 0 is the exact running
+ * max) and, with out_f32 = 1, writes O as f32 [B,H,N,D] instead of bf16 (the
+ * value before the final bf16 rounding). */
 vcattn_status vcattn_attn(const vcattn_shape* shape, const vcattn_prepped* in, float sm_scale,
                           const uint8_t* tile_mask, void* O, float* lse2, void* stream);
 vcattn_status vcattn_attn_ex(const vcattn_shape* shape, const vcattn_prepped* in, float sm_scale,

@@ -24,6 +24,7 @@ SM = float(np.float32(1 / math.sqrt(128)))
 REL_EMUL, ABS_EMUL = 2e-3, 4e-3
 REL_DENSE, COS_DENSE = 0.05, 0.998
 LSE_EMUL = 1e-3
+TAU8 = 6.0   # the library's default lazy-rescale threshold (code units)
 
 
 @pytest.fixture(scope="module")
@@ -131,7 +132,7 @@ def test_prep_identity_perm_and_zero_blocks(vc, orc):
 
 
 # --------------------------------------------------------------- attention
-def _attn_case(vc, orc, N, H, k, seed, mask=None, tau8=0.0, qidx=None):
+def _attn_case(vc, orc, N, H, k, seed, mask=None, tau8=TAU8, qidx=None):
     Q, K, V = _inputs(1, H, N, k, seed)
     labels, perm = vc.group(V, k, 5)
     pp = vc.prep(Q, K, V, perm)
@@ -178,8 +179,10 @@ def test_attn_dense_parity(vc, orc, N, H, k):
     _check_attn(_attn_case(vc, orc, N, H, k, 300 + N))
 
 
-def test_attn_lazy_rescale_parity(vc, orc):
-    _check_attn(_attn_case(vc, orc, 900, 1, 8, 401, tau8=4.0))
+@pytest.mark.parametrize("tau8", [0.0, 4.0])
+def test_attn_rescale_threshold_parity(vc, orc, tau8):
+    """tau8 = 0 is the exact running max; other thresholds rescale lazily."""
+    _check_attn(_attn_case(vc, orc, 900, 1, 8, 401, tau8=tau8))
 
 
 def test_attn_mask_parity(vc, orc):
@@ -217,7 +220,7 @@ def test_live_workload_sampled(vc, orc):
     Q, K, V = W.make_workload(w, device="cuda")
     labels, perm = vc.group(V, w.k, w.iters)
     pp = vc.prep(Q, K, V, perm)
-    O32, L = vc.attn(pp, w.sm_scale, out_f32=True)
+    O32, L = vc.attn(pp, w.sm_scale, out_f32=True)   # library default tau8
     torch.cuda.synchronize()
     assert vc.last_device_error() == 0
     qidx = W.evenly_spaced_queries(w.N)
@@ -229,7 +232,7 @@ def test_live_workload_sampled(vc, orc):
         assert np.array_equal(perm[0, h].cpu().numpy(), op[0])
         for key in ("q8", "k8", "r8t", "q_scale", "k_scale", "v_scale", "v_mean"):
             assert np.array_equal(views[key][h].cpu().numpy(), opp[key][0]), key
-        Oe, Le = orc.attn_emul(opp, 0, w.N, float(np.float32(w.sm_scale)), qidx=qidx)
+        Oe, Le = orc.attn_emul(opp, 0, w.N, float(np.float32(w.sm_scale)), qidx=qidx, tau8=TAU8)
         Od, _ = orc.attn_dense(Qb[0], Kb[0], Vb[0], float(np.float32(w.sm_scale)), qidx=qidx)
         g = O32[0, h].cpu().numpy()[qidx]
         rel, mx, _ = _metrics(g, Oe)
