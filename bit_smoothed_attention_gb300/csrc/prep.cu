@@ -7,7 +7,7 @@
 //    quantised; the gather happens on the fly so the permuted bf16 tensors
 //    never make an HBM round trip.
 //
-// Thread mapping of the block kernels (256 threads, one 64-token block):
+// Thread mapping of the block kernels (256 threads per 64-token block):
 // lane bits 0..3 pick a group of 4 consecutive tokens, lane bit 4 and the
 // warp pick a chunk of 8 channels; each thread loads 4 x 16 bytes.  Block
 // sums are the adjacent-pairing tree: the 4 tokens of a thread first, then a
@@ -64,21 +64,42 @@ __device__ __forceinline__ Map thread_map() {
   return m;
 }
 
-// Load 4 rows x 8 channels; rows past N are zero.  `perm` maps a sorted
+// A block's 64 rows are staged in shared memory with cp.async (all loads in
+// flight at once): [64 rows][16 chunks of 16 bytes], the chunk index XOR-ed
+// with (row / 4) so that the compute mapping (lanes = 4-row groups) reads
+// without bank conflicts.  Rows past N are zero.  `perm` maps a sorted
 // position to its source token (nullptr = identity).
-__device__ __forceinline__ void load_block(const uint16_t* base, const int32_t* perm, int64_t r0,
-                                           int64_t N, int cc, float (&x)[4][8]) {
+constexpr int TILE_SMEM = BLK * D * 2;  // 16 KiB
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 256 + ((chunk ^ ((row >> 2) & 15)) * 16));
+}
+__device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, const int32_t* perm,
+                                           int64_t r0, int64_t N) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t r = r0 + i;
+  for (int u = 0; u < 4; ++u) {
+    const int piece = u * 256 + static_cast<int>(threadIdx.x);
+    const int row = piece >> 4, chunk = piece & 15;
+    const int64_t r = r0 + row;
+    uint8_t* dst = tile + swz(row, chunk);
     if (r < N) {
       const int64_t src = perm ? perm[r] : r;
-      unpack8(*reinterpret_cast<const uint4*>(base + src * D + 8 * cc), x[i]);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                   "l"(base + src * D + chunk * 8)
+                   : "memory");
     } else {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) x[i][c] = 0.0f;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
   }
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int PENDING>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
+}
+// The 4 rows x 8 channels of thread (g, cc) from a staged tile.
+__device__ __forceinline__ void read_rows(const uint8_t* tile, int g, int cc, float (&x)[4][8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack8(*reinterpret_cast<const uint4*>(tile + swz(4 * g + i, cc)), x[i]);
 }
 
 // Adjacent-pairing tree over the 64 tokens of the block (per channel).
@@ -111,45 +132,75 @@ __device__ __forceinline__ float block_max(float a, float* red) {
 }
 
 // Stats: K block sums (original order), mean of each permuted V block, and
-// the per-channel amax of the V residual.  grid (nb, BH), block 256.
+// the per-channel amax of the V residual.  Each CTA handles STATS_BPC
+// consecutive blocks; block b+1 is staged while block b is reduced, and the
+// residual amax is kept in registers until one atomicMax per channel at the
+// end (max is order-independent).  grid (ceil(nb / STATS_BPC), BH), block
+// 256, dynamic shared memory STATS_SMEM (two stages of K and V tiles).
+constexpr int STATS_BPC = 8;
+constexpr int STATS_SMEM = 2 * 2 * TILE_SMEM;
 __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K,
                                                   const uint16_t* __restrict__ V,
                                                   const int32_t* __restrict__ perm, int64_t N,
-                                                  int nbp, float* __restrict__ kbs,
+                                                  int nb, int nbp, float* __restrict__ kbs,
                                                   float* __restrict__ v_mean,
                                                   uint32_t* __restrict__ vamax) {
+  extern __shared__ __align__(128) uint8_t ssm[];
   const Map m = thread_map();
-  const int64_t b = blockIdx.x, bh = blockIdx.y;
-  const int64_t r0 = b * BLK + 4 * m.g;
+  const int64_t bh = blockIdx.y;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * STATS_BPC;
+  const int64_t b1 = b0 + STATS_BPC < nb ? b0 + STATS_BPC : nb;
   const int32_t* ph = perm ? perm + bh * N : nullptr;
-  float kx[4][8], vx[4][8];
-  load_block(K + bh * N * D, nullptr, r0, N, m.cc, kx);
-  load_block(V + bh * N * D, ph, r0, N, m.cc, vx);
-  float ks[8], vs[8], mu[8];
-  block_tree(kx, ks);
-  block_tree(vx, vs);
-  const int64_t nvalid = N - b * BLK < BLK ? N - b * BLK : BLK;
-  const float fn = static_cast<float>(nvalid);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) mu[c] = vs[c] / fn;
+  const uint16_t* Kh = K + bh * N * D;
+  const uint16_t* Vh = V + bh * N * D;
+  auto stage = [&](int64_t b, int buf) {
+    stage_rows(ssm + buf * 2 * TILE_SMEM, Kh, nullptr, b * BLK, N);
+    stage_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, Vh, ph, b * BLK, N);
+    cp_commit();
+  };
+  stage(b0, 0);
   float am[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    float a = 0.0f;
+  for (int c = 0; c < 8; ++c) am[c] = 0.0f;
+  for (int64_t b = b0; b < b1; ++b) {
+    const int buf = static_cast<int>((b - b0) & 1);
+    if (b + 1 < b1) {
+      stage(b + 1, buf ^ 1);
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    const int64_t r0 = b * BLK + 4 * m.g;
+    float kx[4][8], vx[4][8];
+    read_rows(ssm + buf * 2 * TILE_SMEM, m.g, m.cc, kx);
+    read_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, m.g, m.cc, vx);
+    float ks[8], vs[8], mu[8];
+    block_tree(kx, ks);
+    block_tree(vx, vs);
+    const int64_t nvalid = N - b * BLK < BLK ? N - b * BLK : BLK;
+    const float fn = static_cast<float>(nvalid);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (r0 + i < N) a = fmaxf(a, fabsf(vx[i][c] - mu[c]));
-    am[c] = max16(a);
+    for (int c = 0; c < 8; ++c) mu[c] = vs[c] / fn;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (r0 + i < N) am[c] = fmaxf(am[c], fabsf(vx[i][c] - mu[c]));
+    if (m.g == 0) {
+      const int64_t o = (bh * nbp + b) * D + 8 * m.cc;
+      *reinterpret_cast<float4*>(kbs + o) = make_float4(ks[0], ks[1], ks[2], ks[3]);
+      *reinterpret_cast<float4*>(kbs + o + 4) = make_float4(ks[4], ks[5], ks[6], ks[7]);
+      *reinterpret_cast<float4*>(v_mean + o) = make_float4(mu[0], mu[1], mu[2], mu[3]);
+      *reinterpret_cast<float4*>(v_mean + o + 4) = make_float4(mu[4], mu[5], mu[6], mu[7]);
+    }
+    __syncthreads();  // this stage may be restaged next iteration
   }
-  if (m.g == 0) {
-    const int64_t o = (bh * nbp + b) * D + 8 * m.cc;
-    *reinterpret_cast<float4*>(kbs + o) = make_float4(ks[0], ks[1], ks[2], ks[3]);
-    *reinterpret_cast<float4*>(kbs + o + 4) = make_float4(ks[4], ks[5], ks[6], ks[7]);
-    *reinterpret_cast<float4*>(v_mean + o) = make_float4(mu[0], mu[1], mu[2], mu[3]);
-    *reinterpret_cast<float4*>(v_mean + o + 4) = make_float4(mu[4], mu[5], mu[6], mu[7]);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) am[c] = max16(am[c]);
+  if (m.g == 0)
 #pragma unroll
     for (int c = 0; c < 8; ++c) atomicMax(vamax + bh * D + 8 * m.cc + c, __float_as_uint(am[c]));
-  }
 }
 
 // mu_K = (adjacent-pairing tree over the block sums, padded with +0 to a
@@ -174,7 +225,13 @@ __global__ void __launch_bounds__(D) prep_kmean(const float* __restrict__ kbs,
   v_scale[bh * D + d] = a >= AMAX_FLOOR ? a / 448.0f : 1.0f;
 }
 
-// Quantisers.  grid (nbp, BH), block 256.
+// Quantisers.  Each CTA handles QUANT_BPC consecutive blocks; the next
+// block's Q, K (gathered) and V (gathered) rows are staged while the current
+// one is quantised.  grid (ceil(nbp / QUANT_BPC), BH), block 256, dynamic
+// shared memory QUANT_SMEM: two stages of the three tiles, the transposed
+// residual bytes and small reduction buffers.
+constexpr int QUANT_BPC = 4;
+constexpr int QUANT_SMEM = 2 * 3 * TILE_SMEM + D * (BLK + 16) + D * 4 + 64;
 __global__ void __launch_bounds__(256) prep_quant(
     const uint16_t* __restrict__ Q, const uint16_t* __restrict__ K, const uint16_t* __restrict__ V,
     const int32_t* __restrict__ perm, int64_t N, int64_t Npad, int nbp,
@@ -182,127 +239,163 @@ __global__ void __launch_bounds__(256) prep_quant(
     const float* __restrict__ v_scale, float* __restrict__ v_mean, uint8_t* __restrict__ q8,
     uint8_t* __restrict__ k8, uint8_t* __restrict__ r8t, float* __restrict__ q_scale,
     float* __restrict__ k_scale, float* __restrict__ qmu, float* __restrict__ vmu_op) {
-  __shared__ float qs[BLK][D + 1];
-  __shared__ float kmu[D];
-  __shared__ __align__(16) uint8_t tb[D][BLK + 16];
-  __shared__ float red[8];
+  extern __shared__ __align__(128) uint8_t qsm[];
+  uint8_t (*tb)[BLK + 16] = reinterpret_cast<uint8_t (*)[BLK + 16]>(qsm + 6 * TILE_SMEM);
+  float* kmu = reinterpret_cast<float*>(qsm + 6 * TILE_SMEM + D * (BLK + 16));
+  float* red = kmu + D;
   const Map m = thread_map();
-  const int64_t b = blockIdx.x, bh = blockIdx.y;
-  const int64_t r0 = b * BLK + 4 * m.g;
+  const int64_t bh = blockIdx.y;
   const int64_t nb = ceil_div(N, BLK);
-  const bool pad_block = b >= nb;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * QUANT_BPC;
+  const int64_t b1 = b0 + QUANT_BPC < nbp ? b0 + QUANT_BPC : nbp;
   const int32_t* ph = perm ? perm + bh * N : nullptr;
+  auto stage = [&](int64_t b, int buf) {
+    uint8_t* t = qsm + buf * 3 * TILE_SMEM;
+    stage_rows(t, Q + bh * N * D, nullptr, b * BLK, N);
+    stage_rows(t + TILE_SMEM, K + bh * N * D, ph, b * BLK, N);
+    stage_rows(t + 2 * TILE_SMEM, V + bh * N * D, ph, b * BLK, N);
+    cp_commit();
+  };
+  stage(b0, 0);
   if (threadIdx.x < D) kmu[threadIdx.x] = k_mean[bh * D + threadIdx.x];
-
-  // ---- Q: per 64-query block, original order ----
-  float x[4][8];
-  load_block(Q + bh * N * D, nullptr, r0, N, m.cc, x);
-  float a = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      a = fmaxf(a, fabsf(x[i][c]));
-      qs[4 * m.g + i][8 * m.cc + c] = x[i][c];
-    }
-  float amax = block_max(a, red);  // contains a __syncthreads (qs, kmu visible)
-  bool live = amax >= AMAX_FLOOR;
-  float inv = live ? 448.0f / amax : 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float y[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) y[c] = (live && r0 + i < N) ? x[i][c] * inv : 0.0f;
-    *reinterpret_cast<uint2*>(q8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
-  }
-  if (threadIdx.x == 0) q_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
-  if (threadIdx.x < BLK) {
-    const int64_t r = b * BLK + threadIdx.x;
-    if (r < N) {
-      float acc = 0.0f;
-      for (int d = 0; d < D; ++d) acc = __fmaf_rn(qs[threadIdx.x][d], kmu[d], acc);
-      qmu[bh * N + r] = acc;
-    }
-  }
-
-  // ---- K: gathered, centred, per 64-key block ----
-  load_block(K + bh * N * D, ph, r0, N, m.cc, x);
-  a = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      x[i][c] = (r0 + i < N) ? x[i][c] - kmu[8 * m.cc + c] : 0.0f;
-      a = fmaxf(a, fabsf(x[i][c]));
-    }
-  amax = block_max(a, red);
-  live = amax >= AMAX_FLOOR;
-  inv = live ? 448.0f / amax : 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float y[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) y[c] = live ? x[i][c] * inv : 0.0f;
-    *reinterpret_cast<uint2*>(k8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
-  }
-  if (threadIdx.x == 0) k_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
-
-  // ---- V: gathered, block-demeaned residual, per-channel scale, transposed ----
-  load_block(V + bh * N * D, ph, r0, N, m.cc, x);
-  const int64_t mo = (bh * nbp + b) * D + 8 * m.cc;
-  float mu[8], vinv[8];
+  // per-channel inverse scales of the V residual (the same for every block)
+  float vinv[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    mu[c] = pad_block ? 0.0f : v_mean[mo + c];
     const float am = __uint_as_float(vamax[bh * D + 8 * m.cc + c]);
     vinv[c] = am >= AMAX_FLOOR ? 448.0f / am : 0.0f;
   }
+
+  for (int64_t b = b0; b < b1; ++b) {
+    const int buf = static_cast<int>((b - b0) & 1);
+    if (b + 1 < b1) {
+      stage(b + 1, buf ^ 1);
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    const uint8_t* tq = qsm + buf * 3 * TILE_SMEM;
+    const uint8_t* tk = tq + TILE_SMEM;
+    const uint8_t* tv = tq + 2 * TILE_SMEM;
+    const int64_t r0 = b * BLK + 4 * m.g;
+    const bool pad_block = b >= nb;
+
+    // ---- Q: per 64-query block, original order ----
+    float x[4][8];
+    read_rows(tq, m.g, m.cc, x);
+    float a = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float y[8];
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int c = 0; c < 8; ++c) y[c] = (r0 + i < N) ? (x[i][c] - mu[c]) * vinv[c] : 0.0f;
-    const uint2 by = e4m3x8(y);
+      for (int c = 0; c < 8; ++c) a = fmaxf(a, fabsf(x[i][c]));
+    float amax = block_max(a, red);
+    bool live = amax >= AMAX_FLOOR;
+    float inv = live ? 448.0f / amax : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float y[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) y[c] = (live && r0 + i < N) ? x[i][c] * inv : 0.0f;
+      *reinterpret_cast<uint2*>(q8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
+    }
+    if (threadIdx.x == 0) q_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
+    if (threadIdx.x < BLK) {
+      // qmu = q . mu_K: one fmaf chain over d ascending
+      const int rr = threadIdx.x;
+      const int64_t r = b * BLK + rr;
+      if (r < N) {
+        float acc = 0.0f;
+        for (int cc = 0; cc < 16; ++cc) {
+          float qv[8];
+          unpack8(*reinterpret_cast<const uint4*>(tq + swz(rr, cc)), qv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = __fmaf_rn(qv[e], kmu[8 * cc + e], acc);
+        }
+        qmu[bh * N + r] = acc;
+      }
+    }
+
+    // ---- K: gathered, centred, per 64-key block ----
+    read_rows(tk, m.g, m.cc, x);
+    a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        x[i][c] = (r0 + i < N) ? x[i][c] - kmu[8 * m.cc + c] : 0.0f;
+        a = fmaxf(a, fabsf(x[i][c]));
+      }
+    amax = block_max(a, red);
+    live = amax >= AMAX_FLOOR;
+    inv = live ? 448.0f / amax : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float y[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) y[c] = live ? x[i][c] * inv : 0.0f;
+      *reinterpret_cast<uint2*>(k8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
+    }
+    if (threadIdx.x == 0) k_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
+
+    // ---- V: gathered, block-demeaned residual, per-channel scale, transposed ----
+    read_rows(tv, m.g, m.cc, x);
+    const int64_t mo = (bh * nbp + b) * D + 8 * m.cc;
+    float mu[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) mu[c] = pad_block ? 0.0f : v_mean[mo + c];
+    uint2 by[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float y[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) y[c] = (r0 + i < N) ? (x[i][c] - mu[c]) * vinv[c] : 0.0f;
+      by[i] = e4m3x8(y);
+    }
+    // channel c's bytes of the thread's 4 rows -> one 32-bit word of tb[d][4g..4g+3]
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint32_t w = c < 4 ? by.x : by.y;
-      tb[8 * m.cc + c][4 * m.g + i] = static_cast<uint8_t>(w >> (8 * (c & 3)));
+      const uint32_t sel = static_cast<uint32_t>((c & 3) | ((4 + (c & 3)) << 4));
+      const uint32_t w01 = c < 4 ? __byte_perm(by[0].x, by[1].x, sel) : __byte_perm(by[0].y, by[1].y, sel);
+      const uint32_t w23 = c < 4 ? __byte_perm(by[2].x, by[3].x, sel) : __byte_perm(by[2].y, by[3].y, sel);
+      *reinterpret_cast<uint32_t*>(&tb[8 * m.cc + c][4 * m.g]) = __byte_perm(w01, w23, 0x5410);
     }
-  }
-  if (pad_block && m.g == 0) {
-    *reinterpret_cast<float4*>(v_mean + mo) = make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4*>(v_mean + mo + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  __syncthreads();
-  {
-    const int d = threadIdx.x >> 1, h = threadIdx.x & 1;
-    const uint4* src = reinterpret_cast<const uint4*>(&tb[d][32 * h]);
-    uint4* dst = reinterpret_cast<uint4*>(r8t + (bh * D + d) * Npad + b * BLK + 32 * h);
-    dst[0] = src[0];
-    dst[1] = src[1];
-  }
-  // ---- mean operand of the rank-one restoration MMA ----
-  // B[k][n = d] of a [K = 8] x [N = 128] tf32 operand, K-major, no swizzle:
-  // k = 3h, 3h+1, 3h+2 hold (hi, hi, lo) of mu_b[d] / v_scale[d] for the
-  // block's half h of its 128-key tile; k = 6, 7 are zero.
-  if (threadIdx.x < D) {
-    const int d = threadIdx.x;
-    const float mud = pad_block ? 0.0f : v_mean[(bh * nbp + b) * D + d];
-    const float u = mud / v_scale[bh * D + d];
-    const float hi = to_tf32(u);
-    const float lo = to_tf32(u - hi);
-    const int h = static_cast<int>(b & 1);
-    float* tile = vmu_op + (bh * (Npad / TILE) + (b >> 1)) * 1024;
-    auto at = [&](int kk) -> float& {
-      return tile[((d >> 3) * 256 + (kk >> 2) * 128 + (d & 7) * 16 + (kk & 3) * 4) / 4];
-    };
-    at(3 * h) = hi;
-    at(3 * h + 1) = hi;
-    at(3 * h + 2) = lo;
-    if (h == 1) {
-      at(6) = 0.0f;
-      at(7) = 0.0f;
+    if (pad_block && m.g == 0) {
+      *reinterpret_cast<float4*>(v_mean + mo) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(v_mean + mo + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    __syncthreads();
+    {
+      const int d = threadIdx.x >> 1, h = threadIdx.x & 1;
+      const uint4* src = reinterpret_cast<const uint4*>(&tb[d][32 * h]);
+      uint4* dst = reinterpret_cast<uint4*>(r8t + (bh * D + d) * Npad + b * BLK + 32 * h);
+      dst[0] = src[0];
+      dst[1] = src[1];
+    }
+    // ---- mean operand of the rank-one restoration MMA ----
+    // B[k][n = d] of a [K = 8] x [N = 128] tf32 operand, K-major, no swizzle:
+    // k = 3h, 3h+1, 3h+2 hold (hi, hi, lo) of mu_b[d] / v_scale[d] for the
+    // block's half h of its 128-key tile; k = 6, 7 are zero.
+    if (threadIdx.x < D) {
+      const int d = threadIdx.x;
+      const float mud = pad_block ? 0.0f : v_mean[(bh * nbp + b) * D + d];
+      const float u = mud / v_scale[bh * D + d];
+      const float hi = to_tf32(u);
+      const float lo = to_tf32(u - hi);
+      const int h = static_cast<int>(b & 1);
+      float* tile = vmu_op + (bh * (Npad / TILE) + (b >> 1)) * 1024;
+      auto at = [&](int kk) -> float& {
+        return tile[((d >> 3) * 256 + (kk >> 2) * 128 + (d & 7) * 16 + (kk & 3) * 4) / 4];
+      };
+      at(3 * h) = hi;
+      at(3 * h + 1) = hi;
+      at(3 * h + 2) = lo;
+      if (h == 1) {
+        at(6) = 0.0f;
+        at(7) = 0.0f;
+      }
+    }
+    __syncthreads();  // tb and this stage are reused by the next block
   }
 }
 
@@ -330,11 +423,20 @@ cudaError_t launch_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   const int nb = static_cast<int>(ceil_div(N, BLK));
   cudaError_t e = cudaMemsetAsync(ws.vamax, 0, static_cast<size_t>(BH) * D * 4, s);
   if (e != cudaSuccess) return e;
-  prep_stats<<<dim3(nb, static_cast<unsigned>(BH)), 256, 0, s>>>(K, V, perm, N, nbp, ws.kbs,
-                                                                 o.v_mean, ws.vamax);
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(prep_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, STATS_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prep_quant, cudaFuncAttributeMaxDynamicSharedMemorySize, QUANT_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  prep_stats<<<dim3(static_cast<unsigned>(ceil_div(nb, STATS_BPC)), static_cast<unsigned>(BH)), 256,
+               STATS_SMEM, s>>>(K, V, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax);
   prep_kmean<<<static_cast<unsigned>(BH), D, 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp, o.k_mean,
                                                      o.v_scale);
-  prep_quant<<<dim3(nbp, static_cast<unsigned>(BH)), 256, 0, s>>>(
+  prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH)), 256,
+               QUANT_SMEM, s>>>(
       Q, K, V, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
       o.q_scale, o.k_scale, o.qmu, o.vmu_op);
   return cudaGetLastError();

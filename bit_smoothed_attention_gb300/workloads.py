@@ -48,6 +48,9 @@ WORKLOADS = {
     "tiny": Workload("tiny", 1, 2, 1024, 8, 8, seed=1000),
     "mid": Workload("mid", 1, 8, 8192, 32, 32, seed=1001),
     "live": Workload("live", 1, 56, 32626, 64, 64, seed=1002),
+    # 8 of the live workload's heads (inputs still larger than L2): the size
+    # the kernel profiles are captured at
+    "live_h8": Workload("live_h8", 1, 8, 32626, 64, 64, seed=1002),
     "schedule": Workload("schedule", 1, 40, 32760, 64, 64, steps=50, seed=1003),
     "sparse": Workload("sparse", 1, 56, 115328, 64, 64, sparse=True, seed=1004),
 }
