@@ -45,7 +45,8 @@ __global__ void km_init(const uint16_t* __restrict__ V, int64_t N, int k, float*
 
 // Assign: each thread scores TT tokens against all clusters, accumulators in
 // registers; centroids live in shared memory transposed [d][c] so one 16-byte
-// broadcast load feeds 4 x TT FMAs.  Clusters c >= k get h = +inf and never
+// broadcast load feeds 4 x TT FMAs (as packed fma.rn.f32x2 pairs, each two
+// IEEE fmafs).  Clusters c >= k get h = +inf and never
 // win.  grid (ceil(N / (256*TT)), BH), block 256.
 template <int KC, int TT>
 __global__ void __launch_bounds__(256) km_assign(const uint16_t* __restrict__ V, int64_t N, int k,
@@ -80,23 +81,28 @@ __global__ void __launch_bounds__(256) km_assign(const uint16_t* __restrict__ V,
     j[t] = static_cast<int64_t>(blockIdx.x) * (256 * TT) + t * 256 + threadIdx.x;
     ok[t] = j[t] < N;
   }
-  float acc[TT][KC];
+  // accumulators in cluster pairs: one packed fma.rn.f32x2 is two IEEE fmafs
+  float2 acc[TT][KC / 2];
 #pragma unroll
   for (int t = 0; t < TT; ++t)
 #pragma unroll
-    for (int c = 0; c < KC; ++c) acc[t][c] = 0.0f;
+    for (int c = 0; c < KC / 2; ++c) acc[t][c] = make_float2(0.0f, 0.0f);
 
+  // V is streamed 8 channels at a time; the next 8 are loaded while the
+  // current ones are used (software pipelining hides the load latency).
+  uint4 nxt[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+    nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D) : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
   for (int d0 = 0; d0 < D; d0 += 8) {
     float vv[TT][8];
 #pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      if (ok[t]) {
-        unpack8(*reinterpret_cast<const uint4*>(vb + j[t] * D + d0), vv[t]);
-      } else {
+    for (int t = 0; t < TT; ++t) unpack8(nxt[t], vv[t]);
+    if (d0 + 8 < D) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) vv[t][e] = 0.0f;
-      }
+      for (int t = 0; t < TT; ++t)
+        nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D + d0 + 8) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int dd = 0; dd < 8; ++dd) {
@@ -105,10 +111,9 @@ __global__ void __launch_bounds__(256) km_assign(const uint16_t* __restrict__ V,
         const float4 cc = *reinterpret_cast<const float4*>(&cT[d0 + dd][4 * c4]);
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
-          acc[t][4 * c4 + 0] = __fmaf_rn(vv[t][dd], cc.x, acc[t][4 * c4 + 0]);
-          acc[t][4 * c4 + 1] = __fmaf_rn(vv[t][dd], cc.y, acc[t][4 * c4 + 1]);
-          acc[t][4 * c4 + 2] = __fmaf_rn(vv[t][dd], cc.z, acc[t][4 * c4 + 2]);
-          acc[t][4 * c4 + 3] = __fmaf_rn(vv[t][dd], cc.w, acc[t][4 * c4 + 3]);
+          const float2 v2 = make_float2(vv[t][dd], vv[t][dd]);
+          acc[t][2 * c4] = __ffma2_rn(v2, make_float2(cc.x, cc.y), acc[t][2 * c4]);
+          acc[t][2 * c4 + 1] = __ffma2_rn(v2, make_float2(cc.z, cc.w), acc[t][2 * c4 + 1]);
         }
       }
     }
@@ -117,10 +122,10 @@ __global__ void __launch_bounds__(256) km_assign(const uint16_t* __restrict__ V,
   for (int t = 0; t < TT; ++t) {
     if (!ok[t]) continue;
     int best = 0;
-    float bs = acc[t][0] - hs[0];
+    float bs = acc[t][0].x - hs[0];
 #pragma unroll
     for (int c = 1; c < KC; ++c) {
-      const float sc = acc[t][c] - hs[c];
+      const float sc = ((c & 1) ? acc[t][c >> 1].y : acc[t][c >> 1].x) - hs[c];
       if (sc > bs) {
         bs = sc;
         best = c;
@@ -130,46 +135,151 @@ __global__ void __launch_bounds__(256) km_assign(const uint16_t* __restrict__ V,
   }
 }
 
-// Chunk partial sums: thread d owns channel d of every cluster's partial.
-// grid (nchunk, BH), block D.
+// Assign, split variant: a thread scores TT tokens against CH of the KC
+// clusters (KC/CH lanes share a token group), so one 16-byte centroid load
+// feeds 4 x TT FMAs with TT = 4.  The per-lane winners are combined with
+// shuffles: larger score wins, equal scores keep the lower cluster (the
+// lower lane), which is the lowest-index rule of the sequential scan.
+// grid (ceil(N / (256 / (KC/CH) * TT)), BH), block 256.
+template <int KC, int CH, int TT>
+__global__ void __launch_bounds__(256) km_assign_split(const uint16_t* __restrict__ V, int64_t N,
+                                                       int k, const float* __restrict__ cent,
+                                                       int32_t* __restrict__ labels) {
+  constexpr int LPG = KC / CH;          // lanes per token group
+  constexpr int GROUPS = 256 / LPG;     // token groups per CTA
+  __shared__ __align__(16) float cT[D][KC];
+  __shared__ float hs[KC];
+  const int64_t bh = blockIdx.y;
+  const float* cb = cent + bh * k * D;
+  for (int i = threadIdx.x; i < D * KC; i += blockDim.x) {
+    const int d = i / KC, c = i % KC;
+    cT[d][c] = c < k ? cb[c * D + d] : 0.0f;
+  }
+  __syncthreads();
+  if (threadIdx.x < KC) {
+    const int c = threadIdx.x;
+    if (c < k) {
+      float acc = 0.0f;
+      for (int d = 0; d < D; ++d) acc = __fmaf_rn(cT[d][c], cT[d][c], acc);
+      hs[c] = 0.5f * acc;
+    } else {
+      hs[c] = __int_as_float(0x7f800000);  // +inf
+    }
+  }
+  __syncthreads();
+  const int part = threadIdx.x % LPG;   // which CH clusters
+  const int grp = threadIdx.x / LPG;
+  const int c0 = part * CH;
+  const uint16_t* vb = V + bh * N * D;
+  int64_t j[TT];
+  bool ok[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    j[t] = static_cast<int64_t>(blockIdx.x) * (GROUPS * TT) + t * GROUPS + grp;
+    ok[t] = j[t] < N;
+  }
+  float2 acc[TT][CH / 2];  // cluster pairs (packed fma.rn.f32x2)
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int c = 0; c < CH / 2; ++c) acc[t][c] = make_float2(0.0f, 0.0f);
+  uint4 nxt[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+    nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D) : make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+  for (int d0 = 0; d0 < D; d0 += 8) {
+    float vv[TT][8];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) unpack8(nxt[t], vv[t]);
+    if (d0 + 8 < D) {
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+        nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D + d0 + 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int dd = 0; dd < 8; ++dd) {
+#pragma unroll
+      for (int c4 = 0; c4 < CH / 4; ++c4) {
+        const float4 cc = *reinterpret_cast<const float4*>(&cT[d0 + dd][c0 + 4 * c4]);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const float2 v2 = make_float2(vv[t][dd], vv[t][dd]);
+          acc[t][2 * c4] = __ffma2_rn(v2, make_float2(cc.x, cc.y), acc[t][2 * c4]);
+          acc[t][2 * c4 + 1] = __ffma2_rn(v2, make_float2(cc.z, cc.w), acc[t][2 * c4 + 1]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    int best = c0;
+    float bs = acc[t][0].x - hs[c0];
+#pragma unroll
+    for (int c = 1; c < CH; ++c) {
+      const float sc = ((c & 1) ? acc[t][c >> 1].y : acc[t][c >> 1].x) - hs[c0 + c];
+      if (sc > bs) {
+        bs = sc;
+        best = c0 + c;
+      }
+    }
+#pragma unroll
+    for (int m = 1; m < LPG; m <<= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, bs, m);
+      const int ob = __shfl_xor_sync(0xffffffffu, best, m);
+      if (os > bs || (os == bs && ob < best)) {
+        bs = os;
+        best = ob;
+      }
+    }
+    if (ok[t] && part == 0) labels[bh * N + j[t]] = best;
+  }
+}
+
+// Chunk partial sums: thread d owns channel d of every cluster's partial and
+// adds the chunk's tokens in order.  The V rows are staged through shared
+// memory 32 tokens at a time with coalesced 16-byte loads.  grid (nchunk,
+// BH), block D.
 __global__ void __launch_bounds__(D) km_partial(const uint16_t* __restrict__ V,
                                                 const int32_t* __restrict__ labels, int64_t N,
                                                 int k, int nchunk, float* __restrict__ part,
                                                 int32_t* __restrict__ cnt, uint32_t* err) {
+  constexpr int SEG = 32;  // tokens staged at a time
   __shared__ float ps[KMAX][D];
   __shared__ int cs[KMAX];
+  __shared__ __align__(16) uint16_t vs[SEG][D];
+  __shared__ int ls[SEG];
   const int64_t bh = blockIdx.y;
   const int g = blockIdx.x;
   const int d = threadIdx.x;
   for (int c = 0; c < k; ++c) ps[c][d] = 0.0f;
   if (d < KMAX) cs[d] = 0;
-  __syncthreads();
   const int64_t j0 = static_cast<int64_t>(g) * UPD_CHUNK;
   const int64_t j1 = j0 + UPD_CHUNK < N ? j0 + UPD_CHUNK : N;
   const uint16_t* vb = V + bh * N * D;
   const int32_t* lb = labels + bh * N;
   bool bad = false;
-  for (int64_t j = j0; j < j1; j += 8) {
-    int cl[8];
-    float vv[8];
+  for (int64_t s0 = j0; s0 < j1; s0 += SEG) {
+    const int n = static_cast<int>(j1 - s0 < SEG ? j1 - s0 : SEG);
+    __syncthreads();  // previous segment consumed
+    // 32 rows x 256 bytes = 512 16-byte pieces, 4 per thread
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (j + u < j1) {
-        cl[u] = lb[j + u];
-        vv[u] = bf16f(vb[(j + u) * D + d]);
-      }
+    for (int u = 0; u < 4; ++u) {
+      const int piece = u * D + d, row = piece >> 4, col = piece & 15;
+      if (row < n)
+        *reinterpret_cast<uint4*>(&vs[row][col * 8]) =
+            *reinterpret_cast<const uint4*>(vb + (s0 + row) * D + col * 8);
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (j + u < j1) {
-        const int c = cl[u];
-        if (static_cast<unsigned>(c) >= static_cast<unsigned>(k)) {
-          bad = true;
-          continue;
-        }
-        ps[c][d] = ps[c][d] + vv[u];
-        if (d == 0) cs[c] += 1;
+    if (d < SEG && d < n) ls[d] = lb[s0 + d];
+    __syncthreads();
+    for (int jj = 0; jj < n; ++jj) {
+      const int c = ls[jj];
+      if (static_cast<unsigned>(c) >= static_cast<unsigned>(k)) {
+        bad = true;
+        continue;
       }
+      ps[c][d] = ps[c][d] + bf16f(vs[jj][d]);
+      if (d == 0) cs[c] += 1;
     }
   }
   if (bad && d == 0) atomicOr(err, ERR_BAD_LABEL);
@@ -254,6 +364,15 @@ __global__ void __launch_bounds__(UPD_CHUNK) sort_scatter(const int32_t* __restr
   if (c >= 0) perm[bh * N + offs[(bh * nchunk + g) * k + c] + wc[warp][c] + rank] = static_cast<int32_t>(j);
 }
 
+template <int KC, int CH, int TT>
+cudaError_t assign_split(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
+                         int32_t* labels, cudaStream_t s) {
+  constexpr int GROUPS = 256 / (KC / CH);
+  const dim3 grid(static_cast<unsigned>(ceil_div(N, GROUPS * TT)), static_cast<unsigned>(BH));
+  km_assign_split<KC, CH, TT><<<grid, 256, 0, s>>>(V, N, k, cent, labels);
+  return cudaGetLastError();
+}
+
 template <int KC, int TT>
 cudaError_t assign(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
                    int32_t* labels, cudaStream_t s) {
@@ -294,7 +413,7 @@ cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int it
     if (k <= 8) e = assign<8, 8>(V, BH, N, k, cent, labels, s);
     else if (k <= 16) e = assign<16, 8>(V, BH, N, k, cent, labels, s);
     else if (k <= 32) e = assign<32, 4>(V, BH, N, k, cent, labels, s);
-    else e = assign<64, 2>(V, BH, N, k, cent, labels, s);
+    else e = assign_split<64, 32, 4>(V, BH, N, k, cent, labels, s);
     if (e != cudaSuccess) return e;
     km_partial<<<gchunk, D, 0, s>>>(V, labels, N, k, nchunk, ws.part, ws.cnt, err);
     km_finalize<<<dim3(k, static_cast<unsigned>(BH)), D, 0, s>>>(ws.part, ws.cnt, nchunk, k, cent);
