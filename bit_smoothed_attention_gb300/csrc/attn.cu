@@ -9,7 +9,7 @@
 //   the softmax warps turn S into E4M3 probability bytes with ExpCast
 //   (byte = rint(fmaf(x, A, C - m)), bytes below 8 flush to 0) on the FMA
 //   pipe: no exp2, no conversion instruction;
-//   the bytes P8 go back to TMEM and feed, as the A operand,
+//   the bytes P8 go to shared memory and feed, as the A operand,
 //   [O | l] += P8 [R8 ; 1_b0 ; 1_b1] (E4M3, N = 144): the 128 output
 //   channels plus the per-64-key-block row sums of the decoded bytes, from
 //   the same MMA;
@@ -21,21 +21,29 @@
 // CTA = 256 query rows (two 128-row slots) of one (b, h).  Warps 0-3 run the
 // softmax of slot 0 (thread = row = TMEM lane), warps 4-7 slot 1, warp 8
 // issues TMA loads, warp 9 allocates TMEM and issues every MMA from one lane.
-// TMEM columns: S [0,128) shared by the slots, P0 [128,160), P1 [160,192),
-// O0 [192,336), O1 [352,496); columns 128 and 129 of O_s hold the tile's row
-// sums, which the softmax reads and clears after each PV.
+// TMEM columns: S [0,128) shared by the slots, O0 [192,336), O1 [352,496);
+// columns 128 and 129 of O_s hold the tile's row sums, which the softmax
+// reads and clears after each PV.  P of each slot is a 128B-swizzled tile in
+// shared memory (an A operand read from shared memory issues faster than one
+// read from TMEM).  K tiles and V/mean tiles come through separate rings of
+// NS stages: a K stage is released once both slots' QK have read it, a V
+// stage only after both mean terms of its tile.
 //
-// Per KV tile t the MMA lane issues, slot 0 then slot 1,
-//   PV_s(t) | QK_s(t+1) | MEAN_s(t)
-// and the softmax of slot s does
-//   wait S(t), load it, release S -> max, ExpCast -> P(t), rescale O ->
-//   wait PV(t) -> read and clear the row sums, l += ..., write the mean
-//   operand.
-// The two slots overlap: while one computes, the tensor core runs the other
-// slot's MMAs, and QK(t+1) starts as soon as PV(t) is queued, in parallel
-// with the row-sum read-back.  tcgen05 operations of one thread complete in issue order,
-// so "PV(t+1) done" implies MEAN(t) done; a softmax that must rescale O waits
-// for MEAN(t) explicitly first.
+// S is a single TMEM buffer that the two slots take in turn (S0(t), S1(t),
+// S0(t+1), ...).  Per KV tile t the MMA lane issues
+//   QK_0(t+1) | MEAN_0(t-1) PV_0(t) | QK_1(t+1) | MEAN_1(t-1) PV_1(t)
+// each QK as soon as the other slot holds its S in registers, so the next S
+// is computed while the softmax of the current one runs, and the softmax of
+// slot s does
+//   wait S(t), load it, release S -> max -> ExpCast -> wait PV(t-1) ->
+//   P(t) to TMEM, read and clear the row sums of t-1, (rare) rescale O,
+//   write the mean operand of t-1 -> release P(t) and the mean operand.
+// The row sums of tile t-1 are read one tile late, so no softmax waits for
+// its own PV; when the running maximum moves at tile t, O (which then holds
+// PV up to t-1 and the mean terms up to t-2) is rescaled in place and the
+// mean operand of t-1 is written already multiplied by the factor.
+// tcgen05 operations of one thread complete in issue order, so "PV(t-1)
+// done" implies that MEAN(t-2) is done.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -50,14 +58,13 @@ namespace vc {
 namespace {
 
 constexpr int NS = 4;          // K/V/mean pipeline stages
-constexpr int NTHREADS = 320;  // 8 softmax warps + TMA warp + MMA warp
+constexpr int NTHREADS = 352;  // 8 softmax warps + TMA warp + one MMA warp per slot
 constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA = 9;    // + slot
 constexpr int CTA_ROWS = 256;
 
 // TMEM columns
 constexpr uint32_t COL_S = 0;
-constexpr uint32_t COL_P = 128;    // + 32 * slot
 constexpr uint32_t COL_O = 192;    // + 160 * slot; 144 columns each
 constexpr uint32_t COL_L = 128;    // row sums inside O_s
 
@@ -69,19 +76,20 @@ constexpr uint32_t SM_K = SM_Q + 2 * TILE_BYTES;
 constexpr uint32_t SM_V = SM_K + NS * TILE_BYTES;
 constexpr uint32_t SM_MU = SM_V + NS * V_STAGE;
 constexpr uint32_t SM_L = SM_MU + NS * MU_BYTES;
-constexpr uint32_t SM_BAR = SM_L + 2 * MU_BYTES;
+constexpr uint32_t SM_P = SM_L + 2 * MU_BYTES;  // P of each slot, A operand of the PV MMA
+constexpr uint32_t SM_BAR = SM_P + 2 * TILE_BYTES;
 enum {
   B_QFULL = 0,
-  B_KVFULL = 1,
-  B_KVEMPTY = B_KVFULL + NS,
-  B_SFULL = B_KVEMPTY + NS,
+  B_FULL = 1,  // V(j) and its mean tile in stage j % NS, plus K(j+1)
+  B_KEMPTY = B_FULL + NS,
+  B_VEMPTY = B_KEMPTY + NS,
+  B_SFULL = B_VEMPTY + NS,
   B_STAKEN = B_SFULL + 2,
-  B_PFULL = B_STAKEN + 2,
+  B_PFULL = B_STAKEN + 2,  // P(j) and the mean operand of tile j-1
   B_ODONE = B_PFULL + 2,
-  B_LFULL = B_ODONE + 2,
-  B_MDONE = B_LFULL + 2,
+  B_MDONE = B_ODONE + 2,
   B_FIN = B_MDONE + 2,
-  NBAR = B_FIN + 1
+  NBAR = B_FIN + 2
 };
 constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
 constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
@@ -190,18 +198,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar(B_KVFULL + s), 1);
-      mbar_init(bar(B_KVEMPTY + s), 1);
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 2);  // one release per slot's MMA lane
+      mbar_init(bar(B_VEMPTY + s), 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_STAKEN + s), 4);
       mbar_init(bar(B_PFULL + s), 4);
       mbar_init(bar(B_ODONE + s), 1);
-      mbar_init(bar(B_LFULL + s), 4);
       mbar_init(bar(B_MDONE + s), 1);
     }
-    mbar_init(bar(B_FIN), 1);
+    mbar_init(bar(B_FIN + 0), 1);
+    mbar_init(bar(B_FIN + 1), 1);
     *abort = 0;
     mbar_fence_init();
   }
@@ -229,99 +238,120 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int t = 0; t < p.ntile; ++t) ntiles += tile_kept(p, bh, qt0, t) ? 1 : 0;
   }
 
+  // the next kept KV tile after t (-1: none)
+  auto next_tile = [&](int t) {
+    for (int u = t + 1; u < p.ntile; ++u)
+      if (tile_kept(p, bh, qt0, u)) return u;
+    return -1;
+  };
+
   if (warp == WARP_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !(p.debug_flags & 1) && ntiles > 0) {
-      mbar_arrive_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
+      // Q and the first kept K tile
+      int t = next_tile(-1);
+      mbar_arrive_expect_tx(bar(B_QFULL), 3 * TILE_BYTES);
       tma_load_3d(sb + SM_Q, &tmq, 0, q0, static_cast<int>(bh), bar(B_QFULL));
       tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, static_cast<int>(bh), bar(B_QFULL));
-      int i = 0;
-      for (int t = 0; t < p.ntile && !*abort; ++t) {
-        if (!tile_kept(p, bh, qt0, t)) continue;
-        const int st = i % NS;
-        if (i >= NS && !mbar_wait(bar(B_KVEMPTY + st), ((i / NS) - 1) & 1, abort, WAIT_NS)) {
+      tma_load_3d(sb + SM_K, &tmk, 0, t * TILE, static_cast<int>(bh), bar(B_QFULL));
+      // Step j brings V(j) and its mean tile into stage j % NS and K(j+1)
+      // into K stage (j+1) % NS, all on one barrier.  A K stage is free again
+      // once both slots' QK have read it, a V stage once both mean terms of
+      // its tile were issued.
+      for (int j = 0; t >= 0 && !*abort; ++j) {
+        const int st = j % NS, stk = (j + 1) % NS;
+        const int tn = next_tile(t);
+        if (j >= NS && !mbar_wait(bar(B_VEMPTY + st), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
-        mbar_arrive_expect_tx(bar(B_KVFULL + st), 2 * TILE_BYTES + MU_BYTES);
-        tma_load_3d(sb + SM_K + st * TILE_BYTES, &tmk, 0, t * TILE, static_cast<int>(bh),
-                    bar(B_KVFULL + st));
-        tma_load_3d(sb + SM_V + st * V_STAGE, &tmv, t * TILE, 0, static_cast<int>(bh),
-                    bar(B_KVFULL + st));
+        if (tn >= 0 && j + 1 >= NS &&
+            !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / NS) - 1) & 1, abort, WAIT_NS)) {
+          record_timeout(p, abort);
+          break;
+        }
+        mbar_arrive_expect_tx(bar(B_FULL + st), TILE_BYTES + MU_BYTES + (tn >= 0 ? TILE_BYTES : 0));
+        tma_load_3d(sb + SM_V + st * V_STAGE, &tmv, t * TILE, 0, static_cast<int>(bh), bar(B_FULL + st));
         bulk_load(sb + SM_MU + st * MU_BYTES, p.vmu_op + (bh * p.ntile + t) * 1024, MU_BYTES,
-                  bar(B_KVFULL + st));
-        ++i;
+                  bar(B_FULL + st));
+        if (tn >= 0)
+          tma_load_3d(sb + SM_K + stk * TILE_BYTES, &tmk, 0, tn * TILE, static_cast<int>(bh), bar(B_FULL + st));
+        t = tn;
       }
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
     // ----------------------------------------------------------- MMA issue
+    // One issuing lane per slot, so that one slot's waits never hold back
+    // the other slot's MMAs; tcgen05.commit tracks each lane's own MMAs.
+    const int s = warp - WARP_MMA;
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(bar(B_QFULL), 0, abort, WAIT_NS);
       tc_fence_after();
-      auto next_tile = [&](int t) {
-        for (int u = t + 1; u < p.ntile; ++u)
-          if (tile_kept(p, bh, qt0, u)) return u;
-        return -1;
-      };
       // Descriptors are built once; a byte offset o advances them by o >> 4
       // in the start-address field (all of shared memory is below 256 KiB).
-      const uint64_t dQ = sdesc_sw128(sb + SM_Q), dK = sdesc_sw128(sb + SM_K);
+      const uint64_t dQ = sdesc_sw128(sb + SM_Q + s * TILE_BYTES), dK = sdesc_sw128(sb + SM_K);
       const uint64_t dV = sdesc_sw128(sb + SM_V);
-      const uint64_t dL = sdesc_k8_tf32(sb + SM_L), dMu = sdesc_k8_tf32(sb + SM_MU);
+      const uint64_t dL = sdesc_k8_tf32(sb + SM_L + s * MU_BYTES), dMu = sdesc_k8_tf32(sb + SM_MU);
+      const uint64_t dP = sdesc_sw128(sb + SM_P + s * TILE_BYTES);
+      const uint32_t dO = tmem + COL_O + 160 * s;
       auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-      auto qk = [&](int s, int st) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f8(tmem + COL_S, adv(dQ, s * TILE_BYTES + 32 * kk), adv(dK, st * TILE_BYTES + 32 * kk),
-                 IDESC_QK, kk > 0);
-        mma_commit(bar(B_SFULL + s));
-      };
       auto wt = [&](int b, uint32_t par) {
         if (!ok) return;
         ok = mbar_wait(bar(b), par, abort, WAIT_NS);
         tc_fence_after();
       };
-      int t = next_tile(-1);
-      wt(B_KVFULL + 0, 0);
-      if (ok) qk(0, 0);
-      wt(B_STAKEN + 0, 0);  // slot 0 has S(0) in registers: S is free
-      if (ok) qk(1, 0);
-      for (int i = 0; ok && t >= 0; ++i) {
-        const int st = i % NS;
-        const int tn = next_tile(t);
-        const int stn = (i + 1) % NS;
-        for (int s = 0; s < 2 && ok; ++s) {
-          const uint32_t dO = tmem + COL_O + 160 * s;
-          wt(B_PFULL + s, i & 1);
-          if (!ok) break;
+      // S of this slot for the j-th kept tile (K in stage j % NS)
+      auto qk = [&](int j) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8_tmem_a(dO, tmem + COL_P + 32 * s + 8 * kk, adv(dV, st * V_STAGE + 32 * kk), IDESC_PV,
-                          (i > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(B_ODONE + s));
-          if (tn >= 0) {
-            // S is free once the other slot holds its S(t) (slot 0) or slot 0
-            // holds S(t+1) (slot 1).
-            wt(s == 0 ? B_STAKEN + 1 : B_STAKEN + 0, s == 0 ? (i & 1) : ((i + 1) & 1));
-            if (s == 0) wt(B_KVFULL + stn, ((i + 1) / NS) & 1);
-            if (!ok) break;
-            qk(s, stn);
-          }
-          // The softmax has read and cleared the row sums and written the
-          // mean operand: restore the block means of tile t.
-          wt(B_LFULL + s, i & 1);
-          if (!ok) break;
-          mma_tf32(dO, adv(dL, s * MU_BYTES), adv(dMu, st * MU_BYTES), IDESC_TF32, 1);
-          mma_commit(bar(B_MDONE + s));
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8(tmem + COL_S, adv(dQ, 32 * kk), adv(dK, (j % NS) * TILE_BYTES + 32 * kk), IDESC_QK, kk > 0);
+        mma_commit(bar(B_SFULL + s));
+        mma_commit(bar(B_KEMPTY + j % NS));  // this slot has read K(j)
+      };
+      // The single S buffer is taken in turn: S0(j) S1(j) S0(j+1) ...  QK
+      // of slot 0 for tile i waits until slot 1 holds S(i-1), QK of slot 1
+      // until slot 0 holds S(i).  Each QK goes ahead of the PV that the same
+      // slot's softmax releases later.
+      auto pv = [&](int j) {  // mean term of tile j-1, then [O | l] += P(j) [V ; 1_b0 ; 1_b1]
+        wt(B_PFULL + s, j & 1);  // P(j), and for j > 0 the mean operand of j-1
+        if (!ok) return;
+        if (j > 0) {
+          mma_tf32(dO, dL, adv(dMu, ((j - 1) % NS) * MU_BYTES), IDESC_TF32, 1);
+          mma_commit(bar(B_VEMPTY + (j - 1) % NS));  // this slot is done with V(j-1)
         }
-        if (!ok) break;
-        mma_commit(bar(B_KVEMPTY + st));  // tile t fully consumed
-        t = tn;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8(dO, adv(dP, 32 * kk), adv(dV, (j % NS) * V_STAGE + 32 * kk), IDESC_PV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_ODONE + s));
+      };
+      for (int i = 0; ok && i <= ntiles; ++i) {
+        if (i < ntiles) {
+          // K(i) came with Q (i = 0) or with V(i-1)
+          if (i > 0) wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);
+          if (s == 0) {
+            if (i > 0) wt(B_STAKEN + 1, (i - 1) & 1);
+          } else {
+            wt(B_STAKEN + 0, i & 1);
+          }
+          if (!ok) break;
+          qk(i);
+        }
+        if (i > 0) {
+          if (i == ntiles) wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);  // V of the last tile
+          pv(i - 1);
+        }
+      }
+      // the last tile's mean term (the softmax's extra p_full arrival)
+      wt(B_PFULL + s, ntiles & 1);
+      if (ok) {
+        mma_tf32(dO, dL, adv(dMu, ((ntiles - 1) % NS) * MU_BYTES), IDESC_TF32, 1);
+        mma_commit(bar(B_MDONE + s));
       }
       if (!ok) record_timeout(p, abort);
-      // Drain: every issued MMA has completed before TMEM is released.
-      mma_commit(bar(B_FIN));
-      if (!mbar_wait(bar(B_FIN), 0, abort, WAIT_NS) && !*abort) record_timeout(p, abort);
+      // Drain: every MMA of this lane has completed before TMEM is released.
+      mma_commit(bar(B_FIN + s));
+      if (!mbar_wait(bar(B_FIN + s), 0, abort, WAIT_NS) && !*abort) record_timeout(p, abort);
     }
   } else {
     // ------------------------------------------------------ softmax warps
@@ -333,7 +363,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int qt = static_cast<int>(row >> 6);
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_addr + COL_S;
-    const uint32_t tP = tmem + lane_addr + COL_P + 32 * slot;
+    // row r of this slot's P tile (128B-swizzled K-major, like Q and K)
+    uint8_t* Prow = sm + SM_P + slot * TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
     const uint32_t tO = tmem + lane_addr + COL_O + 160 * slot;
     const float qsc = p.q_scale[bh * p.nbp + (qt < p.nbp ? qt : p.nbp - 1)];
     const float a_i = p.c0 * qsc;
@@ -341,26 +372,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t* Lrow = sm + SM_L + slot * MU_BYTES + (r >> 3) * 256 + (r & 7) * 16;
     const float* ksc = p.k_scale + bh * p.nbp;
     const float NEG_INF = -__int_as_float(0x7f800000);
+    const uint32_t FULL = 0xffffffffu;
+    // the row sums of the two 64-key blocks of the previous tile (columns
+    // 128, 129 of O_s)
+    auto ld_rowsums = [&](float& l0, float& l1) {
+      uint32_t ls0, ls1;
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                   : "=r"(ls0), "=r"(ls1)
+                   : "r"(tO + COL_L));
+      tmem_wait_ld();
+      l0 = __uint_as_float(ls0);
+      l1 = __uint_as_float(ls1);
+    };
+    // tf32 A operand row of the mean restoration, [hi0, lo0, hi0, hi1 | lo1, hi1, 0, 0]
+    auto put_lrow = [&](float v0, float v1) {
+      const float h0 = to_tf32(v0), h1 = to_tf32(v1);
+      const float g0 = to_tf32(v0 - h0), g1 = to_tf32(v1 - h1);
+      *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, h1);
+      *reinterpret_cast<float4*>(Lrow + 128) = make_float4(g1, h1, 0.0f, 0.0f);
+      fence_proxy_async_smem();
+    };
     float m_run = NEG_INF;
     float l = 0.0f;
     bool ok = true;
     int i = 0;
-    for (int t = 0; t < p.ntile; ++t) {
-      if (p.mask && !tile_kept(p, bh, qt0, t)) continue;
-      bool keep0 = row_ok, keep1 = row_ok;
-      if (p.mask) {
-        keep0 = keep0 && mrow && mrow[2 * t] != 0;
-        keep1 = keep1 && mrow && mrow[2 * t + 1] != 0;
-      }
+    int t = next_tile(-1);
+    // block scales and mask bytes of the current tile, loaded one tile ahead
+    float2 ks = t >= 0 ? *reinterpret_cast<const float2*>(ksc + 2 * t) : make_float2(0.0f, 0.0f);
+    uint8_t mk0 = (t >= 0 && mrow) ? mrow[2 * t] : 0, mk1 = (t >= 0 && mrow) ? mrow[2 * t + 1] : 0;
+    for (; t >= 0; ++i) {
+      const int tn = next_tile(t);
+      const float2 ks_n = tn >= 0 ? *reinterpret_cast<const float2*>(ksc + 2 * tn) : make_float2(0.0f, 0.0f);
+      const uint8_t mk0_n = (tn >= 0 && mrow) ? mrow[2 * tn] : 0;
+      const uint8_t mk1_n = (tn >= 0 && mrow) ? mrow[2 * tn + 1] : 0;
+      const bool keep0 = row_ok && (!p.mask || mk0 != 0);
+      const bool keep1 = row_ok && (!p.mask || mk1 != 0);
       const int64_t kv_lim = p.N - static_cast<int64_t>(t) * TILE;  // valid keys in the tile
-      const float2 ks = *reinterpret_cast<const float2*>(ksc + 2 * t);
       const float A0 = a_i * ks.x;
       const float A1 = a_i * ks.y;
       // Warp-uniform: does any lane need per-key masking in this tile?
-      const bool full = keep0 && keep1 && kv_lim >= TILE;
-      const bool masked = !__all_sync(0xffffffffu, full);
+      const bool masked = !__all_sync(FULL, keep0 && keep1 && kv_lim >= TILE);
 
-      if (!(ok = mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS))) break;
+      if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS)))) break;
       tc_fence_after();
       float x[128];
       {
@@ -414,8 +467,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const float Bq = live ? (p.C - m_new) * 0.00390625f : 0.0f;
       const float A0q = A0 * 0.00390625f, A1q = A1 * 0.00390625f;
-      // Bytes of masked keys (or of a row with no key kept so far) are
-      // cleared after the cast.
       const int64_t lim0 = !masked ? 64 : (live && keep0) ? (kv_lim < 64 ? kv_lim : 64) : 0;
       const int64_t lim1 = !masked ? 128 : (live && keep1) ? (kv_lim < 128 ? kv_lim : 128) : 64;
       uint32_t w[32];  // the row's 128 E4M3 bytes
@@ -432,69 +483,72 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           w[q] &= keep;
         }
       }
-      tmem_st32(tP, w);  // row r of P_s: 128 bytes in 32 columns
-      // Rescale O (PV(t-1) done; MEAN(t-1) waited for above; PV(t) is issued
-      // only after p_full below).
-      if (i > 0 && __any_sync(0xffffffffu, resc)) {
-        // O must hold MEAN(t-1) before it is scaled
-        if (!(ok = mbar_wait(bar(B_MDONE + slot), (i - 1) & 1, abort, WAIT_NS))) break;
+      if (i > 0) {
+        // PV(i-1) done (and with it the mean term of tile i-2): P may be
+        // overwritten and the row sums of tile i-1 are final.
+        if (!(ok = __all_sync(FULL, mbar_wait(bar(B_ODONE + slot), (i - 1) & 1, abort, WAIT_NS)))) break;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + 32 * c, o);
-        }
       }
+      // row r of P_s: 128 bytes, 16-byte chunk c at position c ^ (r & 7)
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(Prow + ((c ^ (r & 7)) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      if (i > 0) {
+        // Row sums of tile i-1: read and cleared, so that PV(i) accumulates
+        // its own.  If the maximum moved, O (holding PV up to i-1 and the
+        // mean terms up to i-2; the mean term of i-1 is issued only after
+        // this slot's l_full) and l move to the new maximum, and the mean
+        // operand of tile i-1 is written already scaled by alpha.
+        float l0, l1;
+        ld_rowsums(l0, l1);
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tO + COL_L), "r"(0u),
+                     "r"(0u)
+                     : "memory");
+        if (__any_sync(FULL, resc)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
+        }
+        l = (l + (l0 + l1)) * alpha;
+        put_lrow(l0 * alpha, l1 * alpha);
+      }
+      fence_proxy_async_smem();  // P (and the mean operand) to the tensor core
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
-
-      // Row sums of the decoded bytes (columns 128, 129 of the PV result),
-      // the running l, and the tf32 A operand of the mean restoration:
-      // [hi0, lo0, hi0, hi1 | lo1, hi1, 0, 0].  The two columns are cleared
-      // so that the next PV accumulates the next tile's sums alone.
-      if (!(ok = mbar_wait(bar(B_ODONE + slot), i & 1, abort, WAIT_NS))) break;
-      tc_fence_after();
-      uint32_t ls0, ls1;
-      asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
-                   : "=r"(ls0), "=r"(ls1)
-                   : "r"(tO + COL_L));
-      tmem_wait_ld();
-      asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tO + COL_L), "r"(0u),
-                   "r"(0u)
-                   : "memory");
-      const float l0 = __uint_as_float(ls0), l1 = __uint_as_float(ls1);
-      l = l * alpha + (l0 + l1);
-      {
-        const float h0 = to_tf32(l0), h1 = to_tf32(l1);
-        const float g0 = to_tf32(l0 - h0), g1 = to_tf32(l1 - h1);
-        *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, h1);
-        *reinterpret_cast<float4*>(Lrow + 128) = make_float4(g1, h1, 0.0f, 0.0f);
+      t = tn;
+      ks = ks_n;
+      mk0 = mk0_n;
+      mk1 = mk1_n;
+    }
+    // the last tile's row sums, then its mean term
+    if (ok && ntiles > 0) {
+      ok = __all_sync(FULL, mbar_wait(bar(B_ODONE + slot), (ntiles - 1) & 1, abort, WAIT_NS));
+      if (ok) {
+        tc_fence_after();
+        float l0, l1;
+        ld_rowsums(l0, l1);
+        l += l0 + l1;
+        put_lrow(l0, l1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
+        ok = __all_sync(FULL, mbar_wait(bar(B_MDONE + slot), 0, abort, WAIT_NS));
+        tc_fence_after();
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_LFULL + slot));
-      ++i;
     }
     if (!ok) record_timeout(p, abort);
 
     // ------------------------------------------------------------ epilogue
-    bool have = ok && ntiles > 0;
-    if (have) {
-      // the last mean restoration
-      if (!mbar_wait(bar(B_MDONE + slot), (ntiles - 1) & 1, abort, WAIT_NS)) {
-        record_timeout(p, abort);
-        have = false;
-      }
-      tc_fence_after();
-    }
+    const bool have = ok && ntiles > 0;
     if (__all_sync(0xffffffffu, have)) {
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll

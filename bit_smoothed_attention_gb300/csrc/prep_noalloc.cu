@@ -31,6 +31,10 @@
 #include "../../include/vcattn.h"
 #include "internal.h"
 
+namespace vc {
+vcattn_status from_cuda(cudaError_t e);  // records e for vcattn_last_cuda_error
+}  // namespace vc
+
 namespace {
 
 constexpr size_t NOALLOC_SCRATCH_BYTES = static_cast<size_t>(16) << 20;
@@ -46,8 +50,9 @@ std::mutex g_scratch_mu;
 // Device address of g_prep_scratch on the current device (looked up once).
 void* scratch_address(vcattn_status* st) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) {
-    *st = VCATTN_ERR_CUDA;
+  const cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess || dev < 0 || dev >= MAX_DEV) {
+    *st = e0 != cudaSuccess ? vc::from_cuda(e0) : VCATTN_ERR_UNSUPPORTED;
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(g_scratch_mu);
@@ -55,7 +60,7 @@ void* scratch_address(vcattn_status* st) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_prep_scratch);
     if (e != cudaSuccess || !p) {
-      *st = VCATTN_ERR_CUDA;
+      *st = vc::from_cuda(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
       return nullptr;
     }
     g_scratch_ptr[dev] = p;
@@ -93,5 +98,5 @@ extern "C" vcattn_status vcattn_prep_noalloc(const vcattn_shape* s, const void* 
   const cudaError_t e = vc::launch_prep(static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(K),
                                         static_cast<const uint16_t*>(V), perm, BH, s->N, o, w,
                                         static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? VCATTN_OK : VCATTN_ERR_CUDA;
+  return vc::from_cuda(e);
 }

@@ -8,6 +8,18 @@
 #include "../../include/vcattn.h"
 #include "internal.h"
 
+namespace vc {
+// The CUDA error behind the calling thread's last VCATTN_ERR_CUDA.
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+vcattn_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return VCATTN_OK;
+  g_last_cuda = e;
+  return VCATTN_ERR_CUDA;
+}
+}  // namespace vc
+using vc::from_cuda;
+
 namespace {
 
 using vc::D;
@@ -23,15 +35,17 @@ std::mutex g_mu;
 
 uint32_t* err_word(vcattn_status* st) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) {
-    *st = VCATTN_ERR_CUDA;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= MAX_DEV) {
+    *st = e != cudaSuccess ? from_cuda(e) : VCATTN_ERR_UNSUPPORTED;
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_err_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess || !p) {
-      *st = VCATTN_ERR_CUDA;
+    const cudaError_t e2 = cudaGetSymbolAddress(&p, g_err_word);
+    if (e2 != cudaSuccess || !p) {
+      *st = from_cuda(e2 != cudaSuccess ? e2 : cudaErrorInvalidSymbol);
       return nullptr;
     }
     g_err_ptr[dev] = static_cast<uint32_t*>(p);
@@ -49,7 +63,6 @@ vcattn_status check_shape(const vcattn_shape* s) {
   return VCATTN_OK;
 }
 
-vcattn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? VCATTN_OK : VCATTN_ERR_CUDA; }
 
 // Layout of the prepped tensors inside one buffer (256-byte aligned parts).
 size_t prepped_layout(const vcattn_shape* s, void* base, vcattn_prepped* out) {
@@ -219,16 +232,21 @@ vcattn_status vcattn_last_device_error(void* stream) {
   vcattn_status st = VCATTN_OK;
   uint32_t* err = err_word(&st);
   if (!err) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return VCATTN_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e);
   uint32_t h = 0;
-  if (cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return VCATTN_ERR_CUDA;
+  if ((e = cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess) return from_cuda(e);
   if (h) {
     const uint32_t zero = 0;
-    if (cudaMemcpy(err, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess) return VCATTN_ERR_CUDA;
+    if ((e = cudaMemcpy(err, &zero, 4, cudaMemcpyHostToDevice)) != cudaSuccess) return from_cuda(e);
   }
   if (h & vc::ERR_TIMEOUT) return VCATTN_ERR_TIMEOUT;
   if (h) return VCATTN_ERR_DEVICE;
   return VCATTN_OK;
+}
+
+const char* vcattn_last_cuda_error(void) {
+  return vc::g_last_cuda == cudaSuccess ? "no error" : cudaGetErrorString(vc::g_last_cuda);
 }
 
 const char* vcattn_status_string(vcattn_status s) {

@@ -24,7 +24,10 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(
 class VcattnError(RuntimeError):
     def __init__(self, status, what):
         self.status = status
-        super().__init__("%s: %s (status %d)" % (what, _lib().vcattn_status_string(status).decode(), status))
+        msg = "%s: %s (status %d)" % (what, _lib().vcattn_status_string(status).decode(), status)
+        if status == ERR_CUDA:
+            msg += ": " + _lib().vcattn_last_cuda_error().decode()
+        super().__init__(msg)
 
 
 class Shape(ctypes.Structure):
@@ -76,6 +79,8 @@ def _lib():
         lib.vcattn_last_device_error.argtypes = [P]
         lib.vcattn_status_string.restype = ctypes.c_char_p
         lib.vcattn_status_string.argtypes = [st]
+        lib.vcattn_last_cuda_error.restype = ctypes.c_char_p
+        lib.vcattn_last_cuda_error.argtypes = []
         _L = lib
     return _L
 

@@ -196,6 +196,10 @@ vcattn_status vcattn_fwd(const vcattn_shape* shape, const void* Q, const void* K
  * VCATTN_ERR_CUDA when the synchronisation itself fails). */
 vcattn_status vcattn_last_device_error(void* stream);
 const char* vcattn_status_string(vcattn_status s);
+/* Text of the CUDA error behind the calling thread's most recent
+ * VCATTN_ERR_CUDA (host side: a failed launch, attribute, tensor-map or
+ * copy call); "no error" if there was none.  The string is static. */
+const char* vcattn_last_cuda_error(void);
 
 #ifdef __cplusplus
 }
