@@ -506,15 +506,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      "r"(0u)
                      : "memory");
         if (__any_sync(FULL, resc)) {
+          // all 128 accumulator columns in flight at once (x is dead here)
+          uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
+          uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
+          uint32_t (&o2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
+          uint32_t (&o3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
+          tmem_ld32(tO + 0, o0);
+          tmem_ld32(tO + 32, o1);
+          tmem_ld32(tO + 64, o2);
+          tmem_ld32(tO + 96, o3);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + 32 * c, o);
-          }
+          for (int e = 0; e < 128; ++e) x[e] *= alpha;
+          tmem_st32(tO + 0, o0);
+          tmem_st32(tO + 32, o1);
+          tmem_st32(tO + 64, o2);
+          tmem_st32(tO + 96, o3);
         }
         l = (l + (l0 + l1)) * alpha;
         put_lrow(l0 * alpha, l1 * alpha);
