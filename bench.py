@@ -61,6 +61,15 @@ def head_range(H, world, rank):
     return lo, lo + base + (1 if rank < extra else 0)
 
 
+def max_over_ranks(x, device):
+    """The largest of the ranks' values of x (the job's time is the slowest
+    rank's)."""
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
 
@@ -204,10 +213,7 @@ def run_ours(args):
         raise RuntimeError("device-side error during the timed region")
     ms = t_start.elapsed_time(t_end)
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dev)
     ms_step = ms / args.steps
     t_group = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     t_prep = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
@@ -296,10 +302,7 @@ def run_e2e(args, w, vcattn, dev, Q, K, V, mask, sm_scale, flops_step, world):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([dt], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
+        dt = max_over_ranks(dt, dev)
     return {"value": round(flops_step / dt / 1e12, 2), "unit": "TFLOPS",
             "h2d_bytes_per_step": int(3 * Q.numel() * 2) * world,
             "d2h_bytes_per_step": int(Q.numel() * 2) * world,

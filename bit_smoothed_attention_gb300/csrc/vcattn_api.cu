@@ -168,9 +168,10 @@ vcattn_status vcattn_prep(const vcattn_shape* s, const void* Q, const void* K, c
                                    to_prep_out(out), w, static_cast<cudaStream_t>(stream)));
 }
 
-vcattn_status vcattn_attn_ex(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
-                             int off, float tau8, int out_f32, const uint8_t* tile_mask, void* O,
-                             float* lse2, void* stream) {
+namespace {
+vcattn_status attn_impl(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale, int off,
+                        float tau8, int out_f32, const uint8_t* tile_mask, void* O, float* lse2,
+                        void* stream, int debug_flags) {
   vcattn_status st = check_shape(s);
   if (st != VCATTN_OK) return st;
   if (!in || !prepped_ok(in) || !O || !aligned16(O) || (lse2 && !aligned16(lse2)))
@@ -199,8 +200,20 @@ vcattn_status vcattn_attn_ex(const vcattn_shape* s, const vcattn_prepped* in, fl
   a.off = off;
   a.tau8 = tau8;
   a.err = err;
-  a.debug_flags = 0;
+  a.debug_flags = debug_flags;
   return from_cuda(vc::launch_attn(a, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+vcattn_status vcattn_attn_ex(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
+                             int off, float tau8, int out_f32, const uint8_t* tile_mask, void* O,
+                             float* lse2, void* stream) {
+  return attn_impl(s, in, sm_scale, off, tau8, out_f32, tile_mask, O, lse2, stream, 0);
+}
+
+vcattn_status vcattn_test_attn_stalled(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
+                                       void* O, float* lse2, void* stream) {
+  return attn_impl(s, in, sm_scale, 8, 6.0f, 0, nullptr, O, lse2, stream, 1);
 }
 
 vcattn_status vcattn_attn(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,

@@ -233,6 +233,22 @@ def fwd_workspace_bytes(shape_tuple):
     return int(_lib().vcattn_fwd_workspace_bytes(ctypes.byref(s)))
 
 
+def test_attn_stalled(pp, sm_scale, stream=None):
+    """Failure-path test hook: attention with the K/V loader switched off, so
+    every bounded wait in the kernel runs out; last_device_error() then
+    reports ERR_TIMEOUT."""
+    B, H, N = pp.shape.B, pp.shape.H, pp.shape.N
+    O = torch.empty(B, H, N, 128, dtype=torch.bfloat16, device=pp.buf.device)
+    lse2 = torch.empty(B, H, N, dtype=torch.float32, device=pp.buf.device)
+    f = _lib().vcattn_test_attn_stalled
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(PreppedStruct), ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    _check(f(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale), _ptr(O), _ptr(lse2),
+             _stream(stream)), "vcattn_test_attn_stalled")
+    return O, lse2
+
+
 def last_device_error(stream=None):
     """Synchronise and return (and clear) the device error status."""
     return _lib().vcattn_last_device_error(_stream(stream))

@@ -196,6 +196,15 @@ vcattn_status vcattn_fwd(const vcattn_shape* shape, const void* Q, const void* K
  * VCATTN_ERR_CUDA when the synchronisation itself fails). */
 vcattn_status vcattn_last_device_error(void* stream);
 const char* vcattn_status_string(vcattn_status s);
+/* Test hook for the failure path (not part of the method): runs
+ * vcattn_attn with its K/V loader switched off, so no tile ever arrives and
+ * every bounded wait in the kernel (2 s each) runs out.  The kernel records
+ * the timeout in the device error word and returns; O and lse2 are left
+ * undefined, the context stays usable, and the next
+ * vcattn_last_device_error() reports VCATTN_ERR_TIMEOUT.  Arguments as for
+ * vcattn_attn (dense, no mask). */
+vcattn_status vcattn_test_attn_stalled(const vcattn_shape* shape, const vcattn_prepped* in,
+                                       float sm_scale, void* O, float* lse2, void* stream);
 /* Text of the CUDA error behind the calling thread's most recent
  * VCATTN_ERR_CUDA (host side: a failed launch, attribute, tensor-map or
  * copy call); "no error" if there was none.  The string is static. */

@@ -1,0 +1,33 @@
+"""Failure detection on the GPU without a fault: the attention kernel's
+bounded waits.  With the K/V loader switched off (a test hook), no tile ever
+arrives; every wait gives up after its 2 s limit, the kernel records a
+timeout in the device error word and exits, and the CUDA context stays
+usable for the next, normal call."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from bit_smoothed_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SM = float(np.float32(1 / math.sqrt(128)))
+
+
+def test_stalled_loader_reports_timeout_and_context_survives():
+    from bit_smoothed_attention_gb300 import build, vcattn
+    build.build()
+    Q, K, V = W.make_qkv(1, 1, 256, 4, 77, device="cuda")
+    _, perm = vcattn.group(V, 4, 5)
+    pp = vcattn.prep(Q, K, V, perm)
+    torch.cuda.synchronize()
+    assert vcattn.last_device_error() == vcattn.OK
+    vcattn.test_attn_stalled(pp, SM)
+    assert vcattn.last_device_error() == vcattn.ERR_TIMEOUT
+    assert vcattn.last_device_error() == vcattn.OK          # read and cleared
+    O, L = vcattn.attn(pp, SM)                               # the context still works
+    torch.cuda.synchronize()
+    assert vcattn.last_device_error() == vcattn.OK
+    assert torch.isfinite(O.float()).all() and torch.isfinite(L).all()
