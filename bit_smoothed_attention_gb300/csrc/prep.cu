@@ -204,25 +204,59 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
 }
 
 // mu_K = (adjacent-pairing tree over the block sums, padded with +0 to a
-// power of two) / N; v_scale from the residual amax.  grid (BH), block D.
-__global__ void __launch_bounds__(D) prep_kmean(const float* __restrict__ kbs,
-                                                const uint32_t* __restrict__ vamax, int64_t N,
-                                                int nb, int nbp, float* __restrict__ k_mean,
-                                                float* __restrict__ v_scale) {
+// power of two P) / N; v_scale from the residual amax.  The tree over P
+// leaves is cut into KM_SEG aligned subtrees of P / KM_SEG leaves (the
+// tree's own nodes, so the sums are bit-identical): thread (d, seg) reduces
+// subtree seg of channel d with eight independent loads in flight, then the
+// KM_SEG subtree sums are combined in tree order.  grid (BH), block
+// (D, KM_SEG).
+constexpr int KM_SEG = 8;
+__global__ void __launch_bounds__(D * KM_SEG) prep_kmean(const float* __restrict__ kbs,
+                                                         const uint32_t* __restrict__ vamax, int64_t N,
+                                                         int nb, int nbp, float* __restrict__ k_mean,
+                                                         float* __restrict__ v_scale) {
+  __shared__ float sub[KM_SEG][D];
   const int64_t bh = blockIdx.x;
-  const int d = threadIdx.x;
+  const int d = threadIdx.x, seg = threadIdx.y;
   int64_t P = 1;
   while (P < nb) P *= 2;
-  float st[40];
-  int top = 0;
-  for (int64_t b = 0; b < P; ++b) {
-    float v = b < nb ? kbs[(bh * nbp + b) * D + d] : 0.0f;
-    for (int64_t t = b; t & 1; t >>= 1) v = st[--top] + v;
-    st[top++] = v;
+  const int nseg = P < KM_SEG ? static_cast<int>(P) : KM_SEG;  // a power of two
+  const int64_t len = P / nseg;                                 // leaves per subtree
+  if (seg < nseg) {
+    const int64_t lo = seg * len;
+    const float* src = kbs + bh * nbp * D + d;
+    float st[40];
+    int top = 0;
+    for (int64_t b = 0; b < len; b += 8) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int64_t leaf = lo + b + e;
+        v[e] = (b + e < len && leaf < nb) ? src[leaf * D] : 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (b + e >= len) break;
+        float x = v[e];
+        for (int64_t t = b + e; t & 1; t >>= 1) x = st[--top] + x;
+        st[top++] = x;
+      }
+    }
+    sub[seg][d] = st[0];
   }
-  k_mean[bh * D + d] = st[0] / static_cast<float>(N);
-  const float a = __uint_as_float(vamax[bh * D + d]);
-  v_scale[bh * D + d] = a >= AMAX_FLOOR ? a / 448.0f : 1.0f;
+  __syncthreads();
+  if (seg == 0) {
+    float st[4];
+    int top = 0;
+    for (int i = 0; i < nseg; ++i) {
+      float x = sub[i][d];
+      for (int t = i; t & 1; t >>= 1) x = st[--top] + x;
+      st[top++] = x;
+    }
+    k_mean[bh * D + d] = st[0] / static_cast<float>(N);
+    const float a = __uint_as_float(vamax[bh * D + d]);
+    v_scale[bh * D + d] = a >= AMAX_FLOOR ? a / 448.0f : 1.0f;
+  }
 }
 
 // Quantisers.  Each CTA handles QUANT_BPC consecutive blocks; the next
@@ -433,8 +467,8 @@ cudaError_t launch_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   }
   prep_stats<<<dim3(static_cast<unsigned>(ceil_div(nb, STATS_BPC)), static_cast<unsigned>(BH)), 256,
                STATS_SMEM, s>>>(K, V, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax);
-  prep_kmean<<<static_cast<unsigned>(BH), D, 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp, o.k_mean,
-                                                     o.v_scale);
+  prep_kmean<<<static_cast<unsigned>(BH), dim3(D, KM_SEG), 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp,
+                                                                   o.k_mean, o.v_scale);
   prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH)), 256,
                QUANT_SMEM, s>>>(
       Q, K, V, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
