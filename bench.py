@@ -47,6 +47,28 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+def attn_traffic():
+    """DRAM bytes per 56-head attention launch from the committed ncu summary,
+    or None when the kernel source has changed since those counters were
+    taken (the summary records the source hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attn_fwd_live_h8.md")
+    src = os.path.join(ROOT, "bit_smoothed_attention_gb300", "csrc", "attn.cu")
+    try:
+        text = open(path).read()
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    rec = {}
+    for ln in text.splitlines():
+        if ":" in ln and ln.split(":")[0].strip() in ("kernel_source_sha256", "traffic_bytes_per_launch"):
+            k, v = ln.split(":", 1)
+            rec[k.strip()] = v.strip().split()[0]
+    if rec.get("kernel_source_sha256") != h or "traffic_bytes_per_launch" not in rec:
+        return None
+    return int(rec["traffic_bytes_per_launch"])
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -262,7 +284,8 @@ def run_ours(args):
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(attn_tflops / fp8_peak, 4),
                      "peak_source": "%s bf16 sustained x %.0f (nominal FP8/bf16 ratio)" % (pk["src"], FP8_OVER_BF16),
-                     "traffic": None},
+                     "traffic": attn_traffic() if (args.workload == "live" and world == 1) else None,
+                     "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
         "clocks": clock_info,
@@ -380,6 +403,27 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def profile_case(workload):
+    """One grouping, one preprocessing and two attention calls on `workload`,
+    untimed: the launch sequence the committed ncu summaries capture
+    (``-k regex:<kernel> -s <n> -c <m>``)."""
+    from bit_smoothed_attention_gb300 import build, vcattn
+    build.build()
+    w = W.WORKLOADS[workload]
+    Q, K, V = W.make_workload(w, device="cuda")
+    _, perm = vcattn.group(V, w.k, w.iters)
+    pp = vcattn.prep(Q, K, V, perm)
+    pp = vcattn.prep(Q, K, V, perm, out=pp)
+    sm = float(np.float32(w.sm_scale))
+    O, L = vcattn.attn(pp, sm)
+    vcattn.attn(pp, sm, O=O, lse2=L)
+    torch.cuda.synchronize()
+    st = vcattn.last_device_error()
+    if st != 0:
+        raise RuntimeError("device error status %d" % st)
+    print("profile case %s done" % workload)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -389,8 +433,12 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-baseline leg")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--profile-case", default=None, choices=sorted(W.WORKLOADS),
+                    help="run one untimed pass of the path for an ncu capture and exit")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case(args.profile_case)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
