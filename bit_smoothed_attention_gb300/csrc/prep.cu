@@ -73,16 +73,29 @@ constexpr int TILE_SMEM = BLK * D * 2;  // 16 KiB
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 256 + ((chunk ^ ((row >> 2) & 15)) * 16));
 }
-__device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, const int32_t* perm,
-                                           int64_t r0, int64_t N) {
+// The source rows of the 4 pieces a thread stages for the block starting at
+// r0 (rows r0 + threadIdx.x / 16 + 16 u); loaded one block ahead so that the
+// gather index is in a register when the copy is issued.
+struct Src4 {
+  int64_t r[4];
+};
+__device__ __forceinline__ Src4 load_src(const int32_t* perm, int64_t r0, int64_t N) {
+  Src4 s;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int64_t r = r0 + u * 16 + (static_cast<int>(threadIdx.x) >> 4);
+    s.r[u] = r < N ? (perm ? static_cast<int64_t>(perm[r]) : r) : -1;
+  }
+  return s;
+}
+__device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, const Src4& src4) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int piece = u * 256 + static_cast<int>(threadIdx.x);
     const int row = piece >> 4, chunk = piece & 15;
-    const int64_t r = r0 + row;
     uint8_t* dst = tile + swz(row, chunk);
-    if (r < N) {
-      const int64_t src = perm ? perm[r] : r;
+    if (src4.r[u] >= 0) {
+      const int64_t src = src4.r[u];
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                    "l"(base + src * D + chunk * 8)
                    : "memory");
@@ -118,17 +131,26 @@ __device__ __forceinline__ float max16(float a) {
   return a;
 }
 
-// Block max over all 256 threads.
-__device__ __forceinline__ float block_max(float a, float* red) {
+// Block max of two values at once over all 256 threads (one pair of barriers).
+__device__ __forceinline__ float2 block_max2(float a, float b, float* red) {
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  for (int m = 1; m < 32; m <<= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, m));
+  }
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = a;
+    red[8 + (threadIdx.x >> 5)] = b;
+  }
   __syncthreads();
-  float r = red[0];
+  float ra = red[0], rb = red[8];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
-  return r;
+  for (int w = 1; w < 8; ++w) {
+    ra = fmaxf(ra, red[w]);
+    rb = fmaxf(rb, red[8 + w]);
+  }
+  return make_float2(ra, rb);
 }
 
 // Stats: K block sums (original order), mean of each permuted V block, and
@@ -153,10 +175,16 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
   const int32_t* ph = perm ? perm + bh * N : nullptr;
   const uint16_t* Kh = K + bh * N * D;
   const uint16_t* Vh = V + bh * N * D;
+  // gather indices of the next block to stage (one block ahead)
+  Src4 nk = load_src(nullptr, b0 * BLK, N), nv = load_src(ph, b0 * BLK, N);
   auto stage = [&](int64_t b, int buf) {
-    stage_rows(ssm + buf * 2 * TILE_SMEM, Kh, nullptr, b * BLK, N);
-    stage_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, Vh, ph, b * BLK, N);
+    stage_rows(ssm + buf * 2 * TILE_SMEM, Kh, nk);
+    stage_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, Vh, nv);
     cp_commit();
+    if (b + 1 < b1) {
+      nk = load_src(nullptr, (b + 1) * BLK, N);
+      nv = load_src(ph, (b + 1) * BLK, N);
+    }
   };
   stage(b0, 0);
   float am[8];
@@ -283,12 +311,17 @@ __global__ void __launch_bounds__(256) prep_quant(
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * QUANT_BPC;
   const int64_t b1 = b0 + QUANT_BPC < nbp ? b0 + QUANT_BPC : nbp;
   const int32_t* ph = perm ? perm + bh * N : nullptr;
+  Src4 nq = load_src(nullptr, b0 * BLK, N), ng = load_src(ph, b0 * BLK, N);
   auto stage = [&](int64_t b, int buf) {
     uint8_t* t = qsm + buf * 3 * TILE_SMEM;
-    stage_rows(t, Q + bh * N * D, nullptr, b * BLK, N);
-    stage_rows(t + TILE_SMEM, K + bh * N * D, ph, b * BLK, N);
-    stage_rows(t + 2 * TILE_SMEM, V + bh * N * D, ph, b * BLK, N);
+    stage_rows(t, Q + bh * N * D, nq);
+    stage_rows(t + TILE_SMEM, K + bh * N * D, ng);
+    stage_rows(t + 2 * TILE_SMEM, V + bh * N * D, ng);
     cp_commit();
+    if (b + 1 < b1) {
+      nq = load_src(nullptr, (b + 1) * BLK, N);
+      ng = load_src(ph, (b + 1) * BLK, N);
+    }
   };
   stage(b0, 0);
   if (threadIdx.x < D) kmu[threadIdx.x] = k_mean[bh * D + threadIdx.x];
@@ -315,15 +348,28 @@ __global__ void __launch_bounds__(256) prep_quant(
     const int64_t r0 = b * BLK + 4 * m.g;
     const bool pad_block = b >= nb;
 
-    // ---- Q: per 64-query block, original order ----
-    float x[4][8];
+    // the block's V means, needed below (loaded early to hide the latency)
+    const int64_t mo = (bh * nbp + b) * D + 8 * m.cc;
+    float mu[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) mu[c] = pad_block ? 0.0f : v_mean[mo + c];
+
+    // ---- Q (per 64-query block, original order) and K (gathered, centred,
+    // per 64-key block): both block maxima in one reduction ----
+    float x[4][8], xk[4][8];
     read_rows(tq, m.g, m.cc, x);
-    float a = 0.0f;
+    read_rows(tk, m.g, m.cc, xk);
+    float a = 0.0f, ak = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) a = fmaxf(a, fabsf(x[i][c]));
-    float amax = block_max(a, red);
+      for (int c = 0; c < 8; ++c) {
+        a = fmaxf(a, fabsf(x[i][c]));
+        xk[i][c] = (r0 + i < N) ? xk[i][c] - kmu[8 * m.cc + c] : 0.0f;
+        ak = fmaxf(ak, fabsf(xk[i][c]));
+      }
+    const float2 am2 = block_max2(a, ak, red);
+    float amax = am2.x;
     bool live = amax >= AMAX_FLOOR;
     float inv = live ? 448.0f / amax : 0.0f;
 #pragma unroll
@@ -349,35 +395,20 @@ __global__ void __launch_bounds__(256) prep_quant(
         qmu[bh * N + r] = acc;
       }
     }
-
-    // ---- K: gathered, centred, per 64-key block ----
-    read_rows(tk, m.g, m.cc, x);
-    a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        x[i][c] = (r0 + i < N) ? x[i][c] - kmu[8 * m.cc + c] : 0.0f;
-        a = fmaxf(a, fabsf(x[i][c]));
-      }
-    amax = block_max(a, red);
+    amax = am2.y;
     live = amax >= AMAX_FLOOR;
     inv = live ? 448.0f / amax : 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float y[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) y[c] = live ? x[i][c] * inv : 0.0f;
+      for (int c = 0; c < 8; ++c) y[c] = live ? xk[i][c] * inv : 0.0f;
       *reinterpret_cast<uint2*>(k8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
     }
     if (threadIdx.x == 0) k_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
 
     // ---- V: gathered, block-demeaned residual, per-channel scale, transposed ----
     read_rows(tv, m.g, m.cc, x);
-    const int64_t mo = (bh * nbp + b) * D + 8 * m.cc;
-    float mu[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) mu[c] = pad_block ? 0.0f : v_mean[mo + c];
     uint2 by[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
