@@ -410,8 +410,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int64_t kv_lim = p.N - static_cast<int64_t>(t) * TILE;  // valid keys in the tile
       const float A0 = a_i * ks.x;
       const float A1 = a_i * ks.y;
-      // Warp-uniform: does any lane need per-key masking in this tile?
-      const bool masked = !__all_sync(FULL, keep0 && keep1 && kv_lim >= TILE);
+      // Warp-uniform: does the tile run past N (the last tile only)?  Only
+      // then are keys masked one by one; a 64-key block that a row does not
+      // keep is dropped as a whole (no max contribution, bytes cleared).
+      const bool partial = !__all_sync(FULL, kv_lim >= TILE);
 
       if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS)))) break;
       tc_fence_after();
@@ -430,13 +432,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_STAKEN + slot));  // S may be overwritten
-      if (masked) {
-        // masked keys and keys past N never contribute: -inf for the max
+      if (partial) {
+        // keys past N never contribute: -inf for the max
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const bool valid = (j < 64 ? keep0 : keep1) && j < kv_lim;
-          x[j] = valid ? x[j] : NEG_INF;
-        }
+        for (int j = 0; j < 128; ++j) x[j] = j < kv_lim ? x[j] : NEG_INF;
       }
       // four independent max chains (two per 64-key half)
       float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
@@ -450,7 +449,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const float mx0 = fmax3(ma, mb, fmaxf(x[31], x[63]));
       const float mx1 = fmax3(mc, md, fmaxf(x[95], x[127]));
-      const float m_tile = fmaxf(A0 * mx0, A1 * mx1);
+      const float m_tile = fmaxf(keep0 ? A0 * mx0 : NEG_INF, keep1 ? A1 * mx1 : NEG_INF);
       const bool need = m_tile > m_run + p.tau8;
       const float m_new = need ? m_tile : m_run;
       const bool live = m_new != NEG_INF;
@@ -458,22 +457,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
       m_run = m_new;
 
-      // ExpCast -> 32 words of E4M3 bytes.  In a masked tile the -inf scores
-      // are replaced by 0 (keeping the cast finite) and the bytes of masked
-      // keys, or of a row with no key kept so far, are cleared afterwards.
-      if (masked) {
+      // ExpCast -> 32 words of E4M3 bytes.  In the partial tile the -inf
+      // scores are replaced by 0 (keeping the cast finite); the bytes of keys
+      // past N, of dropped blocks, and of a row with no key kept so far are
+      // cleared after the cast (a dropped block's scores are finite, so its
+      // cast is too).
+      if (partial) {
 #pragma unroll
         for (int j = 0; j < 128; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
       }
       const float Bq = live ? (p.C - m_new) * 0.00390625f : 0.0f;
       const float A0q = A0 * 0.00390625f, A1q = A1 * 0.00390625f;
-      const int64_t lim0 = !masked ? 64 : (live && keep0) ? (kv_lim < 64 ? kv_lim : 64) : 0;
-      const int64_t lim1 = !masked ? 128 : (live && keep1) ? (kv_lim < 128 ? kv_lim : 128) : 64;
       uint32_t w[32];  // the row's 128 E4M3 bytes
 #pragma unroll
       for (int q = 0; q < 32; ++q)
         w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q, Bq);
-      if (masked) {
+      const bool k0 = live && keep0, k1 = live && keep1;
+      if (partial || !__all_sync(FULL, k0 && k1)) {
+        const int64_t lim0 = k0 ? (kv_lim < 64 ? kv_lim : 64) : 0;
+        const int64_t lim1 = k1 ? (kv_lim < 128 ? kv_lim : 128) : 64;
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           uint32_t keep = 0;
