@@ -18,9 +18,13 @@
 //   split into tf32 high and low parts and whose B operand is the prepared
 //   mean tile.
 //
-// CTA = 256 query rows (two 128-row slots) of one (b, h).  Warps 0-3 run the
-// softmax of slot 0 (thread = row = TMEM lane), warps 4-7 slot 1, warp 8
-// issues TMA loads, warp 9 allocates TMEM and issues every MMA from one lane.
+// CTA = 256 query rows (two 128-row slots) of one (b, h).  Warps 0 and 1
+// issue the MMAs of slot 0 and slot 1 from one lane each (warp 0 also
+// allocates TMEM), warp 2 issues the TMA loads, warp 3 is idle, warps 4-7 run
+// the softmax of slot 0 (thread = row = TMEM lane quarter warp & 3) and warps
+// 8-11 that of slot 1.  The issuing warps have the lowest warp numbers so that
+// the warp schedulers favour them over the softmax warps sharing their
+// sub-partitions: the kernel's critical path runs through the MMA lanes.
 // TMEM columns: S [0,128) shared by the slots, O0 [192,336), O1 [352,496);
 // columns 128 and 129 of O_s hold the tile's row sums, which the softmax
 // reads and clears after each PV.  P of each slot is a 128B-swizzled tile in
@@ -58,9 +62,10 @@ namespace vc {
 namespace {
 
 constexpr int NS = 4;          // K/V/mean pipeline stages
-constexpr int NTHREADS = 352;  // 8 softmax warps + TMA warp + one MMA warp per slot
-constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;    // + slot
+constexpr int NTHREADS = 384;  // one MMA warp per slot, TMA warp, idle warp, 8 softmax warps
+constexpr int WARP_MMA = 0;    // + slot
+constexpr int WARP_TMA = 2;
+constexpr int WARP_SOFTMAX = 4;
 constexpr int CTA_ROWS = 256;
 
 // TMEM columns
@@ -353,9 +358,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mma_commit(bar(B_FIN + s));
       if (!mbar_wait(bar(B_FIN + s), 0, abort, WAIT_NS) && !*abort) record_timeout(p, abort);
     }
-  } else {
+  } else if (warp >= WARP_SOFTMAX) {
     // ------------------------------------------------------ softmax warps
-    const int slot = warp >> 2;
+    const int slot = (warp - WARP_SOFTMAX) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int64_t row = static_cast<int64_t>(q0) + slot * 128 + r;
