@@ -155,6 +155,11 @@ __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+__device__ __forceinline__ float set_ge(float a, float b) {
+  float d;
+  asm("set.ge.f32.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -165,7 +170,10 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // one little-endian word of E4M3 bytes:
 //   t' = fma(x, A', B')              = t/256 exactly, t = fmaf(x, A, C - m);
 //   u  = sat(t' 2^29 + 1 - 7.5 2^21) = 1 iff t >= 7.5 (iff rint(t) >= 8),
-//        else 0 (t' 2^29 is an integer whenever t is near 7.5);
+//        else 0 (t' 2^29 is an integer whenever t is near 7.5); for the
+//        odd scores the same u comes from set.ge(t', 7.5/256), a compare on
+//        the ALU pipe, so that the FMA and ALU pipes carry about the same
+//        work per four scores (10 issue cycles each);
 //   f  = fma(t', u, 49152)           = 49152 + rint(t)/256 (ulp 2^-8, ties
 //        to even) or 49152 when u = 0, so the low byte of f's bits is the
 //        code.
@@ -177,8 +185,9 @@ __device__ __forceinline__ uint32_t expcast4(float x0, float x1, float x2, float
   const float2 A2 = make_float2(A, A), B2 = make_float2(B, B);
   const float2 t01 = __ffma2_rn(make_float2(x0, x1), A2, B2);
   const float2 t23 = __ffma2_rn(make_float2(x2, x3), A2, B2);
-  const float2 u01 = make_float2(fma_sat(t01.x, S29, K29), fma_sat(t01.y, S29, K29));
-  const float2 u23 = make_float2(fma_sat(t23.x, S29, K29), fma_sat(t23.y, S29, K29));
+  constexpr float T75 = 0.029296875f;  // 7.5 / 256
+  const float2 u01 = make_float2(fma_sat(t01.x, S29, K29), set_ge(t01.y, T75));
+  const float2 u23 = make_float2(fma_sat(t23.x, S29, K29), set_ge(t23.y, T75));
   const float2 M = make_float2(49152.0f, 49152.0f);
   const float2 f01 = __ffma2_rn(t01, u01, M);
   const float2 f23 = __ffma2_rn(t23, u23, M);
