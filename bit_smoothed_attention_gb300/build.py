@@ -23,6 +23,7 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relax
 UNITS = {
     "vcattn_api.cu": [],
     "group.cu": ["--fmad=false"],
+    "km_tc.cu": ["--fmad=false"],
     "prep.cu": ["--fmad=false"],
     "attn.cu": [],
     "prep_noalloc.cu": [],

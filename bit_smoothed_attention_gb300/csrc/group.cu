@@ -7,7 +7,8 @@
 // and the permutation are bit-for-bit reproducible:
 //   assign : h_c = 0.5f * (fmaf chain over d of c_c[d]^2); dot = one fmaf
 //            chain over d = 0..127 ascending; score = dot - h_c; the lowest
-//            cluster with the largest score wins.
+//            cluster with the largest score wins (km_tc.cu: tensor-core
+//            scores with an exact fallback).
 //   update : per 512-token chunk, the members of each cluster are added in
 //            token order to a +0 partial; partials are added in chunk order
 //            to a +0 total; centroid = total / (float)count (IEEE division);
@@ -40,199 +41,6 @@ __global__ void km_init(const uint16_t* __restrict__ V, int64_t N, int k, float*
   for (int c = 0; c < k; ++c) {
     const int64_t j = (static_cast<int64_t>(c) * N) / k;
     cent[(bh * k + c) * D + d] = bf16f(V[(bh * N + j) * D + d]);
-  }
-}
-
-// Assign: each thread scores TT tokens against all clusters, accumulators in
-// registers; centroids live in shared memory transposed [d][c] so one 16-byte
-// broadcast load feeds 4 x TT FMAs (as packed fma.rn.f32x2 pairs, each two
-// IEEE fmafs).  Clusters c >= k get h = +inf and never
-// win.  grid (ceil(N / (256*TT)), BH), block 256.
-template <int KC, int TT>
-__global__ void __launch_bounds__(256) km_assign(const uint16_t* __restrict__ V, int64_t N, int k,
-                                                 const float* __restrict__ cent,
-                                                 int32_t* __restrict__ labels) {
-  __shared__ __align__(16) float cT[D][KC];
-  __shared__ float hs[KC];
-  const int64_t bh = blockIdx.y;
-  const float* cb = cent + bh * k * D;
-  for (int i = threadIdx.x; i < D * KC; i += blockDim.x) {
-    const int d = i / KC, c = i % KC;
-    cT[d][c] = c < k ? cb[c * D + d] : 0.0f;
-  }
-  __syncthreads();
-  if (threadIdx.x < KC) {
-    const int c = threadIdx.x;
-    if (c < k) {
-      float acc = 0.0f;
-      for (int d = 0; d < D; ++d) acc = __fmaf_rn(cT[d][c], cT[d][c], acc);
-      hs[c] = 0.5f * acc;
-    } else {
-      hs[c] = __int_as_float(0x7f800000);  // +inf
-    }
-  }
-  __syncthreads();
-
-  const uint16_t* vb = V + bh * N * D;
-  int64_t j[TT];
-  bool ok[TT];
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    j[t] = static_cast<int64_t>(blockIdx.x) * (256 * TT) + t * 256 + threadIdx.x;
-    ok[t] = j[t] < N;
-  }
-  // accumulators in cluster pairs: one packed fma.rn.f32x2 is two IEEE fmafs
-  float2 acc[TT][KC / 2];
-#pragma unroll
-  for (int t = 0; t < TT; ++t)
-#pragma unroll
-    for (int c = 0; c < KC / 2; ++c) acc[t][c] = make_float2(0.0f, 0.0f);
-
-  // V is streamed 8 channels at a time; the next 8 are loaded while the
-  // current ones are used (software pipelining hides the load latency).
-  uint4 nxt[TT];
-#pragma unroll
-  for (int t = 0; t < TT; ++t)
-    nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D) : make_uint4(0, 0, 0, 0);
-#pragma unroll 1
-  for (int d0 = 0; d0 < D; d0 += 8) {
-    float vv[TT][8];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) unpack8(nxt[t], vv[t]);
-    if (d0 + 8 < D) {
-#pragma unroll
-      for (int t = 0; t < TT; ++t)
-        nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D + d0 + 8) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int dd = 0; dd < 8; ++dd) {
-#pragma unroll
-      for (int c4 = 0; c4 < KC / 4; ++c4) {
-        const float4 cc = *reinterpret_cast<const float4*>(&cT[d0 + dd][4 * c4]);
-#pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          const float2 v2 = make_float2(vv[t][dd], vv[t][dd]);
-          acc[t][2 * c4] = __ffma2_rn(v2, make_float2(cc.x, cc.y), acc[t][2 * c4]);
-          acc[t][2 * c4 + 1] = __ffma2_rn(v2, make_float2(cc.z, cc.w), acc[t][2 * c4 + 1]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    if (!ok[t]) continue;
-    int best = 0;
-    float bs = acc[t][0].x - hs[0];
-#pragma unroll
-    for (int c = 1; c < KC; ++c) {
-      const float sc = ((c & 1) ? acc[t][c >> 1].y : acc[t][c >> 1].x) - hs[c];
-      if (sc > bs) {
-        bs = sc;
-        best = c;
-      }
-    }
-    labels[bh * N + j[t]] = best;
-  }
-}
-
-// Assign, split variant: a thread scores TT tokens against CH of the KC
-// clusters (KC/CH lanes share a token group), so one 16-byte centroid load
-// feeds 4 x TT FMAs with TT = 4.  The per-lane winners are combined with
-// shuffles: larger score wins, equal scores keep the lower cluster (the
-// lower lane), which is the lowest-index rule of the sequential scan.
-// grid (ceil(N / (256 / (KC/CH) * TT)), BH), block 256.
-template <int KC, int CH, int TT>
-__global__ void __launch_bounds__(256) km_assign_split(const uint16_t* __restrict__ V, int64_t N,
-                                                       int k, const float* __restrict__ cent,
-                                                       int32_t* __restrict__ labels) {
-  constexpr int LPG = KC / CH;          // lanes per token group
-  constexpr int GROUPS = 256 / LPG;     // token groups per CTA
-  __shared__ __align__(16) float cT[D][KC];
-  __shared__ float hs[KC];
-  const int64_t bh = blockIdx.y;
-  const float* cb = cent + bh * k * D;
-  for (int i = threadIdx.x; i < D * KC; i += blockDim.x) {
-    const int d = i / KC, c = i % KC;
-    cT[d][c] = c < k ? cb[c * D + d] : 0.0f;
-  }
-  __syncthreads();
-  if (threadIdx.x < KC) {
-    const int c = threadIdx.x;
-    if (c < k) {
-      float acc = 0.0f;
-      for (int d = 0; d < D; ++d) acc = __fmaf_rn(cT[d][c], cT[d][c], acc);
-      hs[c] = 0.5f * acc;
-    } else {
-      hs[c] = __int_as_float(0x7f800000);  // +inf
-    }
-  }
-  __syncthreads();
-  const int part = threadIdx.x % LPG;   // which CH clusters
-  const int grp = threadIdx.x / LPG;
-  const int c0 = part * CH;
-  const uint16_t* vb = V + bh * N * D;
-  int64_t j[TT];
-  bool ok[TT];
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    j[t] = static_cast<int64_t>(blockIdx.x) * (GROUPS * TT) + t * GROUPS + grp;
-    ok[t] = j[t] < N;
-  }
-  float2 acc[TT][CH / 2];  // cluster pairs (packed fma.rn.f32x2)
-#pragma unroll
-  for (int t = 0; t < TT; ++t)
-#pragma unroll
-    for (int c = 0; c < CH / 2; ++c) acc[t][c] = make_float2(0.0f, 0.0f);
-  uint4 nxt[TT];
-#pragma unroll
-  for (int t = 0; t < TT; ++t)
-    nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D) : make_uint4(0, 0, 0, 0);
-#pragma unroll 1
-  for (int d0 = 0; d0 < D; d0 += 8) {
-    float vv[TT][8];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) unpack8(nxt[t], vv[t]);
-    if (d0 + 8 < D) {
-#pragma unroll
-      for (int t = 0; t < TT; ++t)
-        nxt[t] = ok[t] ? *reinterpret_cast<const uint4*>(vb + j[t] * D + d0 + 8) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int dd = 0; dd < 8; ++dd) {
-#pragma unroll
-      for (int c4 = 0; c4 < CH / 4; ++c4) {
-        const float4 cc = *reinterpret_cast<const float4*>(&cT[d0 + dd][c0 + 4 * c4]);
-#pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          const float2 v2 = make_float2(vv[t][dd], vv[t][dd]);
-          acc[t][2 * c4] = __ffma2_rn(v2, make_float2(cc.x, cc.y), acc[t][2 * c4]);
-          acc[t][2 * c4 + 1] = __ffma2_rn(v2, make_float2(cc.z, cc.w), acc[t][2 * c4 + 1]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    int best = c0;
-    float bs = acc[t][0].x - hs[c0];
-#pragma unroll
-    for (int c = 1; c < CH; ++c) {
-      const float sc = ((c & 1) ? acc[t][c >> 1].y : acc[t][c >> 1].x) - hs[c0 + c];
-      if (sc > bs) {
-        bs = sc;
-        best = c0 + c;
-      }
-    }
-#pragma unroll
-    for (int m = 1; m < LPG; m <<= 1) {
-      const float os = __shfl_xor_sync(0xffffffffu, bs, m);
-      const int ob = __shfl_xor_sync(0xffffffffu, best, m);
-      if (os > bs || (os == bs && ob < best)) {
-        bs = os;
-        best = ob;
-      }
-    }
-    if (ok[t] && part == 0) labels[bh * N + j[t]] = best;
   }
 }
 
@@ -364,23 +172,6 @@ __global__ void __launch_bounds__(UPD_CHUNK) sort_scatter(const int32_t* __restr
   if (c >= 0) perm[bh * N + offs[(bh * nchunk + g) * k + c] + wc[warp][c] + rank] = static_cast<int32_t>(j);
 }
 
-template <int KC, int CH, int TT>
-cudaError_t assign_split(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
-                         int32_t* labels, cudaStream_t s) {
-  constexpr int GROUPS = 256 / (KC / CH);
-  const dim3 grid(static_cast<unsigned>(ceil_div(N, GROUPS * TT)), static_cast<unsigned>(BH));
-  km_assign_split<KC, CH, TT><<<grid, 256, 0, s>>>(V, N, k, cent, labels);
-  return cudaGetLastError();
-}
-
-template <int KC, int TT>
-cudaError_t assign(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
-                   int32_t* labels, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>(ceil_div(N, 256 * TT)), static_cast<unsigned>(BH));
-  km_assign<KC, TT><<<grid, 256, 0, s>>>(V, N, k, cent, labels);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws) {
@@ -410,10 +201,7 @@ cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int it
   if (e != cudaSuccess) return e;
   const dim3 gchunk(nchunk, static_cast<unsigned>(BH));
   for (int it = 0; it < iters; ++it) {
-    if (k <= 8) e = assign<8, 8>(V, BH, N, k, cent, labels, s);
-    else if (k <= 16) e = assign<16, 8>(V, BH, N, k, cent, labels, s);
-    else if (k <= 32) e = assign<32, 4>(V, BH, N, k, cent, labels, s);
-    else e = assign_split<64, 32, 4>(V, BH, N, k, cent, labels, s);
+    e = launch_km_assign_tc(V, BH, N, k, cent, labels, err, s);
     if (e != cudaSuccess) return e;
     km_partial<<<gchunk, D, 0, s>>>(V, labels, N, k, nchunk, ws.part, ws.cnt, err);
     km_finalize<<<dim3(k, static_cast<unsigned>(BH)), D, 0, s>>>(ws.part, ws.cnt, nchunk, k, cent);

@@ -29,6 +29,10 @@ struct GroupWs {
   int32_t* offs;  // [BH, nchunk, k]
 };
 size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws);
+// Tensor-core k-means assignment with an exact FP32 fallback (km_tc.cu);
+// 1 <= k <= 64.
+cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
+                                int32_t* labels, uint32_t* err, cudaStream_t s);
 cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
                          int32_t* labels, int32_t* perm, float* centroids_out, const GroupWs& ws,
                          uint32_t* err, cudaStream_t s);

@@ -1,0 +1,396 @@
+// k-means assignment on the tensor core, with an exact fallback
+// ("VC-Attention: Value Smoothing and Softmax Casting for Low-bit
+// Attention", Key Contribution 1: the online k-means of V-Smooth).
+//
+// The label of token j is the lowest cluster c with the largest
+//   score_c = fl(chain_c - h_c),  chain_c = fmaf chain over d = 0..127 of
+//   v_d c_{c,d} from +0,  h_c = 0.5f * (fmaf chain of c_{c,d}^2),
+// the same definition as the FP32-core assign.  Here the tensor core first
+// computes an approximation T_c of every score:
+//   c = hi + lo (two bf16 parts, |c - hi - lo| <= 2^-18 |c|), v exact in
+//   bf16, h = h1 + h2 + h3 (three bf16 parts, exact to 2^-24 |h|);
+//   T = v . hi + v . lo - (h1 + h2 + h3) as one kind::f16 MMA chain with
+//   FP32 accumulation (M = 128 tokens, N = 64 clusters, K = 2 x 128 + 16,
+//   the last K step a constant operand of ones against -h).
+// |T_c - score_c| <= 2^-14 (|v| |c| + |h_c|) + 2^-23 |T_c|: the products
+// are exact; the accumulation of 272 terms, even with every add truncating,
+// errs by at most 272 x 2^-23 < 2^-14.9 of the sum of their magnitudes; the
+// FP32 chain and the split add 2^-17 and 2^-18 of |v| |c|, the final
+// subtraction 2^-24 |score|; and sum_d |v_d c_d| <= |v| |c|.  With the
+// token's E = (2^-13 + 2^-21) (|v| max|c| + max|h|), at least twice that,
+// and m = max_c T_c, the winner w has T_w >= score_w - E/2 >= score_c* -
+// E/2 >= m - E (c* the argmax of T).  So clusters with T_c < m - E cannot
+// win.
+// When one cluster is left it is the label; otherwise the exact chains of
+// the remaining candidates decide, lowest index first on ties.  The labels
+// are those of the FP32 definition, bit for bit, whatever the data; on the
+// live workload about 0.3% of the tokens take the exact path.
+//
+// CTA: up to KT_TPC consecutive 128-token tiles of one (b, h).  Warps 0-3:
+// one thread per token (= TMEM lane) for the selection; warp 4: TMA; warp 5:
+// MMA lane.  V tiles (bf16, two 64-channel K chunks, 128B swizzle) through a
+// ring of KT_NS stages; the scores T in two TMEM buffers of 64 columns.
+// Compiled with --fmad=false: only the explicit __fmaf_rn calls fuse.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace vc {
+namespace {
+
+constexpr int KT_NS = 2;            // V stages
+constexpr int KT_THREADS = 192;     // 4 selection warps, TMA warp, MMA warp
+constexpr int KT_WARP_TMA = 4;
+constexpr int KT_WARP_MMA = 5;
+constexpr uint32_t V_HALF = 128 * 128;       // 128 tokens x 64 bf16 channels
+constexpr uint32_t V_STAGE = 2 * V_HALF;     // one 128-token tile
+constexpr uint32_t CP_CHUNK = 64 * 128;      // 64 clusters x 64 bf16 channels
+constexpr uint32_t SM_V = 0;
+constexpr uint32_t SM_CP = SM_V + KT_NS * V_STAGE;  // [part][K chunk]
+constexpr uint32_t SM_AB = SM_CP + 4 * CP_CHUNK;    // A of the bias step: 128 rows of (1, 1, 1, 0, ...)
+constexpr uint32_t SM_BB = SM_AB + 128 * 32;        // B of the bias step: 64 rows of (-h1, -h2, -h3, 0, ...)
+constexpr uint32_t SM_H = SM_BB + 64 * 32;          // h_c
+constexpr uint32_t SM_CN = SM_H + 64 * 4;           // [0]: max |c|, [1]: max |h|
+enum { KB_FULL = 0, KB_EMPTY = KT_NS, KB_DFULL = 2 * KT_NS, KB_DEMPTY = 2 * KT_NS + 2, KB_FIN = 2 * KT_NS + 4, KB_N };
+constexpr uint32_t SM_BAR = SM_CN + 64 * 4;
+constexpr uint32_t SM_TSLOT = SM_BAR + KB_N * 8;
+constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
+constexpr uint32_t KT_SMEM = SM_ABORT + 8 + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t IDESC_KM = idesc(FMT_BF16, FMT_BF16, 128, 64);
+constexpr uint64_t KT_WAIT_NS = 2000000000ull;
+
+// Byte offset of element e (0..63) of row r in a 128-byte-row, 128B-swizzled
+// K-major tile: 8-row atoms of 1 KiB, 16-byte chunk q stored at q ^ (r & 7).
+__device__ __forceinline__ uint32_t sw128(int r, int e) {
+  const int byte = 2 * e;
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
+}
+
+// Byte offset of element e (0..15) of row r in a K = 16 bf16 operand in the
+// interleaved no-swizzle layout (core matrices of 8 rows x 16 bytes, the
+// two K halves 128 bytes apart, 8-row groups 256 bytes apart).
+__device__ __forceinline__ uint32_t k16(int r, int e) {
+  return static_cast<uint32_t>((r >> 3) * 256 + (e >> 3) * 128 + (r & 7) * 16 + (e & 7) * 2);
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, int r, int e) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + sw128(r, e))) << 16);
+}
+
+__global__ void __launch_bounds__(KT_THREADS, 2)
+    km_assign_tc(const __grid_constant__ CUtensorMap tmv, int64_t N, int k, int tpc, const float* __restrict__ cent,
+                 int32_t* __restrict__ labels, uint32_t* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  auto bar = [&](int i) { return sb + SM_BAR + 8u * static_cast<uint32_t>(i); };
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + SM_ABORT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t bh = blockIdx.y;
+  const int64_t ntile_all = (N + 127) / 128;
+  const int64_t tile0 = static_cast<int64_t>(blockIdx.x) * tpc;
+  const int ntl = static_cast<int>(ntile_all - tile0 < tpc ? ntile_all - tile0 : tpc);
+  const float* cb = cent + bh * k * D;
+  float* hs = reinterpret_cast<float*>(sm + SM_H);
+  float* cn = reinterpret_cast<float*>(sm + SM_CN);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < KT_NS; ++s) {
+      mbar_init(bar(KB_FULL + s), 1);
+      mbar_init(bar(KB_EMPTY + s), 5);  // the MMA lane's commit + the 4 selection warps
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(KB_DFULL + b), 1);
+      mbar_init(bar(KB_DEMPTY + b), 4);
+    }
+    mbar_init(bar(KB_FIN), 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  // The FP32 centroids, staged in V stage 0 (not yet in use) with 16-byte
+  // loads, all in flight at once.
+  float* cs = reinterpret_cast<float*>(sm + SM_V);
+  for (int i = threadIdx.x; i < 64 * D / 4; i += KT_THREADS) {
+    const int c = i >> 5;
+    *reinterpret_cast<float4*>(cs + 4 * i) =
+        c < k ? *reinterpret_cast<const float4*>(cb + 4 * i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+  __syncthreads();
+  // B operand: the centroids as bf16 high and low parts (clusters >= k are 0)
+  for (int i = threadIdx.x; i < 64 * D; i += KT_THREADS) {
+    const int c = i >> 7, d = i & (D - 1);
+    const float x = cs[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    const int kc = d >> 6, e = d & 63;
+    *reinterpret_cast<__nv_bfloat16*>(sm + SM_CP + (0 * 2 + kc) * CP_CHUNK + sw128(c, e)) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(sm + SM_CP + (1 * 2 + kc) * CP_CHUNK + sw128(c, e)) = lo;
+  }
+  // the constant A of the bias step
+  for (int i = threadIdx.x; i < 128 * 16; i += KT_THREADS) {
+    const int r = i >> 4, e = i & 15;
+    *reinterpret_cast<__nv_bfloat16*>(sm + SM_AB + k16(r, e)) = __float2bfloat16_rn(e < 3 ? 1.0f : 0.0f);
+  }
+  if (threadIdx.x < 64) {
+    const int c = threadIdx.x;
+    float acc = 0.0f;
+    if (c < k)
+#pragma unroll 16
+      for (int d = 0; d < D; ++d) acc = __fmaf_rn(cs[c * D + d], cs[c * D + d], acc);
+    const float h = 0.5f * acc;
+    hs[c] = h;
+    // B of the bias step: -h in three bf16 parts; clusters >= k get -inf
+    // (their T is -inf and they never become candidates)
+    float hp[3];
+    hp[0] = c < k ? h : __int_as_float(0x7f800000);
+    hp[1] = c < k ? h - __bfloat162float(__float2bfloat16_rn(hp[0])) : 0.0f;
+    hp[2] = c < k ? hp[1] - __bfloat162float(__float2bfloat16_rn(hp[1])) : 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      *reinterpret_cast<__nv_bfloat16*>(sm + SM_BB + k16(c, e)) =
+          __float2bfloat16_rn(e < 3 ? -hp[e] : 0.0f);
+    // max |c| (sqrt(acc) (1 + 2^-16) >= |c|) and max |h| over the k clusters
+    float cm = c < k ? sqrtf(acc) * 1.0000153f : 0.0f, hm = c < k ? fabsf(h) : 0.0f;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, m));
+      hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, m));
+    }
+    if (lane == 0) {
+      cn[2 + warp * 2] = cm;
+      cn[3 + warp * 2] = hm;
+    }
+  }
+  fence_proxy_async_smem();
+  if (warp == KT_WARP_MMA) tmem_alloc(sb + SM_TSLOT, 128);
+  // (V stage 0 is overwritten by TMA only after this barrier)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TSLOT);
+
+  if (warp == KT_WARP_TMA) {
+    if (lane == 0) {
+      for (int t = 0; t < ntl && !*abort; ++t) {
+        const int s = t % KT_NS;
+        if (t >= KT_NS && !mbar_wait(bar(KB_EMPTY + s), ((t / KT_NS) - 1) & 1, abort, KT_WAIT_NS)) {
+          *abort = 1;
+          atomicOr(err, ERR_TIMEOUT);
+          break;
+        }
+        const int row = static_cast<int>((tile0 + t) * 128);
+        mbar_arrive_expect_tx(bar(KB_FULL + s), V_STAGE);
+        tma_load_3d(sb + SM_V + s * V_STAGE, &tmv, 0, row, static_cast<int>(bh), bar(KB_FULL + s));
+        tma_load_3d(sb + SM_V + s * V_STAGE + V_HALF, &tmv, 64, row, static_cast<int>(bh), bar(KB_FULL + s));
+      }
+    }
+  } else if (warp == KT_WARP_MMA) {
+    if (lane == 0) {
+      bool ok = true;
+      const uint64_t dV = sdesc_sw128(sb + SM_V), dC = sdesc_sw128(sb + SM_CP);
+      const uint64_t dAB = sdesc_k8_tf32(sb + SM_AB), dBB = sdesc_k8_tf32(sb + SM_BB);  // 32-byte rows, no swizzle
+      for (int t = 0; t < ntl && ok; ++t) {
+        const int s = t % KT_NS, b = t & 1;
+        ok = mbar_wait(bar(KB_FULL + s), (t / KT_NS) & 1, abort, KT_WAIT_NS);
+        if (ok && t >= 2) ok = mbar_wait(bar(KB_DEMPTY + b), ((t >> 1) - 1) & 1, abort, KT_WAIT_NS);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16(tmem + 64 * b, dV + ((s * V_STAGE + kc * V_HALF + 32 * ks) >> 4),
+                       dC + (((part * 2 + kc) * CP_CHUNK + 32 * ks) >> 4), IDESC_KM,
+                       (part | kc | ks) != 0 ? 1u : 0u);
+        mma_bf16(tmem + 64 * b, dAB, dBB, IDESC_KM, 1u);  // - h_c
+        mma_commit(bar(KB_DFULL + b));
+        mma_commit(bar(KB_EMPTY + s));  // this V stage has been read by the tensor core
+      }
+      if (!ok) {
+        *abort = 1;
+        atomicOr(err, ERR_TIMEOUT);
+      }
+      mma_commit(bar(KB_FIN));
+      if (!mbar_wait(bar(KB_FIN), 0, abort, KT_WAIT_NS) && !*abort) atomicOr(err, ERR_TIMEOUT);
+    }
+  } else {
+    // ---------------------------------------------------- selection warps
+    const int r = warp * 32 + lane;  // token within the tile = TMEM lane
+    // E = EA |v| + EB, with EA = (2^-13 + 2^-21) max|c|, EB = (2^-13 + 2^-21) max|h|
+    const float EA = (1.220703125e-4f + 4.76837158e-7f) * fmaxf(cn[2], cn[4]);
+    const float EB = (1.220703125e-4f + 4.76837158e-7f) * fmaxf(cn[3], cn[5]);
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t FULLM = 0xffffffffu;
+    for (int t = 0; t < ntl; ++t) {
+      const int s = t % KT_NS, b = t & 1;
+      bool ok = __all_sync(FULLM, mbar_wait(bar(KB_FULL + s), (t / KT_NS) & 1, abort, KT_WAIT_NS));
+      ok = ok && __all_sync(FULLM, mbar_wait(bar(KB_DFULL + b), (t >> 1) & 1, abort, KT_WAIT_NS));
+      if (!ok) {
+        if (lane == 0) atomicOr(err, ERR_TIMEOUT);
+        *abort = 1;
+        break;
+      }
+      tc_fence_after();
+      float T[64];
+      {
+        uint32_t (&u0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&T[0]);
+        uint32_t (&u1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&T[32]);
+        tmem_ld32(tmem + lane_addr + 64 * b, u0);
+        tmem_ld32(tmem + lane_addr + 64 * b + 32, u1);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KB_DEMPTY + b));
+
+      const uint8_t* vt = sm + SM_V + s * V_STAGE;
+      const int64_t j = (tile0 + t) * 128 + r;
+      if (j < N) {
+        // |v| from the staged row (an upper bound: the sum's relative error
+        // is far below the factor)
+        float2 q2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 u = *reinterpret_cast<const uint4*>(vt + kc * V_HALF + sw128(r, 8 * ch));
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 v2 = make_float2(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xFFFF0000u));
+              q2 = __ffma2_rn(v2, v2, q2);
+            }
+          }
+        const float vn = sqrtf(q2.x + q2.y) * 1.0000153f;
+        const float E = EA * vn + EB;
+        // m = max_c T_c (eight independent chains), then the candidates
+        float m8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = T[q];
+#pragma unroll
+        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], T[c]);
+        const float m = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        const float thr = m - E;
+        uint32_t cm8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) cm8[q] = 0u;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) cm8[c >> 3] |= (T[c] >= thr ? 1u : 0u) << (c & 7);
+        uint64_t cand = 0;  // bit c: cluster c can still win
+#pragma unroll
+        for (int q = 0; q < 8; ++q) cand |= static_cast<uint64_t>(cm8[q]) << (8 * q);
+        int best = __ffsll(static_cast<long long>(cand)) - 1;
+        if (cand & (cand - 1)) {
+          // exact chains of the candidates, up to four side by side, in
+          // ascending cluster order; the lowest index is kept on ties
+          float bs = 0.0f;
+          bool have = false;
+          uint64_t rest = cand;
+          while (rest) {
+            int cc[4];
+            int n = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              cc[q] = rest ? __ffsll(static_cast<long long>(rest)) - 1 : cc[0];
+              if (rest) {
+                rest &= rest - 1;
+                n = q + 1;
+              }
+            }
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 8
+            for (int d = 0; d < D; ++d) {
+              const float v = bf16_at(vt + (d >> 6) * V_HALF, r, d & 63);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[q] = __fmaf_rn(v, cb[cc[q] * D + d], acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (q < n) {
+                const float e = acc[q] - hs[cc[q]];
+                if (!have || e > bs) {
+                  bs = e;
+                  best = cc[q];
+                  have = true;
+                }
+              }
+            }
+          }
+        }
+        labels[bh * N + j] = best;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(KB_EMPTY + s));  // done reading this V stage
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == KT_WARP_MMA) tmem_dealloc(tmem, 128);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 km_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// V [BH, N, 128] bf16 as a 3-D tensor map with 64 x 128 boxes, 128B swizzle.
+cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
+                                int32_t* labels, uint32_t* err, cudaStream_t s) {
+  if (k < 1 || k > 64) return cudaErrorInvalidValue;
+  auto enc = km_encoder();
+  if (!enc) return cudaErrorInvalidValue;
+  CUtensorMap m;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(V), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(km_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, KT_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  // Tiles per CTA: at most 16 (the per-CTA set-up is amortised over them),
+  // chosen so that the CTAs fill whole waves of two CTAs per SM.
+  static int slots = 0;
+  if (!slots) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    slots = 2 * (sms > 0 ? sms : 1);
+  }
+  const int64_t ntile = (N + 127) / 128;
+  const int64_t total = ntile * BH;
+  const int64_t waves = (total + 16 * slots - 1) / (16 * slots);
+  const int64_t tpc = (total + slots * waves - 1) / (slots * waves);
+  const dim3 grid(static_cast<unsigned>((ntile + tpc - 1) / tpc), static_cast<unsigned>(BH));
+  km_assign_tc<<<grid, KT_THREADS, KT_SMEM, s>>>(m, N, k, static_cast<int>(tpc), cent, labels, err);
+  return cudaGetLastError();
+}
+
+}  // namespace vc
