@@ -44,57 +44,112 @@ __global__ void km_init(const uint16_t* __restrict__ V, int64_t N, int k, float*
   }
 }
 
-// Chunk partial sums: thread d owns channel d of every cluster's partial and
-// adds the chunk's tokens in order.  The V rows are staged through shared
-// memory 32 tokens at a time with coalesced 16-byte loads.  grid (nchunk,
-// BH), block D.
-__global__ void __launch_bounds__(D) km_partial(const uint16_t* __restrict__ V,
-                                                const int32_t* __restrict__ labels, int64_t N,
-                                                int k, int nchunk, float* __restrict__ part,
-                                                int32_t* __restrict__ cnt, uint32_t* err) {
-  constexpr int SEG = 32;  // tokens staged at a time
-  __shared__ float ps[KMAX][D];
-  __shared__ int cs[KMAX];
-  __shared__ __align__(16) uint16_t vs[SEG][D];
-  __shared__ int ls[SEG];
+// Chunk partial sums.  The chunk's tokens are first listed cluster by
+// cluster, each list in ascending token order (a stable counting sort in
+// shared memory: ranks within a warp from __match_any_sync, then a prefix
+// over the warps).  Thread (g, q) then owns clusters 4g .. 4g+3 and channels
+// 8q .. 8q+7: for each cluster it adds the members' rows in list order to a
+// +0 partial, 16-byte loads straight from global memory, several in flight
+// (the 16 threads of a cluster group read a whole 256-byte row).  grid
+// (nchunk, BH), block 256.
+__global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V,
+                                                  const int32_t* __restrict__ labels, int64_t N,
+                                                  int k, int nchunk, float* __restrict__ part,
+                                                  int32_t* __restrict__ cnt, uint32_t* err) {
+  constexpr int NW = UPD_CHUNK / 32;  // 16 warps' worth of tokens, 2 per thread
+  __shared__ int wc[NW][KMAX];        // per-warp counts, then per-warp offsets
+  __shared__ int cstart[KMAX + 1];
+  __shared__ int16_t order[UPD_CHUNK];
   const int64_t bh = blockIdx.y;
   const int g = blockIdx.x;
-  const int d = threadIdx.x;
-  for (int c = 0; c < k; ++c) ps[c][d] = 0.0f;
-  if (d < KMAX) cs[d] = 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t j0 = static_cast<int64_t>(g) * UPD_CHUNK;
-  const int64_t j1 = j0 + UPD_CHUNK < N ? j0 + UPD_CHUNK : N;
-  const uint16_t* vb = V + bh * N * D;
-  const int32_t* lb = labels + bh * N;
-  bool bad = false;
-  for (int64_t s0 = j0; s0 < j1; s0 += SEG) {
-    const int n = static_cast<int>(j1 - s0 < SEG ? j1 - s0 : SEG);
-    __syncthreads();  // previous segment consumed
-    // 32 rows x 256 bytes = 512 16-byte pieces, 4 per thread
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int piece = u * D + d, row = piece >> 4, col = piece & 15;
-      if (row < n)
-        *reinterpret_cast<uint4*>(&vs[row][col * 8]) =
-            *reinterpret_cast<const uint4*>(vb + (s0 + row) * D + col * 8);
-    }
-    if (d < SEG && d < n) ls[d] = lb[s0 + d];
-    __syncthreads();
-    for (int jj = 0; jj < n; ++jj) {
-      const int c = ls[jj];
-      if (static_cast<unsigned>(c) >= static_cast<unsigned>(k)) {
-        bad = true;
-        continue;
-      }
-      ps[c][d] = ps[c][d] + bf16f(vs[jj][d]);
-      if (d == 0) cs[c] += 1;
-    }
-  }
-  if (bad && d == 0) atomicOr(err, ERR_BAD_LABEL);
+  const int n = static_cast<int>(N - j0 < UPD_CHUNK ? N - j0 : UPD_CHUNK);
+  for (int i = tid; i < NW * KMAX; i += 256) wc[i / KMAX][i % KMAX] = 0;
   __syncthreads();
+  // each thread takes tokens tid and tid + 256 (warps w and w + 8 of 32 tokens)
+  int lab[2], rank[2];
+  bool bad = false;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = tid + 256 * h;
+    int c = t < n ? labels[bh * N + j0 + t] : -1;
+    if (c >= 0 && static_cast<unsigned>(c) >= static_cast<unsigned>(k)) {
+      bad = true;
+      c = -1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, c);
+    rank[h] = __popc(same & ((1u << lane) - 1u));
+    if (c >= 0 && rank[h] == 0) wc[warp + 8 * h][c] = __popc(same);
+    lab[h] = c;
+  }
+  if (bad) atomicOr(err, ERR_BAD_LABEL);
+  __syncthreads();
+  if (tid < KMAX) {
+    int run = 0;
+    for (int w = 0; w < NW; ++w) {
+      const int t = wc[w][tid];
+      wc[w][tid] = run;
+      run += t;
+    }
+    cstart[tid] = run;  // count of cluster tid for now
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int c = 0; c < KMAX; ++c) {
+      const int t = cstart[c];
+      cstart[c] = run;
+      run += t;
+    }
+    cstart[KMAX] = run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (lab[h] >= 0) order[cstart[lab[h]] + wc[warp + 8 * h][lab[h]] + rank[h]] = static_cast<int16_t>(tid + 256 * h);
+  __syncthreads();
+  // sums: clusters 4 cg .. 4 cg + 3, channels 8 q .. 8 q + 7
+  const int cg = tid >> 4, q = tid & 15;
+  const uint16_t* vb = V + (bh * N + j0) * D + 8 * q;
   float* pg = part + (bh * nchunk + g) * static_cast<int64_t>(k) * D;
-  for (int c = 0; c < k; ++c) pg[c * D + d] = ps[c][d];
-  if (d < k) cnt[(bh * nchunk + g) * k + d] = cs[d];
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = 4 * cg + cc;
+    if (c >= k) break;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    const int i1 = cstart[c + 1];
+    int i = cstart[c];
+    for (; i + 8 <= i1; i += 8) {
+      uint4 u[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) u[x] = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i + x]) * D);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const uint32_t w4[4] = {u[x].x, u[x].y, u[x].z, u[x].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] = acc[2 * e] + __uint_as_float(w4[e] << 16);
+          acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(w4[e] & 0xFFFF0000u);
+        }
+      }
+    }
+    for (; i < i1; ++i) {
+      const uint4 u = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i]) * D);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[2 * e] = acc[2 * e] + __uint_as_float(w4[e] << 16);
+        acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(w4[e] & 0xFFFF0000u);
+      }
+    }
+    float* dst = pg + c * D + 8 * q;
+    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (q == 0) cnt[(bh * nchunk + g) * k + c] = i1 - cstart[c];
+  }
 }
 
 // Centroid = (partials added in chunk order) / count.  grid (k, BH), block D.
@@ -203,7 +258,7 @@ cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int it
   for (int it = 0; it < iters; ++it) {
     e = launch_km_assign_tc(V, BH, N, k, cent, labels, err, s);
     if (e != cudaSuccess) return e;
-    km_partial<<<gchunk, D, 0, s>>>(V, labels, N, k, nchunk, ws.part, ws.cnt, err);
+    km_partial<<<gchunk, 256, 0, s>>>(V, labels, N, k, nchunk, ws.part, ws.cnt, err);
     km_finalize<<<dim3(k, static_cast<unsigned>(BH)), D, 0, s>>>(ws.part, ws.cnt, nchunk, k, cent);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
