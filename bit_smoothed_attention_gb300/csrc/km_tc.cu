@@ -21,10 +21,13 @@
 // and m = max_c T_c, the winner w has T_w >= score_w - E/2 >= score_c* -
 // E/2 >= m - E (c* the argmax of T).  So clusters with T_c < m - E cannot
 // win.
-// When one cluster is left it is the label; otherwise the exact chains of
-// the remaining candidates decide, lowest index first on ties.  The labels
-// are those of the FP32 definition, bit for bit, whatever the data; on the
-// live workload about 0.3% of the tokens take the exact path.
+// When one cluster is left it is the label.  Otherwise (0.6% of the tokens
+// on the live workload) a second filter computes the candidates' FP32 dot
+// products in eight interleaved partial sums and drops those more than
+// E2 = 2^-15 (|v| max|c| + max|h|) below the best of them (the same
+// argument with a tighter bound); the exact chains of what is left decide,
+// lowest index first on ties.  The labels are those of the FP32 definition,
+// bit for bit, whatever the data.
 //
 // CTA: up to KT_TPC consecutive 128-token tiles of one (b, h).  Warps 0-3:
 // one thread per token (= TMEM lane) for the selection; warp 4: TMA; warp 5:
@@ -225,8 +228,9 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     // ---------------------------------------------------- selection warps
     const int r = warp * 32 + lane;  // token within the tile = TMEM lane
     // E = EA |v| + EB, with EA = (2^-13 + 2^-21) max|c|, EB = (2^-13 + 2^-21) max|h|
-    const float EA = (1.220703125e-4f + 4.76837158e-7f) * fmaxf(cn[2], cn[4]);
-    const float EB = (1.220703125e-4f + 4.76837158e-7f) * fmaxf(cn[3], cn[5]);
+    const float CM = fmaxf(cn[2], cn[4]), HM = fmaxf(cn[3], cn[5]);
+    const float EA = (1.220703125e-4f + 4.76837158e-7f) * CM;
+    const float EB = (1.220703125e-4f + 4.76837158e-7f) * HM;
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t FULLM = 0xffffffffu;
     for (int t = 0; t < ntl; ++t) {
@@ -289,6 +293,50 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
 #pragma unroll
         for (int q = 0; q < 8; ++q) cand |= static_cast<uint64_t>(cm8[q]) << (8 * q);
         int best = __ffsll(static_cast<long long>(cand)) - 1;
+        if ((cand & (cand - 1)) && __popcll(cand) <= 4) {
+          // Second filter: FP32 dot products of the (at most four)
+          // candidates in eight interleaved partial sums; their error vs
+          // the chain is <= (128 + 19) 2^-24 |v| |c| < 2^-16.7 |v| |c|, so
+          // E2 = 2^-15 (|v| max|c| + max|h|) is again at least twice the
+          // difference of the scores.
+          float st[4];
+          int cl[4];
+          float m2 = -__int_as_float(0x7f800000);
+          uint64_t rest = cand;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            cl[i] = rest ? __ffsll(static_cast<long long>(rest)) - 1 : -1;
+            rest = rest ? rest & (rest - 1) : 0;
+            st[i] = -__int_as_float(0x7f800000);
+            if (cl[i] >= 0) {
+              float a8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+              const float* crow = cb + cl[i] * D;
+#pragma unroll 4
+              for (int ch = 0; ch < 16; ++ch) {
+                const uint4 u = *reinterpret_cast<const uint4*>(vt + (ch >> 3) * V_HALF + sw128(r, 8 * (ch & 7)));
+                const float4 c0 = *reinterpret_cast<const float4*>(crow + 8 * ch);
+                const float4 c1 = *reinterpret_cast<const float4*>(crow + 8 * ch + 4);
+                a8[0] = __fmaf_rn(__uint_as_float(u.x << 16), c0.x, a8[0]);
+                a8[1] = __fmaf_rn(__uint_as_float(u.x & 0xFFFF0000u), c0.y, a8[1]);
+                a8[2] = __fmaf_rn(__uint_as_float(u.y << 16), c0.z, a8[2]);
+                a8[3] = __fmaf_rn(__uint_as_float(u.y & 0xFFFF0000u), c0.w, a8[3]);
+                a8[4] = __fmaf_rn(__uint_as_float(u.z << 16), c1.x, a8[4]);
+                a8[5] = __fmaf_rn(__uint_as_float(u.z & 0xFFFF0000u), c1.y, a8[5]);
+                a8[6] = __fmaf_rn(__uint_as_float(u.w << 16), c1.z, a8[6]);
+                a8[7] = __fmaf_rn(__uint_as_float(u.w & 0xFFFF0000u), c1.w, a8[7]);
+              }
+              st[i] = (((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]))) - hs[cl[i]];
+              m2 = fmaxf(m2, st[i]);
+            }
+          }
+          const float thr2 = m2 - 3.0517578125e-5f * (vn * CM + HM);
+          uint64_t c2 = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (cl[i] >= 0 && st[i] >= thr2) c2 |= 1ull << cl[i];
+          cand = c2;
+          best = __ffsll(static_cast<long long>(cand)) - 1;
+        }
         if (cand & (cand - 1)) {
           // exact chains of the candidates, up to four side by side, in
           // ascending cluster order; the lowest index is kept on ties
