@@ -92,6 +92,34 @@ def test_group_degenerate_inputs(vc, orc):
         assert np.array_equal(labels.reshape(1, 300).cpu().numpy(), ol)
 
 
+def test_group_near_ties(vc, orc):
+    """Pairs of initial centroids one bf16 ulp apart in one channel, and
+    tokens repeated from them: most scores of the first iterations differ in
+    the last bits only, so the tensor-core bound keeps several candidates and
+    the FP32 filter and the exact chains decide.  Still bit-exact."""
+    H, N, k = 2, 2048, 16
+    g = torch.Generator(device="cpu")
+    g.manual_seed(4242)
+    V = (torch.randn(1, H, N, 128, generator=g) * 2.0).to(torch.bfloat16)
+    bits = V.view(torch.int16)
+    for c in range(1, k, 2):
+        j0, j1 = (c - 1) * N // k, c * N // k
+        bits[:, :, j1] = bits[:, :, j0]
+        bits[:, :, j1, c % 128] += 1          # one ulp in one channel
+        # copies of the pair, each tied exactly or nearly between the two
+        for r in range(1, 9):
+            bits[:, :, j1 + r] = bits[:, :, j0 if r % 2 else j1]
+    V = V.cuda()
+    labels, perm, cent = vc.group(V, k, 5, centroids=True)
+    torch.cuda.synchronize()
+    ol, oc = orc.kmeans(_bits(V), k, 5)
+    op = orc.stable_sort(ol, k)
+    assert np.array_equal(labels.reshape(H, N).cpu().numpy(), ol)
+    assert np.array_equal(cent.reshape(H, k, 128).cpu().numpy().view(np.uint32), oc.view(np.uint32))
+    assert np.array_equal(perm.reshape(H, N).cpu().numpy(), op)
+    assert vc.last_device_error() == 0
+
+
 # -------------------------------------------------------------------- prep
 PREP_KEYS = ("q8", "k8", "r8t", "q_scale", "k_scale", "v_scale", "k_mean", "v_mean", "qmu")
 
