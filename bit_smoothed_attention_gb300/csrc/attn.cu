@@ -195,6 +195,9 @@ __device__ __forceinline__ uint32_t expcast4(float x0, float x1, float x2, float
               prmt(__float_as_uint(f23.x), __float_as_uint(f23.y), 0x0040u), 0x5410u);
 }
 
+// kMasked: the block-sparse instantiation (a tile mask is given); the dense
+// one compiles without the per-warp skip below.
+template <bool kMasked>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ Params p) {
@@ -428,77 +431,94 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // then are keys masked one by one; a 64-key block that a row does not
       // keep is dropped as a whole (no max contribution, bytes cleared).
       const bool partial = !__all_sync(FULL, kv_lim >= TILE);
+      const bool skip = kMasked && !__any_sync(FULL, keep0 || keep1);
 
       if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS)))) break;
       tc_fence_after();
       float x[128];
-      {
-        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
-        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
-        uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
-        uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
-        tmem_ld32(tS + 0, c0);
-        tmem_ld32(tS + 32, c1);
-        tmem_ld32(tS + 64, c2);
-        tmem_ld32(tS + 96, c3);
-        tmem_wait_ld();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_STAKEN + slot));  // S may be overwritten
-      if (partial) {
-        // keys past N never contribute: -inf for the max
-#pragma unroll
-        for (int j = 0; j < 128; ++j) x[j] = j < kv_lim ? x[j] : NEG_INF;
-      }
-      // four independent max chains (two per 64-key half)
-      float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
-      float mc = fmax3(x[64], x[65], x[66]), md = fmax3(x[96], x[97], x[98]);
-#pragma unroll
-      for (int j = 3; j < 31; j += 2) {
-        ma = fmax3(ma, x[j], x[j + 1]);
-        mb = fmax3(mb, x[32 + j], x[33 + j]);
-        mc = fmax3(mc, x[64 + j], x[65 + j]);
-        md = fmax3(md, x[96 + j], x[97 + j]);
-      }
-      const float mx0 = fmax3(ma, mb, fmaxf(x[31], x[63]));
-      const float mx1 = fmax3(mc, md, fmaxf(x[95], x[127]));
-      const float m_tile = fmaxf(keep0 ? A0 * mx0 : NEG_INF, keep1 ? A1 * mx1 : NEG_INF);
-      const bool need = m_tile > m_run + p.tau8;
-      const float m_new = need ? m_tile : m_run;
-      const bool live = m_new != NEG_INF;
-      const bool resc = need && m_run != NEG_INF;
-      const float alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
-      m_run = m_new;
-
-      // ExpCast -> 32 words of E4M3 bytes.  In the partial tile the -inf
-      // scores are replaced by 0 (keeping the cast finite); the bytes of keys
-      // past N, of dropped blocks, and of a row with no key kept so far are
-      // cleared after the cast (a dropped block's scores are finite, so its
-      // cast is too).
-      if (partial) {
-#pragma unroll
-        for (int j = 0; j < 128; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
-      }
-      const float Bq = live ? (p.C - m_new) * 0.00390625f : 0.0f;
-      const float A0q = A0 * 0.00390625f, A1q = A1 * 0.00390625f;
       uint32_t w[32];  // the row's 128 E4M3 bytes
+      float m_new, alpha;
+      bool resc;
+      if (kMasked && skip) {
+        // This warp's query tile keeps neither 64-key block of the tile (its
+        // 32 rows share one query tile): no score is needed, the bytes are
+        // 0 and the maximum stays; only the barrier protocol runs.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_STAKEN + slot));
 #pragma unroll
-      for (int q = 0; q < 32; ++q)
-        w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q, Bq);
-      const bool k0 = live && keep0, k1 = live && keep1;
-      if (partial || !__all_sync(FULL, k0 && k1)) {
-        const int64_t lim0 = k0 ? (kv_lim < 64 ? kv_lim : 64) : 0;
-        const int64_t lim1 = k1 ? (kv_lim < 128 ? kv_lim : 128) : 64;
+        for (int q = 0; q < 32; ++q) w[q] = 0u;
+        m_new = m_run;
+        resc = false;
+        alpha = 1.0f;
+      } else {
+        {
+          uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
+          uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
+          uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
+          uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
+          tmem_ld32(tS + 0, c0);
+          tmem_ld32(tS + 32, c1);
+          tmem_ld32(tS + 64, c2);
+          tmem_ld32(tS + 96, c3);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_STAKEN + slot));  // S may be overwritten
+        if (partial) {
+          // keys past N never contribute: -inf for the max
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          uint32_t keep = 0;
+          for (int j = 0; j < 128; ++j) x[j] = j < kv_lim ? x[j] : NEG_INF;
+        }
+        // four independent max chains (two per 64-key half)
+        float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
+        float mc = fmax3(x[64], x[65], x[66]), md = fmax3(x[96], x[97], x[98]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (4 * q + e < (q < 16 ? lim0 : lim1)) keep |= 0xFFu << (8 * e);
-          w[q] &= keep;
+        for (int j = 3; j < 31; j += 2) {
+          ma = fmax3(ma, x[j], x[j + 1]);
+          mb = fmax3(mb, x[32 + j], x[33 + j]);
+          mc = fmax3(mc, x[64 + j], x[65 + j]);
+          md = fmax3(md, x[96 + j], x[97 + j]);
+        }
+        const float mx0 = fmax3(ma, mb, fmaxf(x[31], x[63]));
+        const float mx1 = fmax3(mc, md, fmaxf(x[95], x[127]));
+        const float m_tile = fmaxf(keep0 ? A0 * mx0 : NEG_INF, keep1 ? A1 * mx1 : NEG_INF);
+        const bool need = m_tile > m_run + p.tau8;
+        m_new = need ? m_tile : m_run;
+        const bool live = m_new != NEG_INF;
+        resc = need && m_run != NEG_INF;
+        alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
+
+        // ExpCast -> 32 words of E4M3 bytes.  In the partial tile the -inf
+        // scores are replaced by 0 (keeping the cast finite); the bytes of keys
+        // past N, of dropped blocks, and of a row with no key kept so far are
+        // cleared after the cast (a dropped block's scores are finite, so its
+        // cast is too).
+        if (partial) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
+        }
+        const float Bq = live ? (p.C - m_new) * 0.00390625f : 0.0f;
+        const float A0q = A0 * 0.00390625f, A1q = A1 * 0.00390625f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q, Bq);
+        const bool k0 = live && keep0, k1 = live && keep1;
+        if (partial || !__all_sync(FULL, k0 && k1)) {
+          const int64_t lim0 = k0 ? (kv_lim < 64 ? kv_lim : 64) : 0;
+          const int64_t lim1 = k1 ? (kv_lim < 128 ? kv_lim : 128) : 64;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            uint32_t keep = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * q + e < (q < 16 ? lim0 : lim1)) keep |= 0xFFu << (8 * e);
+            w[q] &= keep;
+          }
         }
       }
+      m_run = m_new;
       if (i > 0) {
         // PV(i-1) done (and with it the mean term of tile i-2): P may be
         // overwritten and the row sums of tile i-1 are final.
@@ -679,12 +699,17 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   p.debug_flags = a.debug_flags;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const dim3 grid(static_cast<unsigned>(ceil_div(Np, CTA_ROWS)), static_cast<unsigned>(a.BH));
-  attn_fwd<<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+  if (p.mask)
+    attn_fwd<true><<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+  else
+    attn_fwd<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
