@@ -48,6 +48,15 @@
 // mean operand of t-1 is written already multiplied by the factor.
 // tcgen05 operations of one thread complete in issue order, so "PV(t-1)
 // done" implies that MEAN(t-2) is done.
+//
+// A KV tile is two 64-key blocks, one per 64-column half of S and P.  Dense,
+// tile t holds blocks 2t and 2t+1 (one 128-row TMA box of K and of V).  With
+// a tile mask, the CTA streams only the blocks that at least one of its four
+// query 64-tiles keeps, in ascending order, two per tile: K arrives as two
+// 64-row boxes, V as two 64-key boxes in the 64B-swizzled layout (each half
+// of the PV B operand has its own indicator row), and the mean tile as two
+// 2 KiB halves.  A softmax warp whose query tile keeps neither block of a
+// tile skips its scores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -75,6 +84,7 @@ constexpr uint32_t COL_L = 128;    // row sums inside O_s
 
 constexpr uint32_t TILE_BYTES = 16384;    // 128 x 128 E4M3
 constexpr uint32_t V_STAGE = 18432;       // V tile + 16 indicator rows
+constexpr uint32_t V_HALF = 9216;         // masked: 144 x 64 keys per block (64B swizzle)
 constexpr uint32_t MU_BYTES = 4096;       // 128 x 8 tf32
 constexpr uint32_t SM_Q = 0;
 constexpr uint32_t SM_K = SM_Q + 2 * TILE_BYTES;
@@ -100,6 +110,13 @@ constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
 constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
 constexpr uint32_t SM_END = SM_ABORT + 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;  // slack for 1024-byte alignment
+// Masked: one bit per 64-key block, set when any of the CTA's query tiles
+// keeps it (the first 32 * KEPT_WORDS blocks; later ones are looked up in the
+// mask itself).
+constexpr uint32_t SM_KEPT = SM_END;
+constexpr int KEPT_WORDS = 448;
+constexpr uint32_t SMEM_BYTES_MASKED = SMEM_BYTES + 4 * KEPT_WORDS;
+static_assert(SMEM_BYTES_MASKED <= 232448, "shared memory per CTA");
 
 constexpr uint32_t IDESC_QK = idesc(FMT_E4M3, FMT_E4M3, 128, 128);
 constexpr uint32_t IDESC_PV = idesc(FMT_E4M3, FMT_E4M3, 128, 144);
@@ -127,17 +144,27 @@ struct Params {
   int debug_flags;
 };
 
-// Does the CTA process KV tile t?  (Any of its query 64-tiles keeps either
-// 64-block of the tile.)
-__device__ __forceinline__ bool tile_kept(const Params& p, int64_t bh, int qt0, int t) {
-  if (!p.mask) return true;
-  const uint8_t* mrow = p.mask + (bh * p.nq64) * p.nbp;
+// Does any of the CTA's four query 64-tiles keep 64-key block b?
+__device__ __forceinline__ bool block_kept(const Params& p, int64_t bh, int qt0, int b) {
+  const uint8_t* mcol = p.mask + (bh * p.nq64) * p.nbp + b;
+  bool kept = false;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int qt = qt0 + q;
-    if (qt < p.nq64 && (mrow[qt * p.nbp + 2 * t] | mrow[qt * p.nbp + 2 * t + 1])) return true;
+    kept |= qt < p.nq64 && mcol[static_cast<int64_t>(qt) * p.nbp] != 0;
   }
-  return false;
+  return kept;
+}
+
+// The kept-union bits of blocks 32w .. 32w+31 read from the mask itself (for
+// blocks beyond the shared-memory bitmask; out of line, it is never hot).
+__device__ __noinline__ uint32_t kept_word_slow(const Params& p, int64_t bh, int qt0, int w) {
+  uint32_t m = 0;
+  for (int e = 0; e < 32; ++e) {
+    const int b = 32 * w + e;
+    if (b < p.nbp && block_kept(p, bh, qt0, b)) m |= 1u << e;
+  }
+  return m;
 }
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort) {
@@ -232,14 +259,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_fence_init();
   }
   // Indicator rows 128..143 of every V stage (B operand rows of the PV MMA,
-  // 128B-swizzled K-major): row 128 = 1.0 on keys 0..63, row 129 = 1.0 on
-  // keys 64..127, rows 130..143 = 0.  TMA writes only rows 0..127.
-  for (int c = threadIdx.x; c < NS * 16 * 8; c += NTHREADS) {
-    const int st = c >> 7, n = (c >> 3) & 15, k = c & 7;  // stage, row, 16-key chunk
-    const uint32_t one4 = 0x38383838u;                    // four E4M3 1.0 bytes
-    const uint32_t v = ((n == 0 && k < 4) || (n == 1 && k >= 4)) ? one4 : 0u;
-    *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + TILE_BYTES + n * 128 + ((k ^ (n & 7)) * 16)) =
-        make_uint4(v, v, v, v);
+  // K-major): row 128 = 1.0 on keys 0..63, row 129 = 1.0 on keys 64..127,
+  // rows 130..143 = 0.  TMA writes only rows 0..127.  Dense: one
+  // 128B-swizzled tile; masked: one 64B-swizzled tile per 64-key half (the
+  // rows are uniform, so the swizzle does not move them).
+  const uint32_t one4 = 0x38383838u;  // four E4M3 1.0 bytes
+  if constexpr (kMasked) {
+    for (int c = threadIdx.x; c < NS * 2 * 16 * 4; c += NTHREADS) {
+      const int st = c >> 7, h = (c >> 6) & 1, n = (c >> 2) & 15, k = c & 3;  // stage, half, row, chunk
+      const uint32_t v = n == h ? one4 : 0u;
+      *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + h * V_HALF + 8192 + n * 64 + k * 16) =
+          make_uint4(v, v, v, v);
+    }
+  } else {
+    for (int c = threadIdx.x; c < NS * 16 * 8; c += NTHREADS) {
+      const int st = c >> 7, n = (c >> 3) & 15, k = c & 7;  // stage, row, 16-key chunk
+      const uint32_t v = ((n == 0 && k < 4) || (n == 1 && k >= 4)) ? one4 : 0u;
+      *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + TILE_BYTES + n * 128 + ((k ^ (n & 7)) * 16)) =
+          make_uint4(v, v, v, v);
+    }
+  }
+  // Masked: the union bitmask of the blocks the CTA's query tiles keep.
+  uint32_t* kept_w = reinterpret_cast<uint32_t*>(sm + SM_KEPT);
+  const int nkw = (p.nbp + 31) >> 5;
+  if (kMasked) {
+    for (int w = warp; w < nkw && w < KEPT_WORDS; w += NTHREADS / 32) {
+      const int b = 32 * w + lane;
+      const uint32_t m = __ballot_sync(0xffffffffu, b < p.nbp && block_kept(p, bh, qt0, b));
+      if (lane == 0) kept_w[w] = m;
+    }
   }
   fence_proxy_async_smem();
   if (warp == WARP_MMA) tmem_alloc(sb + SM_TSLOT, 512);
@@ -248,52 +296,87 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TSLOT);
 
-  // Number of KV tiles this CTA processes (the same in every role).
-  int ntiles = p.ntile;
-  if (p.mask) {
-    ntiles = 0;
-    for (int t = 0; t < p.ntile; ++t) ntiles += tile_kept(p, bh, qt0, t) ? 1 : 0;
-  }
-
-  // the next kept KV tile after t (-1: none)
-  auto next_tile = [&](int t) {
-    for (int u = t + 1; u < p.ntile; ++u)
-      if (tile_kept(p, bh, qt0, u)) return u;
+  // KV tiles as block pairs (x, y): dense (2t, 2t+1); masked, the kept
+  // blocks two by two, y = -1 for the empty second half of an odd last tile;
+  // x = -1 past the last tile.  Every role walks the same sequence.
+  auto kept_word = [&](int w) -> uint32_t {  // bits of blocks 32w .. 32w+31 (0 past nbp)
+    return w < KEPT_WORDS ? kept_w[w] : kept_word_slow(p, bh, qt0, w);
+  };
+  auto next_kept = [&](int b) {
+    for (int u = b + 1; u < p.nbp; u = (u | 31) + 1) {
+      const uint32_t m = kept_word(u >> 5) >> (u & 31);
+      if (m) return u + __ffs(static_cast<int>(m)) - 1;
+    }
     return -1;
   };
+  auto pair_after = [&](int b) -> int2 {  // the tile that starts after block b
+    if constexpr (kMasked) {
+      const int x = next_kept(b);
+      return make_int2(x, x >= 0 ? next_kept(x) : -1);
+    } else {
+      return b + 2 < p.nbp ? make_int2(b + 1, b + 2) : make_int2(-1, -1);
+    }
+  };
+  auto next_pair = [&](int2 pr) { return pr.y < 0 ? make_int2(-1, -1) : pair_after(pr.y); };
+
+  // Number of KV tiles this CTA processes (the same in every role).
+  int ntiles = p.ntile;
+  if constexpr (kMasked) {
+    int nb = 0;
+    for (int w = 0; w < nkw; ++w) nb += __popc(kept_word(w));
+    ntiles = (nb + 1) >> 1;
+  }
 
   if (warp == WARP_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !(p.debug_flags & 1) && ntiles > 0) {
-      // Q and the first kept K tile
-      int t = next_tile(-1);
+      const int h3 = static_cast<int>(bh);
+      const float* mu = p.vmu_op + bh * p.nbp * (4 * D);  // 2 KiB per block
+      // K of a tile: one 128-row box, or (masked) a 64-row box per block
+      auto load_k = [&](uint32_t dst, int2 pr, uint32_t b) {
+        tma_load_3d(dst, &tmk, 0, pr.x * BLK, h3, b);
+        if constexpr (kMasked) tma_load_3d(dst + TILE_BYTES / 2, &tmk, 0, (pr.y >= 0 ? pr.y : pr.x) * BLK, h3, b);
+      };
+      // V and the mean tile of a tile.  An empty second half is filled with
+      // the first block again (finite bytes; its P bytes and row sums are 0).
+      auto load_v = [&](int st, int2 pr, uint32_t b) {
+        const uint32_t dv = sb + SM_V + st * V_STAGE, dm = sb + SM_MU + st * MU_BYTES;
+        tma_load_3d(dv, &tmv, pr.x * BLK, 0, h3, b);
+        if constexpr (kMasked) {
+          const int y = pr.y >= 0 ? pr.y : pr.x;
+          tma_load_3d(dv + V_HALF, &tmv, y * BLK, 0, h3, b);
+          bulk_load(dm, mu + pr.x * (4 * D), MU_BYTES / 2, b);
+          bulk_load(dm + MU_BYTES / 2, mu + y * (4 * D), MU_BYTES / 2, b);
+        } else {
+          bulk_load(dm, mu + pr.x * (4 * D), MU_BYTES, b);
+        }
+      };
+      // Q and the first K tile
+      int2 pr = pair_after(-1);
       mbar_arrive_expect_tx(bar(B_QFULL), 3 * TILE_BYTES);
-      tma_load_3d(sb + SM_Q, &tmq, 0, q0, static_cast<int>(bh), bar(B_QFULL));
-      tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, static_cast<int>(bh), bar(B_QFULL));
-      tma_load_3d(sb + SM_K, &tmk, 0, t * TILE, static_cast<int>(bh), bar(B_QFULL));
+      tma_load_3d(sb + SM_Q, &tmq, 0, q0, h3, bar(B_QFULL));
+      tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, h3, bar(B_QFULL));
+      load_k(sb + SM_K, pr, bar(B_QFULL));
       // Step j brings V(j) and its mean tile into stage j % NS and K(j+1)
       // into K stage (j+1) % NS, all on one barrier.  A K stage is free again
       // once both slots' QK have read it, a V stage once both mean terms of
       // its tile were issued.
-      for (int j = 0; t >= 0 && !*abort; ++j) {
+      for (int j = 0; pr.x >= 0 && !*abort; ++j) {
         const int st = j % NS, stk = (j + 1) % NS;
-        const int tn = next_tile(t);
+        const int2 pn = next_pair(pr);
         if (j >= NS && !mbar_wait(bar(B_VEMPTY + st), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
-        if (tn >= 0 && j + 1 >= NS &&
+        if (pn.x >= 0 && j + 1 >= NS &&
             !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / NS) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
-        mbar_arrive_expect_tx(bar(B_FULL + st), TILE_BYTES + MU_BYTES + (tn >= 0 ? TILE_BYTES : 0));
-        tma_load_3d(sb + SM_V + st * V_STAGE, &tmv, t * TILE, 0, static_cast<int>(bh), bar(B_FULL + st));
-        bulk_load(sb + SM_MU + st * MU_BYTES, p.vmu_op + (bh * p.ntile + t) * 1024, MU_BYTES,
-                  bar(B_FULL + st));
-        if (tn >= 0)
-          tma_load_3d(sb + SM_K + stk * TILE_BYTES, &tmk, 0, tn * TILE, static_cast<int>(bh), bar(B_FULL + st));
-        t = tn;
+        mbar_arrive_expect_tx(bar(B_FULL + st), TILE_BYTES + MU_BYTES + (pn.x >= 0 ? TILE_BYTES : 0));
+        load_v(st, pr, bar(B_FULL + st));
+        if (pn.x >= 0) load_k(sb + SM_K + stk * TILE_BYTES, pn, bar(B_FULL + st));
+        pr = pn;
       }
     }
   } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
@@ -307,8 +390,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Descriptors are built once; a byte offset o advances them by o >> 4
       // in the start-address field (all of shared memory is below 256 KiB).
       const uint64_t dQ = sdesc_sw128(sb + SM_Q + s * TILE_BYTES), dK = sdesc_sw128(sb + SM_K);
-      const uint64_t dV = sdesc_sw128(sb + SM_V);
-      const uint64_t dL = sdesc_k8_tf32(sb + SM_L + s * MU_BYTES), dMu = sdesc_k8_tf32(sb + SM_MU);
+      const uint64_t dV = kMasked ? sdesc_sw64(sb + SM_V) : sdesc_sw128(sb + SM_V);
+      const uint64_t dL = sdesc_k8_tf32(sb + SM_L + s * MU_BYTES);
+      // mean tile: K-slots 0..3 (block of the first half) and 4..7 (second
+      // half) are two 2 KiB parts of 16-byte rows, one row per channel
+      const uint64_t dMu = sdesc(sb + SM_MU, MU_BYTES / 2, 128, 0);
       const uint64_t dP = sdesc_sw128(sb + SM_P + s * TILE_BYTES);
       const uint32_t dO = tmem + COL_O + 160 * s;
       auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
@@ -337,9 +423,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_commit(bar(B_VEMPTY + (j - 1) % NS));  // this slot is done with V(j-1)
         }
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f8(dO, adv(dP, 32 * kk), adv(dV, (j % NS) * V_STAGE + 32 * kk), IDESC_PV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t vo = kMasked ? (kk >> 1) * V_HALF + 32 * (kk & 1) : 32 * kk;
+          mma_f8(dO, adv(dP, 32 * kk), adv(dV, (j % NS) * V_STAGE + vo), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit(bar(B_ODONE + s));
       };
       for (int i = 0; ok && i <= ntiles; ++i) {
@@ -401,36 +488,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       l0 = __uint_as_float(ls0);
       l1 = __uint_as_float(ls1);
     };
-    // tf32 A operand row of the mean restoration, [hi0, lo0, hi0, hi1 | lo1, hi1, 0, 0]
+    // tf32 A operand row of the mean restoration, [hi0, lo0, hi0, 0 | hi1, lo1, hi1, 0]
+    // against the mean tile's (hi, hi, lo, 0) of each half's block
     auto put_lrow = [&](float v0, float v1) {
       const float h0 = to_tf32(v0), h1 = to_tf32(v1);
       const float g0 = to_tf32(v0 - h0), g1 = to_tf32(v1 - h1);
-      *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, h1);
-      *reinterpret_cast<float4*>(Lrow + 128) = make_float4(g1, h1, 0.0f, 0.0f);
+      *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, 0.0f);
+      *reinterpret_cast<float4*>(Lrow + 128) = make_float4(h1, g1, h1, 0.0f);
       fence_proxy_async_smem();
     };
     float m_run = NEG_INF;
     float l = 0.0f;
     bool ok = true;
     int i = 0;
-    int t = next_tile(-1);
-    // block scales and mask bytes of the current tile, loaded one tile ahead
-    float2 ks = t >= 0 ? *reinterpret_cast<const float2*>(ksc + 2 * t) : make_float2(0.0f, 0.0f);
-    uint8_t mk0 = (t >= 0 && mrow) ? mrow[2 * t] : 0, mk1 = (t >= 0 && mrow) ? mrow[2 * t + 1] : 0;
-    for (; t >= 0; ++i) {
-      const int tn = next_tile(t);
-      const float2 ks_n = tn >= 0 ? *reinterpret_cast<const float2*>(ksc + 2 * tn) : make_float2(0.0f, 0.0f);
-      const uint8_t mk0_n = (tn >= 0 && mrow) ? mrow[2 * tn] : 0;
-      const uint8_t mk1_n = (tn >= 0 && mrow) ? mrow[2 * tn + 1] : 0;
-      const bool keep0 = row_ok && (!p.mask || mk0 != 0);
-      const bool keep1 = row_ok && (!p.mask || mk1 != 0);
-      const int64_t kv_lim = p.N - static_cast<int64_t>(t) * TILE;  // valid keys in the tile
+    // block scales and mask bytes of a tile
+    auto pair_scales = [&](int2 pr) -> float2 {
+      if (pr.x < 0) return make_float2(0.0f, 0.0f);
+      if constexpr (kMasked) return make_float2(ksc[pr.x], pr.y >= 0 ? ksc[pr.y] : 0.0f);
+      else return *reinterpret_cast<const float2*>(ksc + pr.x);
+    };
+    auto mask_byte = [&](int b) -> uint8_t { return (kMasked && mrow && b >= 0) ? mrow[b] : 0; };
+    int2 pr = pair_after(-1);
+    // loaded one tile ahead
+    float2 ks = pair_scales(pr);
+    uint8_t mk0 = mask_byte(pr.x), mk1 = mask_byte(pr.y);
+    for (; pr.x >= 0; ++i) {
+      const int2 pn = next_pair(pr);
+      const float2 ks_n = pair_scales(pn);
+      const uint8_t mk0_n = mask_byte(pn.x), mk1_n = mask_byte(pn.y);
+      const bool keep0 = row_ok && (!kMasked || mk0 != 0);
+      const bool keep1 = row_ok && (!kMasked || mk1 != 0);
+      // Score column j of the tile is a valid key iff j < lim_lo (first
+      // half) or j < lim_hi (second half); dense, both are N - 128 t.
+      const int n32 = static_cast<int>(p.N);
+      const int lim_lo = n32 - pr.x * BLK;
+      const int lim_hi = pr.y >= 0 ? BLK + n32 - pr.y * BLK : BLK;
       const float A0 = a_i * ks.x;
       const float A1 = a_i * ks.y;
-      // Warp-uniform: does the tile run past N (the last tile only)?  Only
-      // then are keys masked one by one; a 64-key block that a row does not
-      // keep is dropped as a whole (no max contribution, bytes cleared).
-      const bool partial = !__all_sync(FULL, kv_lim >= TILE);
+      // Warp-uniform: does the tile hold keys past N (the last block of the
+      // sequence, or an empty second half)?  Only then are keys masked one
+      // by one; a 64-key block that a row does not keep is dropped as a
+      // whole (no max contribution, bytes cleared).
+      const bool partial = !__all_sync(FULL, lim_lo >= BLK && lim_hi >= TILE);
       const bool skip = kMasked && !__any_sync(FULL, keep0 || keep1);
 
       if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS)))) break;
@@ -469,7 +568,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (partial) {
           // keys past N never contribute: -inf for the max
 #pragma unroll
-          for (int j = 0; j < 128; ++j) x[j] = j < kv_lim ? x[j] : NEG_INF;
+          for (int j = 0; j < 128; ++j) x[j] = j < (j < 64 ? lim_lo : lim_hi) ? x[j] : NEG_INF;
         }
         // four independent max chains (two per 64-key half)
         float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
@@ -490,24 +589,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         resc = need && m_run != NEG_INF;
         alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
 
-        // ExpCast -> 32 words of E4M3 bytes.  In the partial tile the -inf
-        // scores are replaced by 0 (keeping the cast finite); the bytes of keys
-        // past N, of dropped blocks, and of a row with no key kept so far are
-        // cleared after the cast (a dropped block's scores are finite, so its
-        // cast is too).
+        // ExpCast -> 32 words of E4M3 bytes.  A dropped block, and a row with
+        // no key kept so far, cast with A = B = 0: t = 0, every code 0 (the
+        // scores are finite).  In the partial tile the -inf scores are
+        // replaced by 0 and the bytes of keys past N are cleared after the
+        // cast.
         if (partial) {
 #pragma unroll
           for (int j = 0; j < 128; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
         }
-        const float Bq = live ? (p.C - m_new) * 0.00390625f : 0.0f;
-        const float A0q = A0 * 0.00390625f, A1q = A1 * 0.00390625f;
+        const bool k0 = live && keep0, k1 = live && keep1;
+        const float Bq = (p.C - m_new) * 0.00390625f;
+        const float A0q = k0 ? A0 * 0.00390625f : 0.0f, B0q = k0 ? Bq : 0.0f;
+        const float A1q = k1 ? A1 * 0.00390625f : 0.0f, B1q = k1 ? Bq : 0.0f;
 #pragma unroll
         for (int q = 0; q < 32; ++q)
-          w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q, Bq);
-        const bool k0 = live && keep0, k1 = live && keep1;
-        if (partial || !__all_sync(FULL, k0 && k1)) {
-          const int64_t lim0 = k0 ? (kv_lim < 64 ? kv_lim : 64) : 0;
-          const int64_t lim1 = k1 ? (kv_lim < 128 ? kv_lim : 128) : 64;
+          w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q,
+                          q < 16 ? B0q : B1q);
+        if (partial) {
+          const int lim0 = k0 ? (lim_lo < 64 ? lim_lo : 64) : 0;
+          const int lim1 = k1 ? (lim_hi < 128 ? lim_hi : 128) : 64;
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
             uint32_t keep = 0;
@@ -567,7 +668,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
-      t = tn;
+      pr = pn;
       ks = ks_n;
       mk0 = mk0_n;
       mk1 = mk1_n;
@@ -653,16 +754,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-// 3-D u8 tensor map, 128 x 128 box, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
+// 3-D u8 tensor map with a box of b0 x b1 bytes: 128-byte swizzle for
+// 128-byte box rows, 64-byte swizzle for 64-byte rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+              uint32_t b1) {
   auto enc = get_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {d0, d0 * d1};
-  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t box[3] = {b0, b1, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, b0 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -670,9 +773,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   const int64_t Np = npad(a.N);
+  // Masked, K and V come one 64-key block per box.
+  const uint32_t kb = a.mask ? 64 : 128;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q8, D, Np, a.BH) || !make_map(&mk, a.k8, D, Np, a.BH) ||
-      !make_map(&mv, a.r8t, Np, D, a.BH))
+  if (!make_map(&mq, a.q8, D, Np, a.BH, 128, 128) || !make_map(&mk, a.k8, D, Np, a.BH, 128, kb) ||
+      !make_map(&mv, a.r8t, Np, D, a.BH, kb, 128))
     return cudaErrorInvalidValue;
   Params p{};
   p.q_scale = a.q_scale;
@@ -701,13 +806,13 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_MASKED);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const dim3 grid(static_cast<unsigned>(ceil_div(Np, CTA_ROWS)), static_cast<unsigned>(a.BH));
   if (p.mask)
-    attn_fwd<true><<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+    attn_fwd<true><<<grid, NTHREADS, SMEM_BYTES_MASKED, s>>>(mq, mk, mv, p);
   else
     attn_fwd<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();

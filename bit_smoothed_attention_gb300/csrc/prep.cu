@@ -438,27 +438,17 @@ __global__ void __launch_bounds__(256) prep_quant(
       dst[1] = src[1];
     }
     // ---- mean operand of the rank-one restoration MMA ----
-    // B[k][n = d] of a [K = 8] x [N = 128] tf32 operand, K-major, no swizzle:
-    // k = 3h, 3h+1, 3h+2 hold (hi, hi, lo) of mu_b[d] / v_scale[d] for the
-    // block's half h of its 128-key tile; k = 6, 7 are zero.
+    // One 16-byte row per channel d: (hi, hi, lo, 0) of mu_b[d] / v_scale[d],
+    // K-slots 0..3 of the [K = 8] x [N = 128] tf32 B operand for whichever
+    // half of a 128-key tile the block lands in (2 KiB per block, so the
+    // mean tile of any two blocks is two contiguous copies).
     if (threadIdx.x < D) {
       const int d = threadIdx.x;
       const float mud = pad_block ? 0.0f : v_mean[(bh * nbp + b) * D + d];
       const float u = mud / v_scale[bh * D + d];
       const float hi = to_tf32(u);
       const float lo = to_tf32(u - hi);
-      const int h = static_cast<int>(b & 1);
-      float* tile = vmu_op + (bh * (Npad / TILE) + (b >> 1)) * 1024;
-      auto at = [&](int kk) -> float& {
-        return tile[((d >> 3) * 256 + (kk >> 2) * 128 + (d & 7) * 16 + (kk & 3) * 4) / 4];
-      };
-      at(3 * h) = hi;
-      at(3 * h + 1) = hi;
-      at(3 * h + 2) = lo;
-      if (h == 1) {
-        at(6) = 0.0f;
-        at(7) = 0.0f;
-      }
+      reinterpret_cast<float4*>(vmu_op + (bh * nbp + b) * (4 * D))[d] = make_float4(hi, hi, lo, 0.0f);
     }
     __syncthreads();  // tb and this stage are reused by the next block
   }

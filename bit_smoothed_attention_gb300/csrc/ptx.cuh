@@ -82,7 +82,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ------------------------------------------------------------------ tcgen05
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1 (bit 46), swizzle
-// mode in bits 61-63 (0 = none, 2 = 128-byte).
+// mode in bits 61-63 (0 = none, 2 = 128-byte, 4 = 64-byte).
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
                                           uint32_t swizzle) {
   uint64_t d = 0;
@@ -95,6 +95,8 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 // K-major operand tile with 128-byte rows in the 128B-swizzled layout.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) { return sdesc(saddr, 16, 1024, 2); }
+// K-major operand tile with 64-byte rows in the 64B-swizzled layout (mode 4).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) { return sdesc(saddr, 16, 512, 4); }
 // K-major operand of 32-byte rows (8 tf32) in the interleaved no-swizzle
 // layout: core matrices of 8 rows x 16 bytes, K-neighbours 128 bytes apart,
 // 8-row groups 256 bytes apart.

@@ -83,7 +83,7 @@ size_t prepped_layout(const vcattn_shape* s, void* base, vcattn_prepped* out) {
   p.k_mean = reinterpret_cast<float*>(take(size_t(BH) * D * 4));
   p.v_mean = reinterpret_cast<float*>(take(size_t(BH) * nbp * D * 4));
   p.qmu = reinterpret_cast<float*>(take(size_t(BH) * N * 4));
-  p.vmu_op = reinterpret_cast<float*>(take(size_t(BH) * (Np / vc::TILE) * 1024 * 4));
+  p.vmu_op = reinterpret_cast<float*>(take(size_t(BH) * (Np / vc::BLK) * vc::D * 4 * 4));
   if (out) *out = p;
   return off;
 }

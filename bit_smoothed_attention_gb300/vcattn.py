@@ -174,7 +174,7 @@ class Prepped:
             k_mean=v("k_mean", (B * H, 128), torch.float32),
             v_mean=v("v_mean", (B * H, nbp, 128), torch.float32),
             qmu=v("qmu", (B * H, N), torch.float32),
-            vmu_op=v("vmu_op", (B * H, Np // 128, 1024), torch.float32))
+            vmu_op=v("vmu_op", (B * H, nbp, 128, 4), torch.float32))
 
 
 def prep(Q, K, V, perm=None, out=None, stream=None):

@@ -71,9 +71,9 @@ typedef struct {
  *   k_mean  [B,H,D]       f32 mu_K, the FP32 sequence mean of K
  *   v_mean  [B,H,nbp,D]   f32 mu_b, the FP32 mean of each permuted 64-block of V
  *   qmu     [B,H,N]       f32 q . mu_K (restores the true LSE)
- *   vmu_op  [B,H,Npad/128,1024] f32 the block means divided by v_scale,
- *           split into tf32 high and low parts, laid out as the B operand of
- *           the mean-restoration MMA (one 4 KiB tile per 128 keys).
+ *   vmu_op  [B,H,nbp,D,4] f32 the block means divided by v_scale, split
+ *           into tf32 parts (hi, hi, lo, 0) per channel: one 2 KiB half of
+ *           the B operand of the mean-restoration MMA per 64-key block.
  * vcattn_prepped_carve() fills this struct from one buffer of
  * vcattn_prepped_bytes() bytes. */
 typedef struct {

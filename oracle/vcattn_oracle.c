@@ -41,6 +41,7 @@
 #define ORC_D 128
 #define ORC_BLK 64        /* quantisation / mean block (tokens)            */
 #define ORC_TILE 128      /* KV tile of the online-softmax recurrence      */
+#define ORC_GROUP 256     /* query rows that share one sequence of KV tiles */
 #define ORC_UPD_CHUNK 512 /* token chunk of the centroid-sum order (R4)    */
 
 /* ------------------------------------------------------------------ */
@@ -424,17 +425,22 @@ int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int3
 /* [P3 Key Contributions 1-2; P2 Changes (partial tiles, empty           */
 /* selections, log2-LSE)]                                                */
 /* ------------------------------------------------------------------ */
-/* Per head, for each requested query i (original order), KV tiles of 128
- * permuted keys (two 64-blocks) in ascending order, kept ones only:
+/* Per head, for each requested query i (original order), a sequence of KV
+ * tiles of two permuted 64-key blocks (b_0, b_1) (R9): the query rows go in
+ * groups of 256 (four 64-row tiles); a group's blocks are, in ascending
+ * order, those that any of its four tiles keeps (all blocks when dense),
+ * taken two per tile, and an odd last tile has no second block.  Dense, tile
+ * t is (2t, 2t+1).  Per tile, with the keys of the blocks the row's own tile
+ * keeps:
  *   x_ij  = sum_d dec(q8_id) dec(k8_jd), exact then rounded to FP32;
  *   a_i   = fl(c0 * q_scale[i/64]),  c0 = fl(8 log2(e) sm_scale);
- *   A_h   = fl(a_i * k_scale[2t+h]),  h = half of the tile;
+ *   A_h   = fl(a_i * k_scale[b_h]),  h = half of the tile;
  *   m_tile= max_h fl(A_h * max_{valid j in h} x_ij);
  *   rescale when m_tile > fl(m_run + tau8): m_run = m_tile and the running
  *   sums are multiplied by 2^((m_old - m_tile)/8) (R9);
  *   code  = ExpCast(x_ij, A_h, fl(C - m_run)), p = dec(code) (R7);
  *   l_h   = sum of p over the half (R10);
- *   acc  += sum_j p * (v_scale . dec(r8_j))  +  sum_h l_h mu_{2t+h}
+ *   acc  += sum_j p * (v_scale . dec(r8_j))  +  sum_h l_h mu_{b_h}
  *           (the rank-one mean restoration);   l += l_0 + l_1.
  *   O_i   = acc / l;  lse2_i = m_run/8 - off + log2(l) + qmu_i sm_scale log2(e)
  *   (R11); a row with no kept key gets O = 0, lse2 = -inf.
@@ -454,7 +460,7 @@ int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
                   double* O, double* lse2) {
   const int64_t Npad = ((N + ORC_TILE - 1) / ORC_TILE) * ORC_TILE;
   const int64_t nbp = Npad / ORC_BLK;
-  const int64_t ntile = Npad / ORC_TILE;
+  const int64_t nq64 = (N + ORC_BLK - 1) / ORC_BLK;
   const float c0 = (float)(8.0 * 1.4426950408889634 * (double)sm_scale);
   const float C = (float)(56.0 + 8.0 * off - 8.0 * orc_expcast_cstar());
   double dk[256];
@@ -468,17 +474,29 @@ int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
     double l = 0.0;
     float m_run = -INFINITY;
     const float a_i = c0 * q_scale[i / ORC_BLK];
-    for (int64_t t = 0; t < ntile; ++t) {
+    /* the blocks of the row's group, in ascending order */
+    int64_t* grp = (int64_t*)malloc((size_t)(nbp > 0 ? nbp : 1) * sizeof(int64_t));
+    int64_t ng = 0;
+    const int64_t qt0 = (i / ORC_GROUP) * (ORC_GROUP / ORC_BLK);
+    for (int64_t b = 0; b < nbp; ++b) {
+      int in = mask == NULL;
+      for (int64_t qt = qt0; qt < qt0 + ORC_GROUP / ORC_BLK && qt < nq64 && !in; ++qt)
+        in = mask[qt * nbp + b] != 0;
+      if (in) grp[ng++] = b;
+    }
+    for (int64_t t = 0; 2 * t < ng; ++t) {
+      const int64_t blk[2] = {grp[2 * t], 2 * t + 1 < ng ? grp[2 * t + 1] : -1};
       int kept[2];
       for (int h = 0; h < 2; ++h)
-        kept[h] = mask ? mask[(i / ORC_BLK) * nbp + 2 * t + h] != 0 : 1;
+        kept[h] = blk[h] >= 0 && (mask ? mask[(i / ORC_BLK) * nbp + blk[h]] != 0 : 1);
       if (!kept[0] && !kept[1]) continue;
-      float A[2], mx[2] = {-INFINITY, -INFINITY};
-      for (int h = 0; h < 2; ++h) A[h] = a_i * k_scale[2 * t + h];
+      float A[2] = {0.0f, 0.0f}, mx[2] = {-INFINITY, -INFINITY};
+      for (int h = 0; h < 2; ++h)
+        if (kept[h]) A[h] = a_i * k_scale[blk[h]];
       for (int jj = 0; jj < ORC_TILE; ++jj) {
-        int64_t j = t * ORC_TILE + jj;
         int h = jj / ORC_BLK;
-        valid[jj] = (j < N) && kept[h];
+        int64_t j = blk[h] * ORC_BLK + jj % ORC_BLK;
+        valid[jj] = kept[h] && (j < N);
         if (!valid[jj]) continue;
         double s = 0.0;
         for (int d = 0; d < ORC_D; ++d) s += dk[q8[i * ORC_D + d]] * dk[k8[j * ORC_D + d]];
@@ -486,7 +504,9 @@ int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
         xs[jj] = (double)(float)s;            /* FP32, as accumulated in hardware */
         if ((float)s > mx[h]) mx[h] = (float)s;
       }
-      float m_tile = fmaxf(A[0] * mx[0], A[1] * mx[1]);
+      float m_tile = -INFINITY;
+      for (int h = 0; h < 2; ++h)
+        if (kept[h]) m_tile = fmaxf(m_tile, A[h] * mx[h]);
       if (m_tile == -INFINITY) continue;                 /* nothing valid */
       if (m_tile > m_run + tau8) {
         double alpha = m_run == -INFINITY ? 0.0 : exp2(((double)m_run - (double)m_tile) / 8.0);
@@ -498,13 +518,13 @@ int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
       double lh[2] = {0.0, 0.0};
       for (int jj = 0; jj < ORC_TILE; ++jj) {
         if (!valid[jj]) continue;
-        int64_t j = t * ORC_TILE + jj;
         int h = jj / ORC_BLK;
+        int64_t j = blk[h] * ORC_BLK + jj % ORC_BLK;
         double pv;
         if (flags & 1) {
           /* exact score: FP64 coefficient, no FP32 rounding of A */
           double z = 8.0 * 1.4426950408889634 * (double)sm_scale * (double)q_scale[i / ORC_BLK] *
-                     (double)k_scale[2 * t + h] * xs64[jj];
+                     (double)k_scale[blk[h]] * xs64[jj];
           pv = exp2((double)off + (z - (double)m_run) / 8.0);
         } else {
           pv = dk[orc_expcast_byte((float)xs[jj], A[h], B)];
@@ -520,11 +540,13 @@ int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
       }
       if (!(flags & 2))
         for (int h = 0; h < 2; ++h) {
-          const float* mu = v_mean + (2 * t + h) * ORC_D;
+          if (!kept[h]) continue;
+          const float* mu = v_mean + blk[h] * ORC_D;
           for (int d = 0; d < ORC_D; ++d) acc[d] += lh[h] * (double)mu[d];
         }
       l += lh[0] + lh[1];
     }
+    free(grp);
     if (l > 0.0) {
       for (int d = 0; d < ORC_D; ++d) O[qi * ORC_D + d] = acc[d] / l;
       lse2[qi] = (double)m_run / 8.0 - off + log2(l) + (double)qmu[i] * (double)sm_scale * 1.4426950408889634;

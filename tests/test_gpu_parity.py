@@ -228,6 +228,25 @@ def test_attn_mask_parity(vc, orc):
     assert np.all(g32[192:256] == 0) and np.all(np.isneginf(res[0][2][192:256]))
 
 
+@pytest.mark.parametrize("kind", ["even", "odd", "one", "ones"])
+def test_attn_mask_structures(vc, orc, kind):
+    """Masks whose kept blocks pair up differently from the dense tiles: every
+    other block (the odd ones include the partial last block), a single block
+    (an odd tile count with an empty second half), and every block."""
+    N, H = 1000, 1
+    nq, nbp = (N + 63) // 64, vc.npad(N) // 64
+    mask = np.zeros((1, H, nq, nbp), np.uint8)
+    if kind == "even":
+        mask[..., 0::2] = 1
+    elif kind == "odd":
+        mask[..., 1::2] = 1
+    elif kind == "one":
+        mask[..., 5] = 1
+    else:
+        mask[:] = 1
+    _check_attn(_attn_case(vc, orc, N, H, 8, 403, mask=mask))
+
+
 def test_fwd_equals_prep_then_attn(vc):
     N, H = 700, 2
     Q, K, V = _inputs(1, H, N, 8, 501)

@@ -446,6 +446,60 @@ def test_emul_mask_and_empty_rows(orc):
     assert np.allclose(lq[fin], lse2[fin], atol=1e-9)
 
 
+@pytest.mark.parametrize("tau8", [0.0, 6.0])
+def test_emul_mask_schedule_pairs_group_blocks(orc, tau8):
+    """With a mask, the rows of a 256-row group (four query tiles) visit the
+    blocks that any of the group's tiles keeps, two per KV tile in ascending
+    order.  When all four tiles keep the same four blocks, the group's rows
+    equal the unmasked emulation of a 256-token problem cut down to those
+    blocks (whose tiles are then (S0, S1), (S2, S3)); the masks of other
+    groups do not matter, and a mask that keeps everything is no mask."""
+    N = 1024
+    Q, K, V = _small_inputs(N=N, H=1, seed=60)
+    labels, _ = orc.kmeans(V, 4, 2)
+    perm = orc.stable_sort(labels, 4)
+    pp = orc.prep(Q, K, V, perm)
+    nq = nbp = N // 64
+    rng = np.random.default_rng(61)
+    mask = (rng.random((nq, nbp)) < 0.3).astype(np.uint8)
+    S, g = [1, 4, 5, 9], 2
+    qt = np.arange(4 * g, 4 * g + 4)
+    mask[qt, :] = 0
+    mask[np.ix_(qt, S)] = 1
+    O, L = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=mask)
+    rows = np.arange(256 * g, 256 * g + 256)
+    keys = np.concatenate([np.arange(64 * b, 64 * b + 64) for b in S])
+    sub = {"q8": pp["q8"][:, rows], "k8": pp["k8"][:, keys], "r8t": pp["r8t"][:, :, keys],
+           "q_scale": pp["q_scale"][:, qt], "k_scale": pp["k_scale"][:, S],
+           "v_scale": pp["v_scale"], "k_mean": pp["k_mean"], "v_mean": pp["v_mean"][:, S],
+           "qmu": pp["qmu"][:, rows]}
+    O2, L2 = orc.attn_emul(sub, 0, 256, SM, tau8=tau8)
+    assert np.array_equal(O[rows], O2) and np.array_equal(L[rows], L2)
+    # the tiles (2t, 2t+1) of the unmasked layout give a different answer
+    # here, so the comparison above decides the schedule
+    sub_cons = dict(sub, k8=pp["k8"][:, :256], r8t=pp["r8t"][:, :, :256])
+    assert not np.array_equal(O2, orc.attn_emul(sub_cons, 0, 256, SM, tau8=tau8)[0])
+    m3 = mask.copy()
+    m3[: 4 * g] = 1 - m3[: 4 * g]
+    O3, L3 = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=m3)
+    assert np.array_equal(O3[rows], O[rows]) and np.array_equal(L3[rows], L[rows])
+    # The grouping is by the group's union, not by each row's own blocks:
+    # tile 12 keeps {1, 4}; with tile 13 keeping {2, 7} the group's tiles are
+    # (1, 2), (4, 7), without it (1, 4), and tile 12's rows see the difference.
+    ma = mask.copy()
+    ma[12:16, :] = 0
+    ma[12, [1, 4]] = 1
+    mb = ma.copy()
+    mb[13, [2, 7]] = 1
+    ra = np.arange(12 * 64, 13 * 64)
+    Oa = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=ma, qidx=ra)[0]
+    Ob = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=mb, qidx=ra)[0]
+    assert not np.array_equal(Oa, Ob)
+    Of, Lf = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=np.ones((nq, nbp), np.uint8))
+    Od, Ld = orc.attn_emul(pp, 0, N, SM, tau8=tau8)
+    assert np.array_equal(Of, Od) and np.array_equal(Lf, Ld)
+
+
 def test_emul_expcast_within_prop31(orc):
     """With ExpCast on, every row stays within (3.6368% + tail) * diam(V) of
     the exact-exponential row (Proposition 3.1's output bound)."""
