@@ -27,6 +27,7 @@ UNITS = {
     "prep.cu": ["--fmad=false"],
     "attn.cu": [],
     "prep_noalloc.cu": [],
+    "fwd_host.cu": [],
 }
 HEADERS = ["internal.h", "ptx.cuh"]
 

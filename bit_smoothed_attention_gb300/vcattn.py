@@ -75,6 +75,11 @@ def _lib():
         lib.vcattn_fwd_workspace_bytes.argtypes = [SP]
         lib.vcattn_fwd.restype = st
         lib.vcattn_fwd.argtypes = [SP, P, P, P, P, ctypes.c_float, P, P, P, P, sz, P]
+        lib.vcattn_fwd_host_workspace_bytes.restype = sz
+        lib.vcattn_fwd_host_workspace_bytes.argtypes = [SP, ctypes.c_int, ctypes.c_int]
+        lib.vcattn_fwd_host.restype = st
+        lib.vcattn_fwd_host.argtypes = [SP, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_float, P, P, P,
+                                        ctypes.c_int, P, sz, ctypes.POINTER(P)]
         lib.vcattn_last_device_error.restype = st
         lib.vcattn_last_device_error.argtypes = [P]
         lib.vcattn_status_string.restype = ctypes.c_char_p
@@ -226,6 +231,51 @@ def fwd(Q, K, V, perm, sm_scale, mask=None, O=None, lse2=None, ws=None, stream=N
                              _ptr(mask), _ptr(O), _ptr(lse2), _ptr(ws), ws.numel(), _stream(stream)),
            "vcattn_fwd")
     return O, lse2
+
+
+class HostPipeline:
+    """vcattn_fwd_host with its device workspace and three streams kept
+    across calls: grouping, preprocessing and attention of host-resident
+    Q, K, V (bf16 [B,H,N,128], ideally pinned) into host O (and lse2), the
+    copies overlapped with the computation chunk by chunk."""
+
+    def __init__(self, shape, k, iters=5, chunk_heads=0, device=None, dual=True):
+        self.shape = Shape(*shape)
+        self.k, self.iters, self.chunk_heads = int(k), int(iters), int(chunk_heads)
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        nbytes = _lib().vcattn_fwd_host_workspace_bytes(ctypes.byref(self.shape), self.k, self.chunk_heads)
+        if nbytes == 0:
+            raise VcattnError(ERR_INVALID_ARG, "vcattn_fwd_host_workspace_bytes")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        # compute 0, compute 1 (the same stream unless dual), copy in, copy out
+        st = [torch.cuda.Stream(device=self.device) for _ in range(4 if dual else 3)]
+        self.streams = [st[0], st[1] if dual else st[0]] + st[-2:]
+        self._sp = (ctypes.c_void_p * 4)(*[s.cuda_stream for s in self.streams])
+
+    @property
+    def stream(self):
+        """The stream that completes the call (synchronise it, or wait on it)."""
+        return self.streams[0]
+
+    def __call__(self, hQ, hK, hV, sm_scale, mask=None, hO=None, hlse2=None):
+        for t, n in ((hQ, "hQ"), (hK, "hK"), (hV, "hV")):
+            if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError("%s must be a contiguous host bf16 tensor" % n)
+        if hO is None:
+            hO = torch.empty(hQ.shape, dtype=torch.bfloat16, pin_memory=True)
+        if mask is not None:
+            _req(mask, torch.uint8, "mask")
+        # the compute streams start after the caller's pending work
+        for s in self.streams[:2]:
+            s.wait_stream(torch.cuda.current_stream(self.device))
+        _check(_lib().vcattn_fwd_host(ctypes.byref(self.shape), ctypes.c_void_p(hQ.data_ptr()),
+                                      ctypes.c_void_p(hK.data_ptr()), ctypes.c_void_p(hV.data_ptr()),
+                                      self.k, self.iters, float(sm_scale), _ptr(mask),
+                                      ctypes.c_void_p(hO.data_ptr()),
+                                      None if hlse2 is None else ctypes.c_void_p(hlse2.data_ptr()),
+                                      self.chunk_heads, _ptr(self.ws), self.ws.numel(), self._sp),
+               "vcattn_fwd_host")
+        return hO, hlse2
 
 
 def fwd_workspace_bytes(shape_tuple):

@@ -190,6 +190,45 @@ vcattn_status vcattn_fwd(const vcattn_shape* shape, const void* Q, const void* K
                          const int32_t* perm, float sm_scale, const uint8_t* tile_mask,
                          void* O, float* lse2, void* ws, size_t ws_bytes, void* stream);
 
+/* -------------------------------------------------- host-resident tensors */
+/* The whole path -- vcattn_group (k, iters), vcattn_prep, vcattn_attn -- for
+ * Q, K, V and O in host memory, with the host<->device copies overlapped with
+ * the computation.  The method never mixes heads (k-means, the permutation,
+ * the quantisers and the attention are per (b, h)), so the flattened B*H
+ * heads go through the device in chunks of `chunk_heads` heads (0 = 8; the
+ * first chunk has a quarter of that, rounded up, so computing starts early):
+ * two device slots alternate, chunk c computes on streams[c % 2], and meanwhile
+ * the next chunk's Q, K, V are copied in on streams[2] and finished chunks'
+ * O (and lse2) copied out on streams[3].  streams[0] and streams[1] may be
+ * the same stream (the chunks then compute in turn); distinct, one chunk's
+ * k-means runs beside the other's attention.  O and lse2 equal, bit for bit,
+ * those of vcattn_group followed by vcattn_fwd on the same inputs.
+ *   hQ, hK, hV  bf16 [B,H,N,D] in host memory.  Page-locked buffers
+ *               (cudaHostAlloc, cudaHostRegister) let the copies overlap;
+ *               pageable ones give the same results, copied synchronously.
+ *   k, iters    as for vcattn_group
+ *   tile_mask   u8 [B,H,ceil(N/64),Npad/64] (device), nullable = dense
+ *   hO          bf16 [B,H,N,D] host out; hlse2 f32 [B,H,N] host out, nullable
+ *   ws          device scratch, 256-byte aligned, of at least
+ *               vcattn_fwd_host_workspace_bytes(shape, k, chunk_heads) bytes
+ *               (two slots of chunk_heads heads each)
+ *   streams     four cudaStream_t: compute 0, compute 1 (may equal compute 0),
+ *               copy in, copy out (these two distinct from all others)
+ * The call's work starts after the work already enqueued on streams[0] (the
+ * other three streams wait for it), and all of it is enqueued when the call
+ * returns; streams[0] passes the end of the call only after the last copy
+ * out, so synchronising it (or an event recorded on it afterwards) makes hO
+ * and hlse2 valid, and consecutive calls may share one workspace.  The host
+ * buffers must stay allocated and unchanged until then.  The call allocates
+ * no device memory; it creates eleven CUDA events and releases them (each once
+ * complete) before returning.  On an error return, part of the work may
+ * already be enqueued. */
+size_t vcattn_fwd_host_workspace_bytes(const vcattn_shape* shape, int k, int chunk_heads);
+vcattn_status vcattn_fwd_host(const vcattn_shape* shape, const void* hQ, const void* hK,
+                              const void* hV, int k, int iters, float sm_scale,
+                              const uint8_t* tile_mask, void* hO, float* hlse2, int chunk_heads,
+                              void* ws, size_t ws_bytes, void* const streams[4]);
+
 /* ------------------------------------------------------------------ errors */
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device: VCATTN_OK, VCATTN_ERR_TIMEOUT or VCATTN_ERR_DEVICE (or

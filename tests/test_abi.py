@@ -106,3 +106,41 @@ def test_argument_validation_without_gpu(lib):
                            None) == 1
     assert lib.vcattn_fwd(ctypes.byref(s), fake, fake, fake, None, ctypes.c_float(0.1), None, fake,
                           None, fake, 16, None) == 1
+
+
+def test_fwd_host_validation_without_gpu(lib):
+    """The host-pipeline entry point sizes two chunk slots and rejects bad
+    arguments before any CUDA call."""
+    P = ctypes.c_void_p
+    s = _shape(B=2, H=5, N=1000)
+    one = _shape(B=1, H=1, N=1000)
+    w8 = lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(s), 8, 0)    # default chunk: all 10 > 8 -> 8
+    w2 = lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(s), 8, 2)
+    w1 = lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(one), 8, 0)  # chunk clamps to B*H = 1
+    assert w8 > w2 > 0 and w1 > 0
+    assert lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(s), 8, 20) == \
+        lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(s), 8, 10)
+    # two slots of a one-head chunk hold at least Q, K, V and O of that head twice
+    assert w1 >= 2 * 4 * 1000 * 128 * 2
+    assert lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(s), 0, 2) == 0
+    assert lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(s), 8, -1) == 0
+    assert lib.vcattn_fwd_host_workspace_bytes(ctypes.byref(_shape(D=64)), 8, 2) == 0
+    fake, ws = P(1 << 20), P(1 << 24)
+    streams = (P * 4)(P(1), P(2), P(3), P(4))
+    same = (P * 4)(P(1), P(2), P(3), P(3))
+    shared = (P * 4)(P(1), P(2), P(1), P(4))
+
+    def call(hQ=fake, k=8, iters=5, hO=fake, chunk=2, w=ws, nbytes=w2, st=streams, shape=s):
+        return lib.vcattn_fwd_host(ctypes.byref(shape), hQ, fake, fake, k, iters, ctypes.c_float(0.1),
+                                   None, hO, None, chunk, w, nbytes, st)
+    assert call(hQ=None) == 1
+    assert call(hO=None) == 1
+    assert call(iters=0) == 1
+    assert call(chunk=-1) == 1
+    assert call(k=65) == 2
+    assert call(shape=_shape(D=64)) == 2
+    assert call(w=P((1 << 24) + 16)) == 1        # not 256-byte aligned
+    assert call(nbytes=w2 - 1) == 1
+    assert call(st=same) == 1
+    assert call(st=shared) == 1
+    assert call(st=None) == 1
