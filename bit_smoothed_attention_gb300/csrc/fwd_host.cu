@@ -11,8 +11,9 @@
 //   compute stream 1                 grp+prep(1) attn(1)   grp+prep(3) ...
 //   copy-out stream                          out(0)    out(1) ...
 //
-// The first chunk has a quarter of the heads of the others, so that the
-// device starts computing after a short copy; V of each chunk is copied
+// The first two chunks have an eighth and three eighths of the heads of the
+// others, so that the device starts computing after a short copy and each
+// copy in hides behind the computation before it; V of each chunk is copied
 // first, so the k-means (which reads only V) overlaps the copy of Q and K.
 // Slot s = c % 2 holds chunk c's Q, K, V, labels, perm, workspaces and O, and
 // chunk c computes on compute stream s.  With two distinct compute streams
@@ -148,9 +149,21 @@ vcattn_status vcattn_fwd_host(const vcattn_shape* s, const void* hQ, const void*
 
   const size_t row = size_t(N) * vc::D * 2;  // bytes of one head of Q, K, V or O
   const int64_t nq64 = (N + vc::BLK - 1) / vc::BLK, nbp = vc::npad(N) / vc::BLK;
-  // chunk c covers heads [h0(c), h0(c) + heads(c)): a first chunk of ch0 heads, then ch
-  const int ch0 = (ch + 3) / 4;
-  const int64_t nchunks = BH <= ch0 ? 1 : 1 + (BH - ch0 + ch - 1) / ch;
+  // chunk c covers heads [h0(c), h0(c) + heads(c)): ramp-up chunks of ch/8 and
+  // 3ch/8 heads (rounded up; while the first computes, the second is copied
+  // in, and so on), then ch
+  const int r0 = (ch + 7) / 8, r1 = (3 * ch + 7) / 8;
+  auto chunk_at = [&](int64_t c, int64_t* h0, int64_t* want) {
+    if (c == 0) { *h0 = 0; *want = r0; }
+    else if (c == 1) { *h0 = r0; *want = r1; }
+    else { *h0 = r0 + r1 + (c - 2) * ch; *want = ch; }
+  };
+  int64_t nchunks = 0;
+  for (int64_t h = 0; h < BH; ++nchunks) {
+    int64_t a, b;
+    chunk_at(nchunks, &a, &b);
+    h = a + b;
+  }
   auto cu = [](cudaError_t e) { return e == cudaSuccess ? VCATTN_OK : vc::from_cuda(e); };
   vcattn_status st = cu(cudaEventRecord(ev_start, scs[0]));
   if (st == VCATTN_OK) st = cu(cudaStreamWaitEvent(si, ev_start, 0));
@@ -160,8 +173,8 @@ vcattn_status vcattn_fwd_host(const vcattn_shape* s, const void* hQ, const void*
     const int b = static_cast<int>(c & 1);
     const Slot& sl = slot[b];
     cudaStream_t sc = scs[b];
-    const int64_t h0 = c == 0 ? 0 : ch0 + (c - 1) * ch;
-    const int64_t want = c == 0 ? ch0 : ch;
+    int64_t h0 = 0, want = 0;
+    chunk_at(c, &h0, &want);
     const int heads = static_cast<int>(BH - h0 < want ? BH - h0 : want);
     const vcattn_shape hs = chunk_shape(s, heads);
     const size_t bytes = size_t(heads) * row;

@@ -196,7 +196,8 @@ vcattn_status vcattn_fwd(const vcattn_shape* shape, const void* Q, const void* K
  * the computation.  The method never mixes heads (k-means, the permutation,
  * the quantisers and the attention are per (b, h)), so the flattened B*H
  * heads go through the device in chunks of `chunk_heads` heads (0 = 8; the
- * first chunk has a quarter of that, rounded up, so computing starts early):
+ * first two chunks have an eighth and three eighths of that, rounded up, so
+ * computing starts early):
  * two device slots alternate, chunk c computes on streams[c % 2], and meanwhile
  * the next chunk's Q, K, V are copied in on streams[2] and finished chunks'
  * O (and lse2) copied out on streams[3].  streams[0] and streams[1] may be
