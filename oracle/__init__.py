@@ -37,6 +37,7 @@ def _L():
         lib.orc_tree_sum.argtypes = [P, i64]
         lib.orc_tree_sum.restype = f32
         lib.orc_kmeans.argtypes = [P, i64, i64, i32, i32, P, P]
+        lib.orc_kmeans_from.argtypes = [P, i64, i64, i32, i32, P, P, P]
         lib.orc_kmeans_scores.argtypes = [P, i64, P, i32, P]
         lib.orc_stable_sort.argtypes = [P, i64, i64, i32, P]
         lib.orc_prep.argtypes = [P, P, P, P, i64, i64] + [P] * 9
@@ -104,13 +105,17 @@ def tree_sum(x):
     return np.float32(_L().orc_tree_sum(_p(x), x.size))
 
 
-def kmeans(V, k, iters):
-    """V: uint16 [BH, N, 128] -> labels int32 [BH, N], centroids f32 [BH, k, 128]."""
+def kmeans(V, k, iters, init=None):
+    """V: uint16 [BH, N, 128] -> labels int32 [BH, N], centroids f32 [BH, k, 128].
+    init: None (c_c = v[floor(c N / k)]) or starting centroids f32 [BH, k, 128]."""
     V = _c(V, np.uint16)
     BH, N, _ = V.shape
     labels = np.empty((BH, N), np.int32)
     cent = np.empty((BH, k, D), np.float32)
-    rc = _L().orc_kmeans(_p(V), BH, N, k, iters, _p(labels), _p(cent))
+    ini = None if init is None else _c(init, np.float32)
+    if ini is not None and ini.shape != (BH, k, D):
+        raise ValueError("init must be [BH, k, 128]")
+    rc = _L().orc_kmeans_from(_p(V), BH, N, k, iters, _p(ini), _p(labels), _p(cent))
     if rc:
         raise ValueError("orc_kmeans: bad arguments")
     return labels, cent

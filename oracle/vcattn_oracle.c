@@ -223,9 +223,12 @@ static void kmeans_update_one(const float* v, int64_t N, const int32_t* labels, 
   free(total);
 }
 
-/* V: [BH, N, 128] bf16 bits.  labels [BH, N]; centroids [BH, k, 128]. */
-int orc_kmeans(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
-               int32_t* labels, float* centroids) {
+/* V: [BH, N, 128] bf16 bits.  labels [BH, N]; centroids [BH, k, 128].
+ * init: NULL = the R3 initialisation c_c = v[floor(c N / k)]; otherwise the
+ * starting centroids [BH, k, 128] (a warm start, e.g. from an earlier
+ * step's grouping), after which the same iterations run. */
+int orc_kmeans_from(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
+                    const float* init, int32_t* labels, float* centroids) {
   if (k < 1 || k > 64 || iters < 1 || N < 1) return 1;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t bh = 0; bh < BH; ++bh) {
@@ -233,9 +236,13 @@ int orc_kmeans(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
     const uint16_t* src = V + bh * N * ORC_D;
     for (int64_t i = 0; i < N * ORC_D; ++i) v[i] = bf16_to_f32(src[i]);
     float* cent = centroids + bh * (int64_t)k * ORC_D;
-    for (int c = 0; c < k; ++c) {
-      int64_t j = ((int64_t)c * N) / k;
-      memcpy(cent + c * ORC_D, v + j * ORC_D, ORC_D * sizeof(float));
+    if (init) {
+      memmove(cent, init + bh * (int64_t)k * ORC_D, (size_t)k * ORC_D * sizeof(float));
+    } else {
+      for (int c = 0; c < k; ++c) {
+        int64_t j = ((int64_t)c * N) / k;
+        memcpy(cent + c * ORC_D, v + j * ORC_D, ORC_D * sizeof(float));
+      }
     }
     int32_t* lab = labels + bh * N;
     for (int it = 0; it < iters; ++it) {
@@ -245,6 +252,11 @@ int orc_kmeans(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
     free(v);
   }
   return 0;
+}
+
+int orc_kmeans(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
+               int32_t* labels, float* centroids) {
+  return orc_kmeans_from(V, BH, N, k, iters, NULL, labels, centroids);
 }
 
 /* Scores of the assign step for tie counting: score[j*k + c]. */

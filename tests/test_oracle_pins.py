@@ -282,6 +282,34 @@ def test_kmeans_brute_force_invariants(orc):
             prev_obj, prev_labels, prev_C = obj, labels, C
 
 
+def test_kmeans_warm_start_continues_the_iterations(orc):
+    """Starting from the centroids after n iterations and running m more is
+    the same computation as n + m iterations from the usual seeds (labels
+    and centroids bit for bit); a warm start from arbitrary centroids makes
+    the first assign the brute-force nearest centroid."""
+    rng = np.random.default_rng(14)
+    V = _bits(rng.standard_normal((2, 300, 128)) * 2 + rng.standard_normal((2, 1, 128)))
+    k = 7
+    for n, m in ((1, 1), (2, 3), (4, 1)):
+        _, Cn = orc.kmeans(V, k, n)
+        lw, Cw = orc.kmeans(V, k, m, init=Cn)
+        lc, Cc = orc.kmeans(V, k, n + m)
+        assert np.array_equal(lw, lc) and np.array_equal(Cw, Cc)
+    init = rng.standard_normal((2, k, 128)).astype(np.float32)
+    lab, C = orc.kmeans(V, k, 1, init=init)
+    for h in range(2):
+        v = _f(V[h])
+        d2 = ((v[:, None, :] - init[h][None].astype(np.float64)) ** 2).sum(-1)
+        chosen = d2[np.arange(v.shape[0]), lab[h]]
+        assert np.all(chosen <= d2.min(1) + 1e-6 * (1 + d2.min(1)))
+        for c in range(k):
+            mem = lab[h] == c
+            if mem.any():
+                assert np.allclose(C[h, c], v[mem].mean(0), rtol=2e-6, atol=2e-6)
+            else:
+                assert np.array_equal(C[h, c], init[h, c])
+
+
 def test_kmeans_tie_goes_to_lowest_cluster(orc):
     # two identical points as the only data: both seeds equal, every score ties
     v = np.ones((2, 128), np.float32)
