@@ -247,12 +247,19 @@ size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws) {
 }
 
 cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
-                         int32_t* labels, int32_t* perm, float* centroids_out, const GroupWs& ws,
-                         uint32_t* err, cudaStream_t s) {
+                         const float* init, int32_t* labels, int32_t* perm, float* centroids_out,
+                         const GroupWs& ws, uint32_t* err, cudaStream_t s) {
   const int nchunk = static_cast<int>(ceil_div(N, UPD_CHUNK));
   float* cent = centroids_out ? centroids_out : ws.cent;
-  km_init<<<static_cast<unsigned>(BH), D, 0, s>>>(V, N, k, cent);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (!init) {
+    km_init<<<static_cast<unsigned>(BH), D, 0, s>>>(V, N, k, cent);
+    e = cudaGetLastError();
+  } else if (init != cent) {
+    // warm start: the iterations begin from the given centroids
+    e = cudaMemcpyAsync(cent, init, static_cast<size_t>(BH) * k * D * sizeof(float),
+                        cudaMemcpyDeviceToDevice, s);
+  }
   if (e != cudaSuccess) return e;
   const dim3 gchunk(nchunk, static_cast<unsigned>(BH));
   for (int it = 0; it < iters; ++it) {

@@ -34,7 +34,8 @@ size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws);
 cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
                                 int32_t* labels, uint32_t* err, cudaStream_t s);
 cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
-                         int32_t* labels, int32_t* perm, float* centroids_out, const GroupWs& ws,
+                         const float* init, int32_t* labels, int32_t* perm, float* centroids_out,
+                         const GroupWs& ws,
                          uint32_t* err, cudaStream_t s);
 
 // ---- preprocessing (prep.cu) ----

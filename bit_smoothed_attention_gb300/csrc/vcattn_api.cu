@@ -112,23 +112,42 @@ size_t vcattn_group_workspace_bytes(const vcattn_shape* s, int k) {
   return vc::group_ws_layout(s->B * s->H, s->N, k, nullptr, nullptr);
 }
 
-vcattn_status vcattn_group(const vcattn_shape* s, const void* V, int k, int iters, int32_t* labels,
-                           int32_t* perm, float* centroids, void* ws, size_t ws_bytes,
-                           void* stream) {
+}  // extern "C"
+
+namespace {
+vcattn_status group_impl(const vcattn_shape* s, const void* V, int k, int iters, const float* init,
+                         int32_t* labels, int32_t* perm, float* centroids, void* ws, size_t ws_bytes,
+                         void* stream) {
   vcattn_status st = check_shape(s);
   if (st != VCATTN_OK) return st;
   if (k < 1 || k > vc::KMAX) return VCATTN_ERR_UNSUPPORTED;
   if (iters < 1 || !V || !labels || !perm || !ws) return VCATTN_ERR_INVALID_ARG;
   if (!aligned16(V) || !aligned16(labels) || !aligned16(perm) || !aligned16(ws) ||
-      (centroids && !aligned16(centroids)))
+      (centroids && !aligned16(centroids)) || (init && !aligned16(init)))
     return VCATTN_ERR_INVALID_ARG;
   const int64_t BH = s->B * s->H;
   vc::GroupWs w{};
   if (ws_bytes < vc::group_ws_layout(BH, s->N, k, ws, &w)) return VCATTN_ERR_INVALID_ARG;
   uint32_t* err = err_word(&st);
   if (!err) return st;
-  return from_cuda(vc::launch_group(static_cast<const uint16_t*>(V), BH, s->N, k, iters, labels,
+  return from_cuda(vc::launch_group(static_cast<const uint16_t*>(V), BH, s->N, k, iters, init, labels,
                                     perm, centroids, w, err, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+vcattn_status vcattn_group(const vcattn_shape* s, const void* V, int k, int iters, int32_t* labels,
+                           int32_t* perm, float* centroids, void* ws, size_t ws_bytes,
+                           void* stream) {
+  return group_impl(s, V, k, iters, nullptr, labels, perm, centroids, ws, ws_bytes, stream);
+}
+
+vcattn_status vcattn_group_warm(const vcattn_shape* s, const void* V, int k, int iters,
+                                const float* init_centroids, int32_t* labels, int32_t* perm,
+                                float* centroids, void* ws, size_t ws_bytes, void* stream) {
+  if (!init_centroids) return VCATTN_ERR_INVALID_ARG;
+  return group_impl(s, V, k, iters, init_centroids, labels, perm, centroids, ws, ws_bytes, stream);
 }
 
 size_t vcattn_prepped_bytes(const vcattn_shape* s) {

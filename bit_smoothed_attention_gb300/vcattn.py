@@ -58,6 +58,8 @@ def _lib():
         lib.vcattn_group_workspace_bytes.argtypes = [SP, ctypes.c_int]
         lib.vcattn_group.restype = st
         lib.vcattn_group.argtypes = [SP, P, ctypes.c_int, ctypes.c_int, P, P, P, P, sz, P]
+        lib.vcattn_group_warm.restype = st
+        lib.vcattn_group_warm.argtypes = [SP, P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, sz, P]
         lib.vcattn_prepped_bytes.restype = sz
         lib.vcattn_prepped_bytes.argtypes = [SP]
         lib.vcattn_prepped_carve.restype = st
@@ -123,10 +125,16 @@ def npad(N):
     return int(_lib().vcattn_npad(N))
 
 
-def group(V, k, iters=5, centroids=False, stream=None):
+def group(V, k, iters=5, centroids=False, stream=None, init=None):
     """k-means labels and the stable-sort permutation of V [B,H,N,128] bf16.
-    Returns (labels, perm[, centroids]) as int32 [B,H,N] (and f32 [B,H,k,128])."""
+    Returns (labels, perm[, centroids]) as int32 [B,H,N] (and f32 [B,H,k,128]).
+    init: starting centroids f32 [B,H,k,128] (vcattn_group_warm) instead of
+    the evenly spaced seeds."""
     _req(V, torch.bfloat16, "V")
+    if init is not None:
+        _req(init, torch.float32, "init")
+        if tuple(init.shape) != (V.shape[0], V.shape[1], k, 128):
+            raise ValueError("init must be [B, H, k, 128]")
     s = _shape(V)
     B, H, N, _ = V.shape
     labels = torch.empty(B, H, N, dtype=torch.int32, device=V.device)
@@ -136,8 +144,13 @@ def group(V, k, iters=5, centroids=False, stream=None):
     if nbytes == 0:
         raise ValueError("unsupported grouping shape or k")
     ws = torch.empty(nbytes, dtype=torch.uint8, device=V.device)
-    _check(_lib().vcattn_group(ctypes.byref(s), _ptr(V), k, iters, _ptr(labels), _ptr(perm),
-                               _ptr(cent), _ptr(ws), nbytes, _stream(stream)), "vcattn_group")
+    if init is None:
+        _check(_lib().vcattn_group(ctypes.byref(s), _ptr(V), k, iters, _ptr(labels), _ptr(perm),
+                                   _ptr(cent), _ptr(ws), nbytes, _stream(stream)), "vcattn_group")
+    else:
+        _check(_lib().vcattn_group_warm(ctypes.byref(s), _ptr(V), k, iters, _ptr(init), _ptr(labels),
+                                        _ptr(perm), _ptr(cent), _ptr(ws), nbytes, _stream(stream)),
+               "vcattn_group_warm")
     return (labels, perm, cent) if centroids else (labels, perm)
 
 

@@ -104,6 +104,19 @@ size_t vcattn_group_workspace_bytes(const vcattn_shape* shape, int k);
 vcattn_status vcattn_group(const vcattn_shape* shape, const void* V, int k, int iters,
                            int32_t* labels, int32_t* perm, float* centroids,
                            void* ws, size_t ws_bytes, void* stream);
+/* The same grouping started from given centroids instead of the evenly
+ * spaced seeds (a warm start).  The pages regroup on the first quarter of
+ * the denoising steps; starting each regrouping from the previous one's
+ * centroids lets it run fewer iterations.  Starting from the centroids of
+ * n iterations and running m more gives exactly the result of n + m
+ * iterations of vcattn_group.
+ *   init_centroids  f32 [B,H,k,D] (device), required; `centroids` may be the
+ *                   same buffer (updated in place), otherwise the two must
+ *                   not overlap
+ * Other arguments as for vcattn_group (same workspace size). */
+vcattn_status vcattn_group_warm(const vcattn_shape* shape, const void* V, int k, int iters,
+                                const float* init_centroids, int32_t* labels, int32_t* perm,
+                                float* centroids, void* ws, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------- preprocessing */
 /* Fused preprocessing (TeleFuser PR #40 Changes; VC-Attention Key

@@ -144,3 +144,16 @@ def test_fwd_host_validation_without_gpu(lib):
     assert call(st=same) == 1
     assert call(st=shared) == 1
     assert call(st=None) == 1
+
+
+def test_group_warm_validation_without_gpu(lib):
+    P = ctypes.c_void_p
+    s = _shape()
+    fake = P(1 << 20)
+    # the starting centroids are required and must be 16-byte aligned
+    assert lib.vcattn_group_warm(ctypes.byref(s), fake, 8, 1, None, fake, fake, None, fake, 1 << 30,
+                                 None) == 1
+    assert lib.vcattn_group_warm(ctypes.byref(s), fake, 8, 1, P((1 << 20) + 4), fake, fake, None, fake,
+                                 1 << 30, None) == 1
+    assert lib.vcattn_group_warm(ctypes.byref(s), fake, 65, 1, fake, fake, fake, None, fake, 1 << 30,
+                                 None) == 2

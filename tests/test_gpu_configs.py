@@ -58,6 +58,7 @@ def _check_head(orc, O32, L, Qb, Kb, Vb, opp, sm, qidx, mask_h=None, perm_h=None
     keep = np.linalg.norm(Od, axis=1) > 0
     rel_d, _, cos_d = _metrics(g[keep], Od[keep])
     assert rel_d <= REL_DENSE and cos_d >= COS_DENSE, (rel_d, cos_d)
+    return rel_d
 
 
 def test_mid_full_output(vc, orc):
@@ -137,6 +138,62 @@ def test_schedule_regroup_then_reuse(vc, orc):
                 assert abs(rel_d - rel_m) <= 0.1 * rel_m + 1e-3, (t, h, rel_d, rel_m)
     print("schedule: attention ms per step, median %.3f (min %.3f, max %.3f)"
           % (float(np.median(times[1:])), min(times[1:]), max(times[1:])))
+
+
+def test_schedule_warm_start_regrouping(vc, orc):
+    """Cheaper regrouping on the schedule: step 0 groups from the seeds
+    (5 iterations), steps 1..12 start from the previous step's centroids and
+    run one iteration (vcattn_group_warm).  On two heads the labels, the
+    permutation and the centroids equal the oracle's own warm chain at every
+    regrouping step; attention on steps 0, 6, 12 and 13 meets the bars."""
+    w = W.WORKLOADS["schedule"]
+    sm = float(np.float32(w.sm_scale))
+    Q0, K0, V0 = W.make_workload(w, device="cuda")
+    qidx = W.evenly_spaced_queries(w.N)
+    heads = (0, 39)
+    cent, ocent, operm = None, {}, {}
+    t_warm, t_cold = [], []
+    for t in range(14):
+        Q, K, V = (W.drift(x, t, w.seed + j) for j, x in enumerate((Q0, K0, V0)))
+        if t < 13:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record()
+            if t == 0:
+                labels, perm, cent = vc.group(V, w.k, w.iters, centroids=True)
+            else:
+                labels, perm, cent = vc.group(V, w.k, 1, centroids=True, init=cent)
+            e[1].record()
+            if t > 0:
+                e[2].record()
+                vc.group(V, w.k, w.iters)
+                e[3].record()
+            torch.cuda.synchronize()
+            if t > 0:
+                t_warm.append(e[0].elapsed_time(e[1]))
+                t_cold.append(e[2].elapsed_time(e[3]))
+            for h in heads:
+                Vb = _head_bits(V, h)
+                if t == 0:
+                    ol, oc = orc.kmeans(Vb, w.k, w.iters)
+                else:
+                    ol, oc = orc.kmeans(Vb, w.k, 1, init=ocent[h])
+                ocent[h], operm[h] = oc, orc.stable_sort(ol, w.k)
+                assert np.array_equal(labels[0, h].cpu().numpy(), ol[0]), (t, h)
+                assert np.array_equal(perm[0, h].cpu().numpy(), operm[h][0]), (t, h)
+                assert np.array_equal(cent[0, h].cpu().numpy(), oc[0]), (t, h)
+        if t in (0, 6, 12, 13):
+            pp = vc.prep(Q, K, V, perm)
+            O32, L = vc.attn(pp, sm, out_f32=True)
+            torch.cuda.synchronize()
+            assert vc.last_device_error() == 0
+            for h in heads:
+                Qb, Kb, Vb = (_head_bits(x, h) for x in (Q, K, V))
+                opp = orc.prep(Qb, Kb, Vb, operm[h])
+                rel_d = _check_head(orc, O32[0, h].cpu().numpy(), L[0, h].cpu().numpy(), Qb, Kb, Vb,
+                                    opp, sm, qidx, perm_h=operm[h][0])
+                print("warm schedule step %2d head %2d: rel-L2 vs exact %.4f" % (t, h, rel_d))
+    print("warm regrouping: %.3f ms per step (median of steps 1-12), cold 5 iterations %.3f ms"
+          % (float(np.median(t_warm)), float(np.median(t_cold))))
 
 
 def test_sparse_full_size(vc, orc):

@@ -10,6 +10,7 @@ Bars (the stated tolerances of the method's hot path):
   0.998; log2-LSE vs the emulating oracle: max-abs <= 1e-3;
 * bf16 output: within the FP32 bar plus half a bf16 ulp of the output.
 """
+import ctypes
 import math
 
 import numpy as np
@@ -157,6 +158,39 @@ def test_prep_identity_perm_and_zero_blocks(vc, orc):
     for key in PREP_KEYS:
         assert np.array_equal(got[key], ref[key]), key
     assert np.all(got["v_scale"] == 1.0) and np.all(got["r8t"] == 0)
+
+
+@pytest.mark.parametrize("N,H,k,n,m", [(3000, 2, 16, 2, 3), (777, 1, 5, 1, 1), (2049, 1, 64, 3, 2)])
+def test_group_warm_start(vc, orc, N, H, k, n, m):
+    """vcattn_group_warm: bit-exact against the oracle's warm start, and n
+    iterations followed by m warm-started ones equal n + m iterations (also
+    with the centroids updated in place)."""
+    Q, K, V = _inputs(1, H, N, k, 900 + N)
+    _, _, c_n = vc.group(V, k, n, centroids=True)
+    l_w, p_w, c_w = vc.group(V, k, m, centroids=True, init=c_n)
+    l_c, p_c, c_c = vc.group(V, k, n + m, centroids=True)
+    torch.cuda.synchronize()
+    assert vc.last_device_error() == 0
+    assert torch.equal(l_w, l_c) and torch.equal(p_w, p_c) and torch.equal(c_w, c_c)
+    Vb = _bits(V)
+    _, oc_n = orc.kmeans(Vb, k, n)
+    assert np.array_equal(c_n.reshape(H, k, 128).cpu().numpy(), oc_n)
+    ol, oc = orc.kmeans(Vb, k, m, init=oc_n)
+    assert np.array_equal(l_w.reshape(H, N).cpu().numpy(), ol)
+    assert np.array_equal(p_w.reshape(H, N).cpu().numpy(), orc.stable_sort(ol, k))
+    assert np.array_equal(c_w.reshape(H, k, 128).cpu().numpy(), oc)
+    # in place: the output centroid buffer is the starting one
+    c_in = c_n.clone()
+    s = vc._shape(V)
+    lab = torch.empty(1, H, N, dtype=torch.int32, device="cuda")
+    prm = torch.empty_like(lab)
+    nb = vc.lib().vcattn_group_workspace_bytes(ctypes.byref(s), k)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    assert vc.lib().vcattn_group_warm(ctypes.byref(s), vc._ptr(V), k, m, vc._ptr(c_in), vc._ptr(lab),
+                                      vc._ptr(prm), vc._ptr(c_in), vc._ptr(ws), nb,
+                                      vc._stream(None)) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(c_in, c_w) and torch.equal(lab, l_w)
 
 
 # --------------------------------------------------------------- attention
