@@ -242,6 +242,10 @@ size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws) {
   w.part = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * nchunk * k * D * 4));
   w.cnt = reinterpret_cast<int32_t*>(take(static_cast<size_t>(BH) * nchunk * k * 4));
   w.offs = reinterpret_cast<int32_t*>(take(static_cast<size_t>(BH) * nchunk * k * 4));
+  w.amb = reinterpret_cast<KmAmb*>(take(static_cast<size_t>(BH) * N * sizeof(KmAmb)));
+  w.amb_count = reinterpret_cast<uint32_t*>(take(8));
+  w.head_cn = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * 2 * 4));
+  w.head_h = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * KMAX * 4));
   if (ws) *ws = w;
   return off;
 }
@@ -261,9 +265,11 @@ cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int it
                         cudaMemcpyDeviceToDevice, s);
   }
   if (e != cudaSuccess) return e;
+  // counters of the open assignments (each fix-up clears the next one)
+  if ((e = cudaMemsetAsync(ws.amb_count, 0, 2 * sizeof(uint32_t), s)) != cudaSuccess) return e;
   const dim3 gchunk(nchunk, static_cast<unsigned>(BH));
   for (int it = 0; it < iters; ++it) {
-    e = launch_km_assign_tc(V, BH, N, k, cent, labels, err, s);
+    e = launch_km_assign_tc(V, BH, N, k, cent, labels, ws, it, err, s);
     if (e != cudaSuccess) return e;
     km_partial<<<gchunk, 256, 0, s>>>(V, labels, N, k, nchunk, ws.part, ws.cnt, err);
     km_finalize<<<dim3(k, static_cast<unsigned>(BH)), D, 0, s>>>(ws.part, ws.cnt, nchunk, k, cent);

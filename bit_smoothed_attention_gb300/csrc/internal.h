@@ -22,17 +22,30 @@ __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // ---- grouping (group.cu) ----
+// A token whose assignment the tensor-core filter left open: its flat index
+// b*H*N + h*N + j, the candidate clusters and its |v| bound.
+struct KmAmb {
+  int64_t tok;
+  uint64_t cand;
+  float vn;
+  float pad;
+};
 struct GroupWs {
-  float* cent;    // [BH, k, D]
-  float* part;    // [BH, nchunk, k, D]
-  int32_t* cnt;   // [BH, nchunk, k]
-  int32_t* offs;  // [BH, nchunk, k]
+  float* cent;         // [BH, k, D]
+  float* part;         // [BH, nchunk, k, D]
+  int32_t* cnt;        // [BH, nchunk, k]
+  int32_t* offs;       // [BH, nchunk, k]
+  KmAmb* amb;          // [BH * N] open assignments of one iteration
+  uint32_t* amb_count; // [2]: how many, for even and odd iterations
+  float* head_cn;      // [BH, 2]: max |c| and max |h| bounds of each head
+  float* head_h;       // [BH, 64]: h_c of each head
 };
 size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws);
 // Tensor-core k-means assignment with an exact FP32 fallback (km_tc.cu);
 // 1 <= k <= 64.
 cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
-                                int32_t* labels, uint32_t* err, cudaStream_t s);
+                                int32_t* labels, const GroupWs& ws, int iter, uint32_t* err,
+                                cudaStream_t s);
 cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
                          const float* init, int32_t* labels, int32_t* perm, float* centroids_out,
                          const GroupWs& ws,

@@ -22,12 +22,15 @@
 // E/2 >= m - E (c* the argmax of T).  So clusters with T_c < m - E cannot
 // win.
 // When one cluster is left it is the label.  Otherwise (0.6% of the tokens
-// on the live workload) a second filter computes the candidates' FP32 dot
-// products in eight interleaved partial sums and drops those more than
-// E2 = 2^-15 (|v| max|c| + max|h|) below the best of them (the same
-// argument with a tighter bound); the exact chains of what is left decide,
-// lowest index first on ties.  The labels are those of the FP32 definition,
-// bit for bit, whatever the data.
+// on the live workload) the token goes on a list, and km_fixup, launched
+// right after, resolves every listed token with one thread each: a second
+// filter computes the candidates' FP32 dot products in eight interleaved
+// partial sums and drops those more than E2 = 2^-15 (|v| max|c| + max|h|)
+// below the best of them (the same argument with a tighter bound); the
+// exact chains of what is left decide, lowest index first on ties.  (Done in
+// place, these few tokens held their whole warp on a chain of global loads:
+// a third of the assignment time.)  The labels are those of the FP32
+// definition, bit for bit, whatever the data.
 //
 // CTA: up to KT_TPC consecutive 128-token tiles of one (b, h).  Warps 0-3:
 // one thread per token (= TMEM lane) for the selection; warp 4: TMA; warp 5:
@@ -81,13 +84,10 @@ __device__ __forceinline__ uint32_t k16(int r, int e) {
   return static_cast<uint32_t>((r >> 3) * 256 + (e >> 3) * 128 + (r & 7) * 16 + (e & 7) * 2);
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t* tile, int r, int e) {
-  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + sw128(r, e))) << 16);
-}
-
 __global__ void __launch_bounds__(KT_THREADS, 2)
     km_assign_tc(const __grid_constant__ CUtensorMap tmv, int64_t N, int k, int tpc, const float* __restrict__ cent,
-                 int32_t* __restrict__ labels, uint32_t* __restrict__ err) {
+                 int32_t* __restrict__ labels, KmAmb* __restrict__ amb, uint32_t* __restrict__ amb_count,
+                 float* __restrict__ head_cn, float* __restrict__ head_h, uint32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -229,6 +229,13 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     const int r = warp * 32 + lane;  // token within the tile = TMEM lane
     // E = EA |v| + EB, with EA = (2^-13 + 2^-21) max|c|, EB = (2^-13 + 2^-21) max|h|
     const float CM = fmaxf(cn[2], cn[4]), HM = fmaxf(cn[3], cn[5]);
+    if (blockIdx.x == 0) {  // the same in every CTA of the head
+      if (threadIdx.x == 0) {
+        head_cn[2 * bh] = CM;
+        head_cn[2 * bh + 1] = HM;
+      }
+      if (threadIdx.x < 64) head_h[bh * 64 + threadIdx.x] = hs[threadIdx.x];
+    }
     const float EA = (1.220703125e-4f + 4.76837158e-7f) * CM;
     const float EB = (1.220703125e-4f + 4.76837158e-7f) * HM;
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
@@ -292,87 +299,10 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
         uint64_t cand = 0;  // bit c: cluster c can still win
 #pragma unroll
         for (int q = 0; q < 8; ++q) cand |= static_cast<uint64_t>(cm8[q]) << (8 * q);
-        int best = __ffsll(static_cast<long long>(cand)) - 1;
-        if ((cand & (cand - 1)) && __popcll(cand) <= 4) {
-          // Second filter: FP32 dot products of the (at most four)
-          // candidates in eight interleaved partial sums; their error vs
-          // the chain is <= (128 + 19) 2^-24 |v| |c| < 2^-16.7 |v| |c|, so
-          // E2 = 2^-15 (|v| max|c| + max|h|) is again at least twice the
-          // difference of the scores.
-          float st[4];
-          int cl[4];
-          float m2 = -__int_as_float(0x7f800000);
-          uint64_t rest = cand;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            cl[i] = rest ? __ffsll(static_cast<long long>(rest)) - 1 : -1;
-            rest = rest ? rest & (rest - 1) : 0;
-            st[i] = -__int_as_float(0x7f800000);
-            if (cl[i] >= 0) {
-              float a8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-              const float* crow = cb + cl[i] * D;
-#pragma unroll 4
-              for (int ch = 0; ch < 16; ++ch) {
-                const uint4 u = *reinterpret_cast<const uint4*>(vt + (ch >> 3) * V_HALF + sw128(r, 8 * (ch & 7)));
-                const float4 c0 = *reinterpret_cast<const float4*>(crow + 8 * ch);
-                const float4 c1 = *reinterpret_cast<const float4*>(crow + 8 * ch + 4);
-                a8[0] = __fmaf_rn(__uint_as_float(u.x << 16), c0.x, a8[0]);
-                a8[1] = __fmaf_rn(__uint_as_float(u.x & 0xFFFF0000u), c0.y, a8[1]);
-                a8[2] = __fmaf_rn(__uint_as_float(u.y << 16), c0.z, a8[2]);
-                a8[3] = __fmaf_rn(__uint_as_float(u.y & 0xFFFF0000u), c0.w, a8[3]);
-                a8[4] = __fmaf_rn(__uint_as_float(u.z << 16), c1.x, a8[4]);
-                a8[5] = __fmaf_rn(__uint_as_float(u.z & 0xFFFF0000u), c1.y, a8[5]);
-                a8[6] = __fmaf_rn(__uint_as_float(u.w << 16), c1.z, a8[6]);
-                a8[7] = __fmaf_rn(__uint_as_float(u.w & 0xFFFF0000u), c1.w, a8[7]);
-              }
-              st[i] = (((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]))) - hs[cl[i]];
-              m2 = fmaxf(m2, st[i]);
-            }
-          }
-          const float thr2 = m2 - 3.0517578125e-5f * (vn * CM + HM);
-          uint64_t c2 = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (cl[i] >= 0 && st[i] >= thr2) c2 |= 1ull << cl[i];
-          cand = c2;
-          best = __ffsll(static_cast<long long>(cand)) - 1;
-        }
-        if (cand & (cand - 1)) {
-          // exact chains of the candidates, up to four side by side, in
-          // ascending cluster order; the lowest index is kept on ties
-          float bs = 0.0f;
-          bool have = false;
-          uint64_t rest = cand;
-          while (rest) {
-            int cc[4];
-            int n = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              cc[q] = rest ? __ffsll(static_cast<long long>(rest)) - 1 : cc[0];
-              if (rest) {
-                rest &= rest - 1;
-                n = q + 1;
-              }
-            }
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 8
-            for (int d = 0; d < D; ++d) {
-              const float v = bf16_at(vt + (d >> 6) * V_HALF, r, d & 63);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) acc[q] = __fmaf_rn(v, cb[cc[q] * D + d], acc[q]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (q < n) {
-                const float e = acc[q] - hs[cc[q]];
-                if (!have || e > bs) {
-                  bs = e;
-                  best = cc[q];
-                  have = true;
-                }
-              }
-            }
-          }
+        const int best = __ffsll(static_cast<long long>(cand)) - 1;
+        if (cand & (cand - 1)) {  // left open: km_fixup decides
+          const uint32_t slot = atomicAdd(amb_count, 1u);
+          amb[slot] = KmAmb{bh * N + j, cand, vn, 0.0f};
         }
         labels[bh * N + j] = best;
       }
@@ -384,6 +314,104 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
   __syncthreads();
   tc_fence_after();
   if (warp == KT_WARP_MMA) tmem_dealloc(tmem, 128);
+}
+
+// The assignments the tensor-core filter left open, one thread each: the
+// second filter (at most four candidates), then the exact chains.  v comes
+// from the bf16 row in global memory, h_c as km_assign_tc computed it.
+__global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, int64_t N, int k,
+                                                const float* __restrict__ cent, int32_t* __restrict__ labels,
+                                                const KmAmb* __restrict__ amb, const uint32_t* __restrict__ count,
+                                                uint32_t* __restrict__ next_count,
+                                                const float* __restrict__ head_cn,
+                                                const float* __restrict__ head_h) {
+  const uint32_t n = *count;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *next_count = 0;  // for the next iteration's assign
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const KmAmb a = amb[i];
+    const int64_t bh = a.tok / N;
+    const uint16_t* vrow = V + a.tok * D;
+    const float* cb = cent + bh * k * D;
+    const float CM = head_cn[2 * bh], HM = head_cn[2 * bh + 1];
+    const float* hh = head_h + bh * 64;
+    uint64_t cand = a.cand;
+    int best = __ffsll(static_cast<long long>(cand)) - 1;
+    if (__popcll(cand) <= 4) {
+      // Second filter: FP32 dot products of the (at most four) candidates in
+      // eight interleaved partial sums; their error vs the chain is
+      // <= (128 + 19) 2^-24 |v| |c| < 2^-16.7 |v| |c|, so E2 = 2^-15 (|v|
+      // max|c| + max|h|) is again at least twice the difference of the scores.
+      float st[4];
+      int cl[4];
+      float m2 = -__int_as_float(0x7f800000);
+      uint64_t rest = cand;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        cl[q] = rest ? __ffsll(static_cast<long long>(rest)) - 1 : -1;
+        rest = rest ? rest & (rest - 1) : 0;
+        st[q] = -__int_as_float(0x7f800000);
+        if (cl[q] >= 0) {
+          float a8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+          const float* crow = cb + cl[q] * D;
+#pragma unroll 4
+          for (int ch = 0; ch < 16; ++ch) {
+            const uint4 u = *reinterpret_cast<const uint4*>(vrow + 8 * ch);
+            const float4 c0 = *reinterpret_cast<const float4*>(crow + 8 * ch);
+            const float4 c1 = *reinterpret_cast<const float4*>(crow + 8 * ch + 4);
+            a8[0] = __fmaf_rn(__uint_as_float(u.x << 16), c0.x, a8[0]);
+            a8[1] = __fmaf_rn(__uint_as_float(u.x & 0xFFFF0000u), c0.y, a8[1]);
+            a8[2] = __fmaf_rn(__uint_as_float(u.y << 16), c0.z, a8[2]);
+            a8[3] = __fmaf_rn(__uint_as_float(u.y & 0xFFFF0000u), c0.w, a8[3]);
+            a8[4] = __fmaf_rn(__uint_as_float(u.z << 16), c1.x, a8[4]);
+            a8[5] = __fmaf_rn(__uint_as_float(u.z & 0xFFFF0000u), c1.y, a8[5]);
+            a8[6] = __fmaf_rn(__uint_as_float(u.w << 16), c1.z, a8[6]);
+            a8[7] = __fmaf_rn(__uint_as_float(u.w & 0xFFFF0000u), c1.w, a8[7]);
+          }
+          st[q] = (((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]))) - hh[cl[q]];
+          m2 = fmaxf(m2, st[q]);
+        }
+      }
+      const float thr2 = m2 - 3.0517578125e-5f * (a.vn * CM + HM);
+      uint64_t c2 = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (cl[q] >= 0 && st[q] >= thr2) c2 |= 1ull << cl[q];
+      cand = c2;
+      best = __ffsll(static_cast<long long>(cand)) - 1;
+    }
+    if (cand & (cand - 1)) {
+      // exact chains of the candidates in ascending cluster order; the
+      // lowest index is kept on ties
+      float bs = 0.0f;
+      bool have = false;
+      for (uint64_t rest = cand; rest; rest &= rest - 1) {
+        const int c = __ffsll(static_cast<long long>(rest)) - 1;
+        const float* crow = cb + c * D;
+        float acc = 0.0f;
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ++ch) {  // d = 8 ch .. 8 ch + 7, in order
+          const uint4 u = *reinterpret_cast<const uint4*>(vrow + 8 * ch);
+          const float4 c0 = *reinterpret_cast<const float4*>(crow + 8 * ch);
+          const float4 c1 = *reinterpret_cast<const float4*>(crow + 8 * ch + 4);
+          acc = __fmaf_rn(__uint_as_float(u.x << 16), c0.x, acc);
+          acc = __fmaf_rn(__uint_as_float(u.x & 0xFFFF0000u), c0.y, acc);
+          acc = __fmaf_rn(__uint_as_float(u.y << 16), c0.z, acc);
+          acc = __fmaf_rn(__uint_as_float(u.y & 0xFFFF0000u), c0.w, acc);
+          acc = __fmaf_rn(__uint_as_float(u.z << 16), c1.x, acc);
+          acc = __fmaf_rn(__uint_as_float(u.z & 0xFFFF0000u), c1.y, acc);
+          acc = __fmaf_rn(__uint_as_float(u.w << 16), c1.z, acc);
+          acc = __fmaf_rn(__uint_as_float(u.w & 0xFFFF0000u), c1.w, acc);
+        }
+        const float e = acc - hh[c];
+        if (!have || e > bs) {
+          bs = e;
+          best = c;
+          have = true;
+        }
+      }
+    }
+    labels[a.tok] = best;
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 km_encoder() {
@@ -403,7 +431,8 @@ PFN_cuTensorMapEncodeTiled_v12000 km_encoder() {
 
 // V [BH, N, 128] bf16 as a 3-D tensor map with 64 x 128 boxes, 128B swizzle.
 cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
-                                int32_t* labels, uint32_t* err, cudaStream_t s) {
+                                int32_t* labels, const GroupWs& ws, int iter, uint32_t* err,
+                                cudaStream_t s) {
   if (k < 1 || k > 64) return cudaErrorInvalidValue;
   auto enc = km_encoder();
   if (!enc) return cudaErrorInvalidValue;
@@ -437,7 +466,16 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k,
   const int64_t waves = (total + 16 * slots - 1) / (16 * slots);
   const int64_t tpc = (total + slots * waves - 1) / (slots * waves);
   const dim3 grid(static_cast<unsigned>((ntile + tpc - 1) / tpc), static_cast<unsigned>(BH));
-  km_assign_tc<<<grid, KT_THREADS, KT_SMEM, s>>>(m, N, k, static_cast<int>(tpc), cent, labels, err);
+  // The open-assignment counter of this iteration starts at 0 (cleared
+  // before the first iteration, then by the previous fix-up).
+  uint32_t* cnt = ws.amb_count + (iter & 1);
+  km_assign_tc<<<grid, KT_THREADS, KT_SMEM, s>>>(m, N, k, static_cast<int>(tpc), cent, labels, ws.amb, cnt,
+                                                 ws.head_cn, ws.head_h, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  km_fixup<<<static_cast<unsigned>(slots * 2), 128, 0, s>>>(V, N, k, cent, labels, ws.amb, cnt,
+                                                            ws.amb_count + ((iter + 1) & 1), ws.head_cn,
+                                                            ws.head_h);
   return cudaGetLastError();
 }
 
