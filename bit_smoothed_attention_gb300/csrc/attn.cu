@@ -55,8 +55,7 @@
 // query 64-tiles keeps, in ascending order, two per tile: K arrives as two
 // 64-row boxes, V as two 64-key boxes in the 64B-swizzled layout (each half
 // of the PV B operand has its own indicator row), and the mean tile as two
-// 2 KiB halves.  A softmax warp whose query tile keeps neither block of a
-// tile skips its scores.
+// 2 KiB halves.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -156,15 +155,13 @@ __device__ __forceinline__ bool block_kept(const Params& p, int64_t bh, int qt0,
   return kept;
 }
 
-// The kept-union bits of blocks 32w .. 32w+31 read from the mask itself (for
-// blocks beyond the shared-memory bitmask; out of line, it is never hot).
-__device__ __noinline__ uint32_t kept_word_slow(const Params& p, int64_t bh, int qt0, int w) {
-  uint32_t m = 0;
-  for (int e = 0; e < 32; ++e) {
-    const int b = 32 * w + e;
-    if (b < p.nbp && block_kept(p, bh, qt0, b)) m |= 1u << e;
-  }
-  return m;
+// The first block at or after u that any of the CTA's query tiles keeps,
+// read from the mask itself (blocks beyond the shared-memory bitmask; out of
+// line, it is never hot), or -1.
+__device__ __noinline__ int next_kept_slow(const Params& p, int64_t bh, int qt0, int u) {
+  for (; u < p.nbp; ++u)
+    if (block_kept(p, bh, qt0, u)) return u;
+  return -1;
 }
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort) {
@@ -222,8 +219,9 @@ __device__ __forceinline__ uint32_t expcast4(float x0, float x1, float x2, float
               prmt(__float_as_uint(f23.x), __float_as_uint(f23.y), 0x0040u), 0x5410u);
 }
 
-// kMasked: the block-sparse instantiation (a tile mask is given); the dense
-// one compiles without the per-warp skip below.
+// kMasked: the block-sparse instantiation (a tile mask is given: the union
+// bitmask, the block-pair walk, 64-key boxes); the dense one compiles
+// without them.
 template <bool kMasked>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -299,15 +297,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // KV tiles as block pairs (x, y): dense (2t, 2t+1); masked, the kept
   // blocks two by two, y = -1 for the empty second half of an odd last tile;
   // x = -1 past the last tile.  Every role walks the same sequence.
-  auto kept_word = [&](int w) -> uint32_t {  // bits of blocks 32w .. 32w+31 (0 past nbp)
-    return w < KEPT_WORDS ? kept_w[w] : kept_word_slow(p, bh, qt0, w);
-  };
+  const int kept_lim = p.nbp < 32 * KEPT_WORDS ? p.nbp : 32 * KEPT_WORDS;
   auto next_kept = [&](int b) {
-    for (int u = b + 1; u < p.nbp; u = (u | 31) + 1) {
-      const uint32_t m = kept_word(u >> 5) >> (u & 31);
+    int u = b + 1;
+    for (; u < kept_lim; u = (u | 31) + 1) {  // bits past nbp are 0
+      const uint32_t m = kept_w[u >> 5] >> (u & 31);
       if (m) return u + __ffs(static_cast<int>(m)) - 1;
     }
-    return -1;
+    return u < p.nbp ? next_kept_slow(p, bh, qt0, u) : -1;
   };
   auto pair_after = [&](int b) -> int2 {  // the tile that starts after block b
     if constexpr (kMasked) {
@@ -323,7 +320,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int ntiles = p.ntile;
   if constexpr (kMasked) {
     int nb = 0;
-    for (int w = 0; w < nkw; ++w) nb += __popc(kept_word(w));
+    for (int w = 0; w < nkw && w < KEPT_WORDS; ++w) nb += __popc(kept_w[w]);
+    for (int u = 32 * KEPT_WORDS; u >= 0 && (u = next_kept_slow(p, bh, qt0, u)) >= 0; ++u) ++nb;
     ntiles = (nb + 1) >> 1;
   }
 
@@ -530,7 +528,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // by one; a 64-key block that a row does not keep is dropped as a
       // whole (no max contribution, bytes cleared).
       const bool partial = !__all_sync(FULL, lim_lo >= BLK && lim_hi >= TILE);
-      const bool skip = kMasked && !__any_sync(FULL, keep0 || keep1);
 
       if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS)))) break;
       tc_fence_after();
@@ -538,19 +535,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t w[32];  // the row's 128 E4M3 bytes
       float m_new, alpha;
       bool resc;
-      if (kMasked && skip) {
-        // This warp's query tile keeps neither 64-key block of the tile (its
-        // 32 rows share one query tile): no score is needed, the bytes are
-        // 0 and the maximum stays; only the barrier protocol runs.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_STAKEN + slot));
-#pragma unroll
-        for (int q = 0; q < 32; ++q) w[q] = 0u;
-        m_new = m_run;
-        resc = false;
-        alpha = 1.0f;
-      } else {
+      {
         {
           uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
           uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
