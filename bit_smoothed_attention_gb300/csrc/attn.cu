@@ -93,8 +93,8 @@ constexpr uint32_t SM_L = SM_MU + NS * MU_BYTES;
 constexpr uint32_t SM_P = SM_L + 2 * MU_BYTES;  // P of each slot, A operand of the PV MMA
 constexpr uint32_t SM_BAR = SM_P + 2 * TILE_BYTES;
 enum {
-  B_QFULL = 0,
-  B_FULL = 1,  // V(j) and its mean tile in stage j % NS, plus K(j+1)
+  B_QFULL = 0,  // + slot (dense: entry 0 for both Q tiles)
+  B_FULL = 2,   // V(j) and its mean tile in stage j's, plus K(j+1)
   B_KEMPTY = B_FULL + NS,
   B_VEMPTY = B_KEMPTY + NS,
   B_SFULL = B_VEMPTY + NS,
@@ -109,12 +109,12 @@ constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
 constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
 constexpr uint32_t SM_END = SM_ABORT + 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;  // slack for 1024-byte alignment
-// Masked: one bit per 64-key block, set when any of the CTA's query tiles
-// keeps it (the first 32 * KEPT_WORDS blocks; later ones are looked up in the
-// mask itself).
+// Masked: per slot, one bit per 64-key block, set when either of the slot's
+// two query tiles keeps it (the first 32 * KEPT_WORDS blocks; later ones are
+// looked up in the mask itself).
 constexpr uint32_t SM_KEPT = SM_END;
-constexpr int KEPT_WORDS = 448;
-constexpr uint32_t SMEM_BYTES_MASKED = SMEM_BYTES + 4 * KEPT_WORDS;
+constexpr int KEPT_WORDS = 224;  // per slot
+constexpr uint32_t SMEM_BYTES_MASKED = SMEM_BYTES + 2 * 4 * KEPT_WORDS;
 static_assert(SMEM_BYTES_MASKED <= 232448, "shared memory per CTA");
 
 constexpr uint32_t IDESC_QK = idesc(FMT_E4M3, FMT_E4M3, 128, 128);
@@ -143,24 +143,24 @@ struct Params {
   int debug_flags;
 };
 
-// Does any of the CTA's four query 64-tiles keep 64-key block b?
-__device__ __forceinline__ bool block_kept(const Params& p, int64_t bh, int qt0, int b) {
+// Does either of the query 64-tiles qa, qa + 1 keep 64-key block b?
+__device__ __forceinline__ bool block_kept(const Params& p, int64_t bh, int qa, int b) {
   const uint8_t* mcol = p.mask + (bh * p.nq64) * p.nbp + b;
   bool kept = false;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int qt = qt0 + q;
+  for (int q = 0; q < 2; ++q) {
+    const int qt = qa + q;
     kept |= qt < p.nq64 && mcol[static_cast<int64_t>(qt) * p.nbp] != 0;
   }
   return kept;
 }
 
-// The first block at or after u that any of the CTA's query tiles keeps,
-// read from the mask itself (blocks beyond the shared-memory bitmask; out of
-// line, it is never hot), or -1.
-__device__ __noinline__ int next_kept_slow(const Params& p, int64_t bh, int qt0, int u) {
+// The first block at or after u that the query tiles qa, qa + 1 keep, read
+// from the mask itself (blocks beyond the shared-memory bitmask; out of line,
+// it is never hot), or -1.
+__device__ __noinline__ int next_kept_slow(const Params& p, int64_t bh, int qa, int u) {
   for (; u < p.nbp; ++u)
-    if (block_kept(p, bh, qt0, u)) return u;
+    if (block_kept(p, bh, qa, u)) return u;
   return -1;
 }
 
@@ -238,11 +238,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int qt0 = q0 / BLK;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QFULL + 0), 1);
+    mbar_init(bar(B_QFULL + 1), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_KEMPTY + s), 2);  // one release per slot's MMA lane
-      mbar_init(bar(B_VEMPTY + s), 2);
+      // dense: both slots' MMA lanes release a stage; masked: its own slot's
+      mbar_init(bar(B_KEMPTY + s), kMasked ? 1 : 2);
+      mbar_init(bar(B_VEMPTY + s), kMasked ? 1 : 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
@@ -277,14 +279,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           make_uint4(v, v, v, v);
     }
   }
-  // Masked: the union bitmask of the blocks the CTA's query tiles keep.
+  // Masked: per slot, the bitmask of the blocks its two query tiles keep.
   uint32_t* kept_w = reinterpret_cast<uint32_t*>(sm + SM_KEPT);
   const int nkw = (p.nbp + 31) >> 5;
   if (kMasked) {
     for (int w = warp; w < nkw && w < KEPT_WORDS; w += NTHREADS / 32) {
       const int b = 32 * w + lane;
-      const uint32_t m = __ballot_sync(0xffffffffu, b < p.nbp && block_kept(p, bh, qt0, b));
-      if (lane == 0) kept_w[w] = m;
+#pragma unroll
+      for (int sl = 0; sl < 2; ++sl) {
+        const uint32_t m = __ballot_sync(0xffffffffu, b < p.nbp && block_kept(p, bh, qt0 + 2 * sl, b));
+        if (lane == 0) kept_w[sl * KEPT_WORDS + w] = m;
+      }
     }
   }
   fence_proxy_async_smem();
@@ -294,40 +299,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TSLOT);
 
-  // KV tiles as block pairs (x, y): dense (2t, 2t+1); masked, the kept
-  // blocks two by two, y = -1 for the empty second half of an odd last tile;
-  // x = -1 past the last tile.  Every role walks the same sequence.
+  // KV tiles as block pairs (x, y): dense, (2t, 2t+1) for both slots;
+  // masked, each slot walks the blocks its query tiles keep, two by two,
+  // y = -1 for the empty second half of an odd last tile; x = -1 past the
+  // last tile.  Every role of a slot walks the same sequence.
   const int kept_lim = p.nbp < 32 * KEPT_WORDS ? p.nbp : 32 * KEPT_WORDS;
-  auto next_kept = [&](int b) {
+  auto next_kept = [&](int sl, int b) {
+    const uint32_t* kw = kept_w + sl * KEPT_WORDS;
     int u = b + 1;
     for (; u < kept_lim; u = (u | 31) + 1) {  // bits past nbp are 0
-      const uint32_t m = kept_w[u >> 5] >> (u & 31);
+      const uint32_t m = kw[u >> 5] >> (u & 31);
       if (m) return u + __ffs(static_cast<int>(m)) - 1;
     }
-    return u < p.nbp ? next_kept_slow(p, bh, qt0, u) : -1;
+    return u < p.nbp ? next_kept_slow(p, bh, qt0 + 2 * sl, u) : -1;
   };
-  auto pair_after = [&](int b) -> int2 {  // the tile that starts after block b
+  auto pair_after = [&](int sl, int b) -> int2 {  // the slot's tile that starts after block b
     if constexpr (kMasked) {
-      const int x = next_kept(b);
-      return make_int2(x, x >= 0 ? next_kept(x) : -1);
+      const int x = next_kept(sl, b);
+      return make_int2(x, x >= 0 ? next_kept(sl, x) : -1);
     } else {
       return b + 2 < p.nbp ? make_int2(b + 1, b + 2) : make_int2(-1, -1);
     }
   };
-  auto next_pair = [&](int2 pr) { return pr.y < 0 ? make_int2(-1, -1) : pair_after(pr.y); };
+  auto next_pair = [&](int sl, int2 pr) { return pr.y < 0 ? make_int2(-1, -1) : pair_after(sl, pr.y); };
 
-  // Number of KV tiles this CTA processes (the same in every role).
-  int ntiles = p.ntile;
+  // Number of KV tiles of each slot (the same in every role).
+  int nt0 = p.ntile, nt1 = p.ntile;
   if constexpr (kMasked) {
-    int nb = 0;
-    for (int w = 0; w < nkw && w < KEPT_WORDS; ++w) nb += __popc(kept_w[w]);
-    for (int u = 32 * KEPT_WORDS; u >= 0 && (u = next_kept_slow(p, bh, qt0, u)) >= 0; ++u) ++nb;
-    ntiles = (nb + 1) >> 1;
+    auto count = [&](int sl) {
+      int nb = 0;
+      for (int w = 0; w < nkw && w < KEPT_WORDS; ++w) nb += __popc(kept_w[sl * KEPT_WORDS + w]);
+      for (int u = 32 * KEPT_WORDS; u >= 0 && (u = next_kept_slow(p, bh, qt0 + 2 * sl, u)) >= 0; ++u) ++nb;
+      return (nb + 1) >> 1;
+    };
+    nt0 = count(0);
+    nt1 = count(1);
   }
+  auto nt = [&](int sl) { return sl ? nt1 : nt0; };
+  // K/V/mean stages: dense, one ring of NS shared by both slots; masked, two
+  // stages of its own per slot.
+  constexpr int SN = kMasked ? 2 : NS;
 
-  if (warp == WARP_TMA) {
+  if (warp == WARP_TMA || (kMasked && warp == WARP_TMA + 1)) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !(p.debug_flags & 1) && ntiles > 0) {
+    // Dense: warp 2 loads both Q tiles and the shared K/V ring.  Masked:
+    // warp 2 + s loads slot s's Q tile and its own two stages.
+    const int ps = kMasked ? warp - WARP_TMA : 0;  // the slot whose sequence is walked
+    const int sbase = kMasked ? 2 * ps : 0;
+    if (lane == 0 && !(p.debug_flags & 1) && nt(ps) > 0) {
       const int h3 = static_cast<int>(bh);
       const float* mu = p.vmu_op + bh * p.nbp * (4 * D);  // 2 KiB per block
       // K of a tile: one 128-row box, or (masked) a 64-row box per block
@@ -350,24 +369,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       };
       // Q and the first K tile
-      int2 pr = pair_after(-1);
-      mbar_arrive_expect_tx(bar(B_QFULL), 3 * TILE_BYTES);
-      tma_load_3d(sb + SM_Q, &tmq, 0, q0, h3, bar(B_QFULL));
-      tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, h3, bar(B_QFULL));
-      load_k(sb + SM_K, pr, bar(B_QFULL));
-      // Step j brings V(j) and its mean tile into stage j % NS and K(j+1)
-      // into K stage (j+1) % NS, all on one barrier.  A K stage is free again
-      // once both slots' QK have read it, a V stage once both mean terms of
-      // its tile were issued.
+      int2 pr = pair_after(ps, -1);
+      const uint32_t qb = bar(B_QFULL + ps);
+      if constexpr (kMasked) {
+        mbar_arrive_expect_tx(qb, 2 * TILE_BYTES);
+        tma_load_3d(sb + SM_Q + ps * TILE_BYTES, &tmq, 0, q0 + 128 * ps, h3, qb);
+      } else {
+        mbar_arrive_expect_tx(qb, 3 * TILE_BYTES);
+        tma_load_3d(sb + SM_Q, &tmq, 0, q0, h3, qb);
+        tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, h3, qb);
+      }
+      load_k(sb + SM_K + sbase * TILE_BYTES, pr, qb);
+      // Step j brings V(j) and its mean tile into stage sbase + j % SN and
+      // K(j+1) into K stage sbase + (j+1) % SN, all on one barrier.  A K
+      // stage is free again once the QKs that read it were done, a V stage
+      // once the mean terms of its tile were issued (dense: both slots').
       for (int j = 0; pr.x >= 0 && !*abort; ++j) {
-        const int st = j % NS, stk = (j + 1) % NS;
-        const int2 pn = next_pair(pr);
-        if (j >= NS && !mbar_wait(bar(B_VEMPTY + st), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
+        const int st = sbase + j % SN, stk = sbase + (j + 1) % SN;
+        const int2 pn = next_pair(ps, pr);
+        if (j >= SN && !mbar_wait(bar(B_VEMPTY + st), ((j / SN) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
-        if (pn.x >= 0 && j + 1 >= NS &&
-            !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / NS) - 1) & 1, abort, WAIT_NS)) {
+        if (pn.x >= 0 && j + 1 >= SN &&
+            !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / SN) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
@@ -382,8 +407,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // One issuing lane per slot, so that one slot's waits never hold back
     // the other slot's MMAs; tcgen05.commit tracks each lane's own MMAs.
     const int s = warp - WARP_MMA;
+    const int ntiles = nt(s), nother = nt(1 - s);
+    const int sbase = kMasked ? 2 * s : 0;  // this slot's stages: sbase + j % SN
     if (lane == 0 && ntiles > 0) {
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort, WAIT_NS);
+      bool ok = mbar_wait(bar(B_QFULL + (kMasked ? s : 0)), 0, abort, WAIT_NS);
       tc_fence_after();
       // Descriptors are built once; a byte offset o advances them by o >> 4
       // in the start-address field (all of shared memory is below 256 KiB).
@@ -401,53 +428,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = mbar_wait(bar(b), par, abort, WAIT_NS);
         tc_fence_after();
       };
-      // S of this slot for the j-th kept tile (K in stage j % NS)
+      auto stg = [&](int j) { return sbase + j % SN; };
+      // S of this slot for its j-th tile
       auto qk = [&](int j) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f8(tmem + COL_S, adv(dQ, 32 * kk), adv(dK, (j % NS) * TILE_BYTES + 32 * kk), IDESC_QK, kk > 0);
+          mma_f8(tmem + COL_S, adv(dQ, 32 * kk), adv(dK, stg(j) * TILE_BYTES + 32 * kk), IDESC_QK, kk > 0);
         mma_commit(bar(B_SFULL + s));
-        mma_commit(bar(B_KEMPTY + j % NS));  // this slot has read K(j)
+        mma_commit(bar(B_KEMPTY + stg(j)));  // this slot has read K(j)
       };
-      // The single S buffer is taken in turn: S0(j) S1(j) S0(j+1) ...  QK
-      // of slot 0 for tile i waits until slot 1 holds S(i-1), QK of slot 1
-      // until slot 0 holds S(i).  Each QK goes ahead of the PV that the same
-      // slot's softmax releases later.
+      // The single S buffer is taken in turn: S0(0) S1(0) S0(1) S1(1) ...
+      // while both slots have tiles, then the slot with more goes on alone.
+      // QK of slot 0 for tile i waits until slot 1 holds S(i-1) (or, once
+      // slot 1 is done, until slot 0 holds its own S(i-1)); QK of slot 1
+      // until slot 0 holds S(i) (once slot 0 is done: its own S(i-1)).
+      // Dense, both slots have the same count.  Each QK goes ahead of the PV
+      // that the same slot's softmax releases later.
       auto pv = [&](int j) {  // mean term of tile j-1, then [O | l] += P(j) [V ; 1_b0 ; 1_b1]
         wt(B_PFULL + s, j & 1);  // P(j), and for j > 0 the mean operand of j-1
         if (!ok) return;
         if (j > 0) {
-          mma_tf32(dO, dL, adv(dMu, ((j - 1) % NS) * MU_BYTES), IDESC_TF32, 1);
-          mma_commit(bar(B_VEMPTY + (j - 1) % NS));  // this slot is done with V(j-1)
+          mma_tf32(dO, dL, adv(dMu, stg(j - 1) * MU_BYTES), IDESC_TF32, 1);
+          mma_commit(bar(B_VEMPTY + stg(j - 1)));  // this slot is done with V(j-1)
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t vo = kMasked ? (kk >> 1) * V_HALF + 32 * (kk & 1) : 32 * kk;
-          mma_f8(dO, adv(dP, 32 * kk), adv(dV, (j % NS) * V_STAGE + vo), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f8(dO, adv(dP, 32 * kk), adv(dV, stg(j) * V_STAGE + vo), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(B_ODONE + s));
       };
       for (int i = 0; ok && i <= ntiles; ++i) {
         if (i < ntiles) {
           // K(i) came with Q (i = 0) or with V(i-1)
-          if (i > 0) wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);
+          if (i > 0) wt(B_FULL + stg(i - 1), ((i - 1) / SN) & 1);
           if (s == 0) {
-            if (i > 0) wt(B_STAKEN + 1, (i - 1) & 1);
+            if (i > 0) wt(B_STAKEN + (i - 1 < nother ? 1 : 0), (i - 1) & 1);
           } else {
-            wt(B_STAKEN + 0, i & 1);
+            if (i < nother) {
+              wt(B_STAKEN + 0, i & 1);
+            } else if (i > 0) {
+              wt(B_STAKEN + 1, (i - 1) & 1);
+            }
           }
           if (!ok) break;
           qk(i);
         }
         if (i > 0) {
-          if (i == ntiles) wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);  // V of the last tile
+          if (i == ntiles) wt(B_FULL + stg(i - 1), ((i - 1) / SN) & 1);  // V of the last tile
           pv(i - 1);
         }
       }
       // the last tile's mean term (the softmax's extra p_full arrival)
       wt(B_PFULL + s, ntiles & 1);
       if (ok) {
-        mma_tf32(dO, dL, adv(dMu, ((ntiles - 1) % NS) * MU_BYTES), IDESC_TF32, 1);
+        mma_tf32(dO, dL, adv(dMu, stg(ntiles - 1) * MU_BYTES), IDESC_TF32, 1);
         mma_commit(bar(B_MDONE + s));
       }
       if (!ok) record_timeout(p, abort);
@@ -506,12 +541,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       else return *reinterpret_cast<const float2*>(ksc + pr.x);
     };
     auto mask_byte = [&](int b) -> uint8_t { return (kMasked && mrow && b >= 0) ? mrow[b] : 0; };
-    int2 pr = pair_after(-1);
+    const int ntiles = nt(slot);
+    int2 pr = pair_after(slot, -1);
     // loaded one tile ahead
     float2 ks = pair_scales(pr);
     uint8_t mk0 = mask_byte(pr.x), mk1 = mask_byte(pr.y);
     for (; pr.x >= 0; ++i) {
-      const int2 pn = next_pair(pr);
+      const int2 pn = next_pair(slot, pr);
       const float2 ks_n = pair_scales(pn);
       const uint8_t mk0_n = mask_byte(pn.x), mk1_n = mask_byte(pn.y);
       const bool keep0 = row_ok && (!kMasked || mk0 != 0);

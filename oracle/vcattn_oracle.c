@@ -41,7 +41,7 @@
 #define ORC_D 128
 #define ORC_BLK 64        /* quantisation / mean block (tokens)            */
 #define ORC_TILE 128      /* KV tile of the online-softmax recurrence      */
-#define ORC_GROUP 256     /* query rows that share one sequence of KV tiles */
+#define ORC_GROUP 128     /* query rows that share one sequence of KV tiles */
 #define ORC_UPD_CHUNK 512 /* token chunk of the centroid-sum order (R4)    */
 
 /* ------------------------------------------------------------------ */
@@ -439,8 +439,8 @@ int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int3
 /* ------------------------------------------------------------------ */
 /* Per head, for each requested query i (original order), a sequence of KV
  * tiles of two permuted 64-key blocks (b_0, b_1) (R9): the query rows go in
- * groups of 256 (four 64-row tiles); a group's blocks are, in ascending
- * order, those that any of its four tiles keeps (all blocks when dense),
+ * groups of 128 (two 64-row tiles); a group's blocks are, in ascending
+ * order, those that either of its two tiles keeps (all blocks when dense),
  * taken two per tile, and an odd last tile has no second block.  Dense, tile
  * t is (2t, 2t+1).  Per tile, with the keys of the blocks the row's own tile
  * keeps:

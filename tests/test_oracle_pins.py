@@ -476,9 +476,9 @@ def test_emul_mask_and_empty_rows(orc):
 
 @pytest.mark.parametrize("tau8", [0.0, 6.0])
 def test_emul_mask_schedule_pairs_group_blocks(orc, tau8):
-    """With a mask, the rows of a 256-row group (four query tiles) visit the
-    blocks that any of the group's tiles keeps, two per KV tile in ascending
-    order.  When all four tiles keep the same four blocks, the group's rows
+    """With a mask, the rows of a 128-row group (two query tiles) visit the
+    blocks that either of the group's tiles keeps, two per KV tile in
+    ascending order.  When four tiles keep the same four blocks, their rows
     equal the unmasked emulation of a 256-token problem cut down to those
     blocks (whose tiles are then (S0, S1), (S2, S3)); the masks of other
     groups do not matter, and a mask that keeps everything is no mask."""
@@ -514,15 +514,20 @@ def test_emul_mask_schedule_pairs_group_blocks(orc, tau8):
     # The grouping is by the group's union, not by each row's own blocks:
     # tile 12 keeps {1, 4}; with tile 13 keeping {2, 7} the group's tiles are
     # (1, 2), (4, 7), without it (1, 4), and tile 12's rows see the difference.
+    # Tile 14 is in the next 128-row group: what it keeps does not matter.
     ma = mask.copy()
     ma[12:16, :] = 0
     ma[12, [1, 4]] = 1
     mb = ma.copy()
     mb[13, [2, 7]] = 1
+    mc = ma.copy()
+    mc[14, [2, 7]] = 1
     ra = np.arange(12 * 64, 13 * 64)
     Oa = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=ma, qidx=ra)[0]
     Ob = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=mb, qidx=ra)[0]
+    Oc = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=mc, qidx=ra)[0]
     assert not np.array_equal(Oa, Ob)
+    assert np.array_equal(Oa, Oc)
     Of, Lf = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=np.ones((nq, nbp), np.uint8))
     Od, Ld = orc.attn_emul(pp, 0, N, SM, tau8=tau8)
     assert np.array_equal(Of, Od) and np.array_equal(Lf, Ld)
