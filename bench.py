@@ -253,7 +253,9 @@ def run_ours(args):
                            (Np // 128) * 4096)
     prep_gbs = prep_bytes / (t_prep * 1e-3) / 1e9
     kmeans_flop = 2.0 * N * w.k * 128 * w.iters * Hl * B
-    launches_per_step = (1 + 3 * w.iters + 2) + 3 + 1
+    # k-means: init, per iteration assign + fix-up + chunk sums + finalize,
+    # two sort kernels; preprocessing: 3; attention: 1
+    launches_per_step = (1 + 4 * w.iters + 2) + 3 + 1
 
     e2e = run_e2e(args, w, vcattn, dev, Q, K, V, mask, sm_scale, flops_step, world)
     out = {
