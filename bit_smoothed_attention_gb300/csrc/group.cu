@@ -35,12 +35,13 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
 }
 
 // Init: c_c = v[floor(c*N/k)].  grid (BH), block D.
-__global__ void km_init(const uint16_t* __restrict__ V, int64_t N, int k, float* __restrict__ cent) {
+__global__ void km_init(const uint16_t* __restrict__ V, RowLayout lv, int64_t N, int k,
+                        float* __restrict__ cent) {
   const int64_t bh = blockIdx.x;
   const int d = threadIdx.x;
   for (int c = 0; c < k; ++c) {
     const int64_t j = (static_cast<int64_t>(c) * N) / k;
-    cent[(bh * k + c) * D + d] = bf16f(V[(bh * N + j) * D + d]);
+    cent[(bh * k + c) * D + d] = bf16f(V[lv.head(bh) + j * lv.sn + d]);
   }
 }
 
@@ -52,7 +53,7 @@ __global__ void km_init(const uint16_t* __restrict__ V, int64_t N, int k, float*
 // +0 partial, 16-byte loads straight from global memory, several in flight
 // (the 16 threads of a cluster group read a whole 256-byte row).  grid
 // (nchunk, BH), block 256.
-__global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V,
+__global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V, RowLayout lv,
                                                   const int32_t* __restrict__ labels, int64_t N,
                                                   int k, int nchunk, float* __restrict__ part,
                                                   int32_t* __restrict__ cnt, uint32_t* err) {
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
   __syncthreads();
   // sums: clusters 4 cg .. 4 cg + 3, channels 8 q .. 8 q + 7
   const int cg = tid >> 4, q = tid & 15;
-  const uint16_t* vb = V + (bh * N + j0) * D + 8 * q;
+  const uint16_t* vb = V + lv.head(bh) + j0 * lv.sn + 8 * q;
   float* pg = part + (bh * nchunk + g) * static_cast<int64_t>(k) * D;
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
     for (; i + 8 <= i1; i += 8) {
       uint4 u[8];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) u[x] = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i + x]) * D);
+      for (int x = 0; x < 8; ++x) u[x] = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i + x]) * lv.sn);
 #pragma unroll
       for (int x = 0; x < 8; ++x) {
         const uint32_t w4[4] = {u[x].x, u[x].y, u[x].z, u[x].w};
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
       }
     }
     for (; i < i1; ++i) {
-      const uint4 u = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i]) * D);
+      const uint4 u = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i]) * lv.sn);
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -250,14 +251,14 @@ size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws) {
   return off;
 }
 
-cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
+cudaError_t launch_group(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k, int iters,
                          const float* init, int32_t* labels, int32_t* perm, float* centroids_out,
                          const GroupWs& ws, uint32_t* err, cudaStream_t s) {
   const int nchunk = static_cast<int>(ceil_div(N, UPD_CHUNK));
   float* cent = centroids_out ? centroids_out : ws.cent;
   cudaError_t e = cudaSuccess;
   if (!init) {
-    km_init<<<static_cast<unsigned>(BH), D, 0, s>>>(V, N, k, cent);
+    km_init<<<static_cast<unsigned>(BH), D, 0, s>>>(V, lv, N, k, cent);
     e = cudaGetLastError();
   } else if (init != cent) {
     // warm start: the iterations begin from the given centroids
@@ -269,9 +270,9 @@ cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int it
   if ((e = cudaMemsetAsync(ws.amb_count, 0, 2 * sizeof(uint32_t), s)) != cudaSuccess) return e;
   const dim3 gchunk(nchunk, static_cast<unsigned>(BH));
   for (int it = 0; it < iters; ++it) {
-    e = launch_km_assign_tc(V, BH, N, k, cent, labels, ws, it, err, s);
+    e = launch_km_assign_tc(V, lv, BH, N, k, cent, labels, ws, it, err, s);
     if (e != cudaSuccess) return e;
-    km_partial<<<gchunk, 256, 0, s>>>(V, labels, N, k, nchunk, ws.part, ws.cnt, err);
+    km_partial<<<gchunk, 256, 0, s>>>(V, lv, labels, N, k, nchunk, ws.part, ws.cnt, err);
     km_finalize<<<dim3(k, static_cast<unsigned>(BH)), D, 0, s>>>(ws.part, ws.cnt, nchunk, k, cent);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -21,6 +21,15 @@ __host__ __device__ inline int64_t npad(int64_t n) { return ((n + TILE - 1) / TI
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Where the rows of a bf16 [B, H, N, D] tensor live: element strides of the
+// batch, head and token dimensions (channels contiguous).  Row (bh, n) starts
+// at head(bh) + n * sn, bh = b * H + h.
+struct RowLayout {
+  int64_t sb, sh, sn, H;
+  __host__ __device__ int64_t head(int64_t bh) const { return (bh / H) * sb + (bh % H) * sh; }
+};
+inline RowLayout contiguous_rows(int64_t H, int64_t N) { return RowLayout{H * N * D, N * D, D, H}; }
+
 // ---- grouping (group.cu) ----
 // A token whose assignment the tensor-core filter left open: its flat index
 // b*H*N + h*N + j, the candidate clusters and its |v| bound.
@@ -43,13 +52,12 @@ struct GroupWs {
 size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws);
 // Tensor-core k-means assignment with an exact FP32 fallback (km_tc.cu);
 // 1 <= k <= 64.
-cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
-                                int32_t* labels, const GroupWs& ws, int iter, uint32_t* err,
-                                cudaStream_t s);
-cudaError_t launch_group(const uint16_t* V, int64_t BH, int64_t N, int k, int iters,
+cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k,
+                                const float* cent, int32_t* labels, const GroupWs& ws, int iter,
+                                uint32_t* err, cudaStream_t s);
+cudaError_t launch_group(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k, int iters,
                          const float* init, int32_t* labels, int32_t* perm, float* centroids_out,
-                         const GroupWs& ws,
-                         uint32_t* err, cudaStream_t s);
+                         const GroupWs& ws, uint32_t* err, cudaStream_t s);
 
 // ---- preprocessing (prep.cu) ----
 struct PrepOut {
@@ -61,8 +69,9 @@ struct PrepWs {
   uint32_t* vamax;  // [BH, D] V residual amax (float bits)
 };
 size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws);
-cudaError_t launch_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
-                        int64_t BH, int64_t N, const PrepOut& out, const PrepWs& ws, cudaStream_t s);
+cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* K, const RowLayout& lk,
+                        const uint16_t* V, const RowLayout& lv, const int32_t* perm, int64_t BH, int64_t N,
+                        const PrepOut& out, const PrepWs& ws, cudaStream_t s);
 
 // ---- attention (attn.cu) ----
 struct AttnArgs {
@@ -70,6 +79,7 @@ struct AttnArgs {
   const float *q_scale, *k_scale, *v_scale, *qmu, *vmu_op;
   const uint8_t* mask;  // nullable
   void* O;              // bf16, or f32 when out_f32
+  RowLayout lo;         // rows of O (in elements of O's type)
   int out_f32;
   float* lse2;          // nullable
   int64_t BH, N;

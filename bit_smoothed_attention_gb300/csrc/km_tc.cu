@@ -85,7 +85,8 @@ __device__ __forceinline__ uint32_t k16(int r, int e) {
 }
 
 __global__ void __launch_bounds__(KT_THREADS, 2)
-    km_assign_tc(const __grid_constant__ CUtensorMap tmv, int64_t N, int k, int tpc, const float* __restrict__ cent,
+    km_assign_tc(const __grid_constant__ CUtensorMap tmv, int64_t N, int64_t H, int k, int tpc,
+                 const float* __restrict__ cent,
                  int32_t* __restrict__ labels, KmAmb* __restrict__ amb, uint32_t* __restrict__ amb_count,
                  float* __restrict__ head_cn, float* __restrict__ head_h, uint32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
@@ -189,8 +190,9 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
         }
         const int row = static_cast<int>((tile0 + t) * 128);
         mbar_arrive_expect_tx(bar(KB_FULL + s), V_STAGE);
-        tma_load_3d(sb + SM_V + s * V_STAGE, &tmv, 0, row, static_cast<int>(bh), bar(KB_FULL + s));
-        tma_load_3d(sb + SM_V + s * V_STAGE + V_HALF, &tmv, 64, row, static_cast<int>(bh), bar(KB_FULL + s));
+        const int hh = static_cast<int>(bh % H), bb = static_cast<int>(bh / H);
+        tma_load_4d(sb + SM_V + s * V_STAGE, &tmv, 0, row, hh, bb, bar(KB_FULL + s));
+        tma_load_4d(sb + SM_V + s * V_STAGE + V_HALF, &tmv, 64, row, hh, bb, bar(KB_FULL + s));
       }
     }
   } else if (warp == KT_WARP_MMA) {
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
 // The assignments the tensor-core filter left open, one thread each: the
 // second filter (at most four candidates), then the exact chains.  v comes
 // from the bf16 row in global memory, h_c as km_assign_tc computed it.
-__global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, int64_t N, int k,
+__global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, RowLayout lv, int64_t N, int k,
                                                 const float* __restrict__ cent, int32_t* __restrict__ labels,
                                                 const KmAmb* __restrict__ amb, const uint32_t* __restrict__ count,
                                                 uint32_t* __restrict__ next_count,
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, 
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const KmAmb a = amb[i];
     const int64_t bh = a.tok / N;
-    const uint16_t* vrow = V + a.tok * D;
+    const uint16_t* vrow = V + lv.head(bh) + (a.tok - bh * N) * lv.sn;
     const float* cb = cent + bh * k * D;
     const float CM = head_cn[2 * bh], HM = head_cn[2 * bh + 1];
     const float* hh = head_h + bh * 64;
@@ -429,19 +431,23 @@ PFN_cuTensorMapEncodeTiled_v12000 km_encoder() {
 
 }  // namespace
 
-// V [BH, N, 128] bf16 as a 3-D tensor map with 64 x 128 boxes, 128B swizzle.
-cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k, const float* cent,
+// V as a 4-D tensor map (channels, tokens, heads, batches; strides from the
+// row layout) with 64 x 128 boxes, 128B swizzle.
+cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k,
+                                const float* cent,
                                 int32_t* labels, const GroupWs& ws, int iter, uint32_t* err,
                                 cudaStream_t s) {
   if (k < 1 || k > 64) return cudaErrorInvalidValue;
   auto enc = km_encoder();
   if (!enc) return cudaErrorInvalidValue;
   CUtensorMap m;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(V), dims, strides, box, es,
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(lv.H), static_cast<cuuint64_t>(BH / lv.H)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(lv.sn) * 2, static_cast<cuuint64_t>(lv.sh) * 2,
+                                 static_cast<cuuint64_t>(lv.sb) * 2};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(V), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -469,11 +475,11 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, int64_t BH, int64_t N, int k,
   // The open-assignment counter of this iteration starts at 0 (cleared
   // before the first iteration, then by the previous fix-up).
   uint32_t* cnt = ws.amb_count + (iter & 1);
-  km_assign_tc<<<grid, KT_THREADS, KT_SMEM, s>>>(m, N, k, static_cast<int>(tpc), cent, labels, ws.amb, cnt,
+  km_assign_tc<<<grid, KT_THREADS, KT_SMEM, s>>>(m, N, lv.H, k, static_cast<int>(tpc), cent, labels, ws.amb, cnt,
                                                  ws.head_cn, ws.head_h, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  km_fixup<<<static_cast<unsigned>(slots * 2), 128, 0, s>>>(V, N, k, cent, labels, ws.amb, cnt,
+  km_fixup<<<static_cast<unsigned>(slots * 2), 128, 0, s>>>(V, lv, N, k, cent, labels, ws.amb, cnt,
                                                             ws.amb_count + ((iter + 1) & 1), ws.head_cn,
                                                             ws.head_h);
   return cudaGetLastError();

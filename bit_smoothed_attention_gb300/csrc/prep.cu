@@ -88,7 +88,8 @@ __device__ __forceinline__ Src4 load_src(const int32_t* perm, int64_t r0, int64_
   }
   return s;
 }
-__device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, const Src4& src4) {
+// rows src of the head at `base`, `sn` elements apart
+__device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, int64_t sn, const Src4& src4) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int piece = u * 256 + static_cast<int>(threadIdx.x);
@@ -97,7 +98,7 @@ __device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, 
     if (src4.r[u] >= 0) {
       const int64_t src = src4.r[u];
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                   "l"(base + src * D + chunk * 8)
+                   "l"(base + src * sn + chunk * 8)
                    : "memory");
     } else {
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
@@ -161,8 +162,8 @@ __device__ __forceinline__ float2 block_max2(float a, float b, float* red) {
 // 256, dynamic shared memory STATS_SMEM (two stages of K and V tiles).
 constexpr int STATS_BPC = 8;
 constexpr int STATS_SMEM = 2 * 2 * TILE_SMEM;
-__global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K,
-                                                  const uint16_t* __restrict__ V,
+__global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K, RowLayout lk,
+                                                  const uint16_t* __restrict__ V, RowLayout lv,
                                                   const int32_t* __restrict__ perm, int64_t N,
                                                   int nb, int nbp, float* __restrict__ kbs,
                                                   float* __restrict__ v_mean,
@@ -173,13 +174,13 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * STATS_BPC;
   const int64_t b1 = b0 + STATS_BPC < nb ? b0 + STATS_BPC : nb;
   const int32_t* ph = perm ? perm + bh * N : nullptr;
-  const uint16_t* Kh = K + bh * N * D;
-  const uint16_t* Vh = V + bh * N * D;
+  const uint16_t* Kh = K + lk.head(bh);
+  const uint16_t* Vh = V + lv.head(bh);
   // gather indices of the next block to stage (one block ahead)
   Src4 nk = load_src(nullptr, b0 * BLK, N), nv = load_src(ph, b0 * BLK, N);
   auto stage = [&](int64_t b, int buf) {
-    stage_rows(ssm + buf * 2 * TILE_SMEM, Kh, nk);
-    stage_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, Vh, nv);
+    stage_rows(ssm + buf * 2 * TILE_SMEM, Kh, lk.sn, nk);
+    stage_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, Vh, lv.sn, nv);
     cp_commit();
     if (b + 1 < b1) {
       nk = load_src(nullptr, (b + 1) * BLK, N);
@@ -295,7 +296,8 @@ __global__ void __launch_bounds__(D * KM_SEG) prep_kmean(const float* __restrict
 constexpr int QUANT_BPC = 4;
 constexpr int QUANT_SMEM = 2 * 3 * TILE_SMEM + D * (BLK + 16) + D * 4 + 64;
 __global__ void __launch_bounds__(256) prep_quant(
-    const uint16_t* __restrict__ Q, const uint16_t* __restrict__ K, const uint16_t* __restrict__ V,
+    const uint16_t* __restrict__ Q, RowLayout lq, const uint16_t* __restrict__ K, RowLayout lk,
+    const uint16_t* __restrict__ V, RowLayout lv,
     const int32_t* __restrict__ perm, int64_t N, int64_t Npad, int nbp,
     const uint32_t* __restrict__ vamax, const float* __restrict__ k_mean,
     const float* __restrict__ v_scale, float* __restrict__ v_mean, uint8_t* __restrict__ q8,
@@ -314,9 +316,9 @@ __global__ void __launch_bounds__(256) prep_quant(
   Src4 nq = load_src(nullptr, b0 * BLK, N), ng = load_src(ph, b0 * BLK, N);
   auto stage = [&](int64_t b, int buf) {
     uint8_t* t = qsm + buf * 3 * TILE_SMEM;
-    stage_rows(t, Q + bh * N * D, nq);
-    stage_rows(t + TILE_SMEM, K + bh * N * D, ng);
-    stage_rows(t + 2 * TILE_SMEM, V + bh * N * D, ng);
+    stage_rows(t, Q + lq.head(bh), lq.sn, nq);
+    stage_rows(t + TILE_SMEM, K + lk.head(bh), lk.sn, ng);
+    stage_rows(t + 2 * TILE_SMEM, V + lv.head(bh), lv.sn, ng);
     cp_commit();
     if (b + 1 < b1) {
       nq = load_src(nullptr, (b + 1) * BLK, N);
@@ -471,8 +473,9 @@ size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws) {
   return off;
 }
 
-cudaError_t launch_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
-                        int64_t BH, int64_t N, const PrepOut& o, const PrepWs& ws, cudaStream_t s) {
+cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* K, const RowLayout& lk,
+                        const uint16_t* V, const RowLayout& lv, const int32_t* perm, int64_t BH, int64_t N,
+                        const PrepOut& o, const PrepWs& ws, cudaStream_t s) {
   const int64_t Np = npad(N);
   const int nbp = static_cast<int>(Np / BLK);
   const int nb = static_cast<int>(ceil_div(N, BLK));
@@ -487,12 +490,12 @@ cudaError_t launch_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
     attr_set = true;
   }
   prep_stats<<<dim3(static_cast<unsigned>(ceil_div(nb, STATS_BPC)), static_cast<unsigned>(BH)), 256,
-               STATS_SMEM, s>>>(K, V, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax);
+               STATS_SMEM, s>>>(K, lk, V, lv, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax);
   prep_kmean<<<static_cast<unsigned>(BH), dim3(D, KM_SEG), 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp,
                                                                    o.k_mean, o.v_scale);
   prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH)), 256,
                QUANT_SMEM, s>>>(
-      Q, K, V, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
+      Q, lq, K, lk, V, lv, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
       o.q_scale, o.k_scale, o.qmu, o.vmu_op);
   return cudaGetLastError();
 }

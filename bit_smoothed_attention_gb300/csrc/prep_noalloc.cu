@@ -95,8 +95,9 @@ extern "C" vcattn_status vcattn_prep_noalloc(const vcattn_shape* s, const void* 
   vc::prep_ws_layout(BH, s->N, base, &w);
   const vc::PrepOut o{out->q8, out->k8, out->r8t, out->q_scale, out->k_scale, out->v_scale,
                       out->k_mean, out->v_mean, out->qmu, out->vmu_op};
-  const cudaError_t e = vc::launch_prep(static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(K),
-                                        static_cast<const uint16_t*>(V), perm, BH, s->N, o, w,
+  const vc::RowLayout lc = vc::contiguous_rows(s->H, s->N);
+  const cudaError_t e = vc::launch_prep(static_cast<const uint16_t*>(Q), lc, static_cast<const uint16_t*>(K), lc,
+                                        static_cast<const uint16_t*>(V), lc, perm, BH, s->N, o, w,
                                         static_cast<cudaStream_t>(stream));
   return vc::from_cuda(e);
 }

@@ -64,6 +64,20 @@ vcattn_status check_shape(const vcattn_shape* s) {
 }
 
 
+// Row layout of a [B, H, N, D] tensor from caller strides (nullptr = contiguous).
+// Strides must be positive multiples of 8 elements (every row 16-byte aligned).
+bool rows_of(const vcattn_shape* s, const vcattn_strides* st, vc::RowLayout* out) {
+  if (!st) {
+    *out = vc::contiguous_rows(s->H, s->N);
+    return true;
+  }
+  const int64_t v[3] = {st->b, st->h, st->n};
+  for (int64_t x : v)
+    if (x <= 0 || (x & 7) != 0 || x > (int64_t(1) << 38)) return false;
+  *out = vc::RowLayout{st->b, st->h, st->n, s->H};
+  return true;
+}
+
 // Layout of the prepped tensors inside one buffer (256-byte aligned parts).
 size_t prepped_layout(const vcattn_shape* s, void* base, vcattn_prepped* out) {
   const int64_t BH = s->B * s->H, N = s->N, Np = vc::npad(N), nbp = Np / vc::BLK;
@@ -115,11 +129,13 @@ size_t vcattn_group_workspace_bytes(const vcattn_shape* s, int k) {
 }  // extern "C"
 
 namespace {
-vcattn_status group_impl(const vcattn_shape* s, const void* V, int k, int iters, const float* init,
-                         int32_t* labels, int32_t* perm, float* centroids, void* ws, size_t ws_bytes,
-                         void* stream) {
+vcattn_status group_impl(const vcattn_shape* s, const void* V, const vcattn_strides* sv, int k, int iters,
+                         const float* init, int32_t* labels, int32_t* perm, float* centroids, void* ws,
+                         size_t ws_bytes, void* stream) {
   vcattn_status st = check_shape(s);
   if (st != VCATTN_OK) return st;
+  vc::RowLayout lv{};
+  if (!rows_of(s, sv, &lv)) return VCATTN_ERR_INVALID_ARG;
   if (k < 1 || k > vc::KMAX) return VCATTN_ERR_UNSUPPORTED;
   if (iters < 1 || !V || !labels || !perm || !ws) return VCATTN_ERR_INVALID_ARG;
   if (!aligned16(V) || !aligned16(labels) || !aligned16(perm) || !aligned16(ws) ||
@@ -130,7 +146,7 @@ vcattn_status group_impl(const vcattn_shape* s, const void* V, int k, int iters,
   if (ws_bytes < vc::group_ws_layout(BH, s->N, k, ws, &w)) return VCATTN_ERR_INVALID_ARG;
   uint32_t* err = err_word(&st);
   if (!err) return st;
-  return from_cuda(vc::launch_group(static_cast<const uint16_t*>(V), BH, s->N, k, iters, init, labels,
+  return from_cuda(vc::launch_group(static_cast<const uint16_t*>(V), lv, BH, s->N, k, iters, init, labels,
                                     perm, centroids, w, err, static_cast<cudaStream_t>(stream)));
 }
 }  // namespace
@@ -140,14 +156,21 @@ extern "C" {
 vcattn_status vcattn_group(const vcattn_shape* s, const void* V, int k, int iters, int32_t* labels,
                            int32_t* perm, float* centroids, void* ws, size_t ws_bytes,
                            void* stream) {
-  return group_impl(s, V, k, iters, nullptr, labels, perm, centroids, ws, ws_bytes, stream);
+  return group_impl(s, V, nullptr, k, iters, nullptr, labels, perm, centroids, ws, ws_bytes, stream);
 }
 
 vcattn_status vcattn_group_warm(const vcattn_shape* s, const void* V, int k, int iters,
                                 const float* init_centroids, int32_t* labels, int32_t* perm,
                                 float* centroids, void* ws, size_t ws_bytes, void* stream) {
   if (!init_centroids) return VCATTN_ERR_INVALID_ARG;
-  return group_impl(s, V, k, iters, init_centroids, labels, perm, centroids, ws, ws_bytes, stream);
+  return group_impl(s, V, nullptr, k, iters, init_centroids, labels, perm, centroids, ws, ws_bytes, stream);
+}
+
+vcattn_status vcattn_group_strided(const vcattn_shape* s, const void* V, const vcattn_strides* sv, int k,
+                                   int iters, const float* init_centroids, int32_t* labels, int32_t* perm,
+                                   float* centroids, void* ws, size_t ws_bytes, void* stream) {
+  if (!sv) return VCATTN_ERR_INVALID_ARG;
+  return group_impl(s, V, sv, k, iters, init_centroids, labels, perm, centroids, ws, ws_bytes, stream);
 }
 
 size_t vcattn_prepped_bytes(const vcattn_shape* s) {
@@ -170,11 +193,16 @@ size_t vcattn_prep_workspace_bytes(const vcattn_shape* s) {
   return vc::prep_ws_layout(s->B * s->H, s->N, nullptr, nullptr);
 }
 
-vcattn_status vcattn_prep(const vcattn_shape* s, const void* Q, const void* K, const void* V,
-                          const int32_t* perm, const vcattn_prepped* out, void* ws,
-                          size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+vcattn_status prep_impl(const vcattn_shape* s, const void* Q, const vcattn_strides* sq, const void* K,
+                        const vcattn_strides* sk, const void* V, const vcattn_strides* sv, const int32_t* perm,
+                        const vcattn_prepped* out, void* ws, size_t ws_bytes, void* stream) {
   vcattn_status st = check_shape(s);
   if (st != VCATTN_OK) return st;
+  vc::RowLayout lq{}, lk{}, lv{};
+  if (!rows_of(s, sq, &lq) || !rows_of(s, sk, &lk) || !rows_of(s, sv, &lv)) return VCATTN_ERR_INVALID_ARG;
   if (!Q || !K || !V || !out || !ws || !prepped_ok(out)) return VCATTN_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(ws) ||
       (perm && !aligned16(perm)))
@@ -182,17 +210,36 @@ vcattn_status vcattn_prep(const vcattn_shape* s, const void* Q, const void* K, c
   const int64_t BH = s->B * s->H;
   vc::PrepWs w{};
   if (ws_bytes < vc::prep_ws_layout(BH, s->N, ws, &w)) return VCATTN_ERR_INVALID_ARG;
-  return from_cuda(vc::launch_prep(static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(K),
-                                   static_cast<const uint16_t*>(V), perm, BH, s->N,
+  return from_cuda(vc::launch_prep(static_cast<const uint16_t*>(Q), lq, static_cast<const uint16_t*>(K), lk,
+                                   static_cast<const uint16_t*>(V), lv, perm, BH, s->N,
                                    to_prep_out(out), w, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+vcattn_status vcattn_prep(const vcattn_shape* s, const void* Q, const void* K, const void* V,
+                          const int32_t* perm, const vcattn_prepped* out, void* ws,
+                          size_t ws_bytes, void* stream) {
+  return prep_impl(s, Q, nullptr, K, nullptr, V, nullptr, perm, out, ws, ws_bytes, stream);
+}
+
+vcattn_status vcattn_prep_strided(const vcattn_shape* s, const void* Q, const vcattn_strides* sq,
+                                  const void* K, const vcattn_strides* sk, const void* V,
+                                  const vcattn_strides* sv, const int32_t* perm, const vcattn_prepped* out,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (!sq || !sk || !sv) return VCATTN_ERR_INVALID_ARG;
+  return prep_impl(s, Q, sq, K, sk, V, sv, perm, out, ws, ws_bytes, stream);
 }
 
 namespace {
 vcattn_status attn_impl(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale, int off,
-                        float tau8, int out_f32, const uint8_t* tile_mask, void* O, float* lse2,
-                        void* stream, int debug_flags) {
+                        float tau8, int out_f32, const uint8_t* tile_mask, void* O, const vcattn_strides* so,
+                        float* lse2, void* stream, int debug_flags) {
   vcattn_status st = check_shape(s);
   if (st != VCATTN_OK) return st;
+  vc::RowLayout lo{};
+  if (!rows_of(s, so, &lo)) return VCATTN_ERR_INVALID_ARG;
   if (!in || !prepped_ok(in) || !O || !aligned16(O) || (lse2 && !aligned16(lse2)))
     return VCATTN_ERR_INVALID_ARG;
   if (!(sm_scale > 0.0f) || off < 0 || off > 8 || !(tau8 >= 0.0f) || tau8 > 8.0f * (8.75f - off) ||
@@ -211,6 +258,7 @@ vcattn_status attn_impl(const vcattn_shape* s, const vcattn_prepped* in, float s
   a.vmu_op = in->vmu_op;
   a.mask = tile_mask;
   a.O = O;
+  a.lo = lo;
   a.out_f32 = out_f32;
   a.lse2 = lse2;
   a.BH = s->B * s->H;
@@ -227,12 +275,19 @@ vcattn_status attn_impl(const vcattn_shape* s, const vcattn_prepped* in, float s
 vcattn_status vcattn_attn_ex(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
                              int off, float tau8, int out_f32, const uint8_t* tile_mask, void* O,
                              float* lse2, void* stream) {
-  return attn_impl(s, in, sm_scale, off, tau8, out_f32, tile_mask, O, lse2, stream, 0);
+  return attn_impl(s, in, sm_scale, off, tau8, out_f32, tile_mask, O, nullptr, lse2, stream, 0);
+}
+
+vcattn_status vcattn_attn_strided(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
+                                  int off, float tau8, int out_f32, const uint8_t* tile_mask, void* O,
+                                  const vcattn_strides* so, float* lse2, void* stream) {
+  if (!so) return VCATTN_ERR_INVALID_ARG;
+  return attn_impl(s, in, sm_scale, off, tau8, out_f32, tile_mask, O, so, lse2, stream, 0);
 }
 
 vcattn_status vcattn_test_attn_stalled(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
                                        void* O, float* lse2, void* stream) {
-  return attn_impl(s, in, sm_scale, 8, 6.0f, 0, nullptr, O, lse2, stream, 1);
+  return attn_impl(s, in, sm_scale, 8, 6.0f, 0, nullptr, O, nullptr, lse2, stream, 1);
 }
 
 vcattn_status vcattn_attn(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,

@@ -35,6 +35,11 @@ class Shape(ctypes.Structure):
                 ("D", ctypes.c_int64)]
 
 
+class Strides(ctypes.Structure):
+    """vcattn_strides: element strides of the batch, head and token dims."""
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("n", ctypes.c_int64)]
+
+
 class PreppedStruct(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("q8", "k8", "r8t", "q_scale", "k_scale", "v_scale", "k_mean", "v_mean", "qmu",
@@ -60,6 +65,14 @@ def _lib():
         lib.vcattn_group.argtypes = [SP, P, ctypes.c_int, ctypes.c_int, P, P, P, P, sz, P]
         lib.vcattn_group_warm.restype = st
         lib.vcattn_group_warm.argtypes = [SP, P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, sz, P]
+        SS = ctypes.POINTER(Strides)
+        lib.vcattn_group_strided.restype = st
+        lib.vcattn_group_strided.argtypes = [SP, P, SS, ctypes.c_int, ctypes.c_int, P, P, P, P, P, sz, P]
+        lib.vcattn_prep_strided.restype = st
+        lib.vcattn_prep_strided.argtypes = [SP, P, SS, P, SS, P, SS, P, ctypes.POINTER(PreppedStruct), P, sz, P]
+        lib.vcattn_attn_strided.restype = st
+        lib.vcattn_attn_strided.argtypes = [SP, ctypes.POINTER(PreppedStruct), ctypes.c_float, ctypes.c_int,
+                                            ctypes.c_float, ctypes.c_int, P, P, SS, P, P]
         lib.vcattn_prepped_bytes.restype = sz
         lib.vcattn_prepped_bytes.argtypes = [SP]
         lib.vcattn_prepped_carve.restype = st
@@ -121,6 +134,18 @@ def _req(x, dtype, name):
         raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
 
 
+def _rows(x, dtype, name):
+    """None for a contiguous [B,H,N,128] tensor, else its Strides (channels
+    contiguous, e.g. a (B,N,H,D) tensor viewed as (B,H,N,D) by transpose(1, 2))."""
+    if not (x.is_cuda and x.dtype == dtype and x.dim() == 4 and x.shape[-1] == 128):
+        raise ValueError("%s must be a CUDA %s tensor [B, H, N, 128]" % (name, dtype))
+    if x.is_contiguous():
+        return None
+    if x.stride(3) != 1:
+        raise ValueError("%s: the 128 channels must be contiguous" % name)
+    return Strides(x.stride(0), x.stride(1), x.stride(2))
+
+
 def npad(N):
     return int(_lib().vcattn_npad(N))
 
@@ -130,7 +155,7 @@ def group(V, k, iters=5, centroids=False, stream=None, init=None):
     Returns (labels, perm[, centroids]) as int32 [B,H,N] (and f32 [B,H,k,128]).
     init: starting centroids f32 [B,H,k,128] (vcattn_group_warm) instead of
     the evenly spaced seeds."""
-    _req(V, torch.bfloat16, "V")
+    sv = _rows(V, torch.bfloat16, "V")
     if init is not None:
         _req(init, torch.float32, "init")
         if tuple(init.shape) != (V.shape[0], V.shape[1], k, 128):
@@ -144,7 +169,11 @@ def group(V, k, iters=5, centroids=False, stream=None, init=None):
     if nbytes == 0:
         raise ValueError("unsupported grouping shape or k")
     ws = torch.empty(nbytes, dtype=torch.uint8, device=V.device)
-    if init is None:
+    if sv is not None:
+        _check(_lib().vcattn_group_strided(ctypes.byref(s), _ptr(V), ctypes.byref(sv), k, iters, _ptr(init),
+                                           _ptr(labels), _ptr(perm), _ptr(cent), _ptr(ws), nbytes,
+                                           _stream(stream)), "vcattn_group_strided")
+    elif init is None:
         _check(_lib().vcattn_group(ctypes.byref(s), _ptr(V), k, iters, _ptr(labels), _ptr(perm),
                                    _ptr(cent), _ptr(ws), nbytes, _stream(stream)), "vcattn_group")
     else:
@@ -196,18 +225,26 @@ class Prepped:
 
 
 def prep(Q, K, V, perm=None, out=None, stream=None):
-    """Fused K mean, gather by perm, V block demean and Q/K/V quantisers."""
-    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
-        _req(t, torch.bfloat16, n)
+    """Fused K mean, gather by perm, V block demean and Q/K/V quantisers.
+    Q, K, V may be strided views (channels contiguous)."""
+    rows = [_rows(t, torch.bfloat16, n) for t, n in ((Q, "Q"), (K, "K"), (V, "V"))]
     if perm is not None:
         _req(perm, torch.int32, "perm")
     pp = out if out is not None else Prepped(tuple(Q.shape), Q.device)
     s = _shape(Q)
     nbytes = _lib().vcattn_prep_workspace_bytes(ctypes.byref(s))
     ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
-    _check(_lib().vcattn_prep(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(perm),
-                              ctypes.byref(pp.struct), _ptr(ws), nbytes, _stream(stream)),
-           "vcattn_prep")
+    if all(r is None for r in rows):
+        _check(_lib().vcattn_prep(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(perm),
+                                  ctypes.byref(pp.struct), _ptr(ws), nbytes, _stream(stream)),
+               "vcattn_prep")
+    else:
+        B, H, N, D = Q.shape
+        st = [r if r is not None else Strides(H * N * D, N * D, D) for r in rows]
+        _check(_lib().vcattn_prep_strided(ctypes.byref(s), _ptr(Q), ctypes.byref(st[0]), _ptr(K),
+                                          ctypes.byref(st[1]), _ptr(V), ctypes.byref(st[2]), _ptr(perm),
+                                          ctypes.byref(pp.struct), _ptr(ws), nbytes, _stream(stream)),
+               "vcattn_prep_strided")
     return pp
 
 
@@ -223,10 +260,16 @@ def attn(pp, sm_scale, mask=None, off=8, tau8=6.0, out_f32=False, O=None, lse2=N
         lse2 = torch.empty(B, H, N, dtype=torch.float32, device=dev)
     if mask is not None:
         _req(mask, torch.uint8, "mask")
-    _check(_lib().vcattn_attn_ex(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale),
-                                 int(off), float(tau8), int(bool(out_f32)), _ptr(mask), _ptr(O),
-                                 _ptr(lse2),
-                                 _stream(stream)), "vcattn_attn")
+    so = _rows(O, torch.float32 if out_f32 else torch.bfloat16, "O")
+    if so is None:
+        _check(_lib().vcattn_attn_ex(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale),
+                                     int(off), float(tau8), int(bool(out_f32)), _ptr(mask), _ptr(O),
+                                     _ptr(lse2),
+                                     _stream(stream)), "vcattn_attn")
+    else:
+        _check(_lib().vcattn_attn_strided(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale),
+                                          int(off), float(tau8), int(bool(out_f32)), _ptr(mask), _ptr(O),
+                                          ctypes.byref(so), _ptr(lse2), _stream(stream)), "vcattn_attn_strided")
     return O, lse2
 
 

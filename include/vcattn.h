@@ -58,6 +58,15 @@ typedef enum {
 typedef struct {
   int64_t B, H, N, D;
 } vcattn_shape;
+/* Element strides of a [B, H, N, D] tensor whose D channels are contiguous:
+ * row (b, h, n) starts at element b*b_stride + h*h_stride + n*n_stride.  The
+ * *_strided entry points take them, e.g. for the (B, N, H, D) layout of
+ * many models: b = N*H*D, h = D, n = H*D.  Each must be a positive multiple
+ * of 8 elements (every row 16-byte aligned) below 2^38; rows must not
+ * overlap.  The other entry points take contiguous [B, H, N, D] tensors. */
+typedef struct {
+  int64_t b, h, n;
+} vcattn_strides;
 
 /* Output of vcattn_prep, input of vcattn_attn.  With Npad = 128*ceil(N/128)
  * rows and nbp = Npad/64 metadata blocks per head (blocks at or past
@@ -117,6 +126,13 @@ vcattn_status vcattn_group(const vcattn_shape* shape, const void* V, int k, int 
 vcattn_status vcattn_group_warm(const vcattn_shape* shape, const void* V, int k, int iters,
                                 const float* init_centroids, int32_t* labels, int32_t* perm,
                                 float* centroids, void* ws, size_t ws_bytes, void* stream);
+/* vcattn_group (init_centroids NULL) or vcattn_group_warm (not NULL) for a
+ * V with the row strides `sv` (required).  Same results as on a contiguous
+ * copy of V. */
+vcattn_status vcattn_group_strided(const vcattn_shape* shape, const void* V, const vcattn_strides* sv,
+                                   int k, int iters, const float* init_centroids, int32_t* labels,
+                                   int32_t* perm, float* centroids, void* ws, size_t ws_bytes,
+                                   void* stream);
 
 /* ----------------------------------------------------------- preprocessing */
 /* Fused preprocessing (TeleFuser PR #40 Changes; VC-Attention Key
@@ -139,6 +155,12 @@ size_t vcattn_prep_workspace_bytes(const vcattn_shape* shape);
 vcattn_status vcattn_prep(const vcattn_shape* shape, const void* Q, const void* K, const void* V,
                           const int32_t* perm, const vcattn_prepped* out,
                           void* ws, size_t ws_bytes, void* stream);
+/* vcattn_prep for Q, K and V with their own row strides (all three
+ * required).  The prepped tensors are the same as for contiguous copies. */
+vcattn_status vcattn_prep_strided(const vcattn_shape* shape, const void* Q, const vcattn_strides* sq,
+                                  const void* K, const vcattn_strides* sk, const void* V,
+                                  const vcattn_strides* sv, const int32_t* perm,
+                                  const vcattn_prepped* out, void* ws, size_t ws_bytes, void* stream);
 
 /* Preprocessing without a caller-provided workspace.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot
@@ -195,6 +217,11 @@ vcattn_status vcattn_attn(const vcattn_shape* shape, const vcattn_prepped* in, f
 vcattn_status vcattn_attn_ex(const vcattn_shape* shape, const vcattn_prepped* in, float sm_scale,
                              int off, float tau8, int out_f32, const uint8_t* tile_mask, void* O,
                              float* lse2, void* stream);
+/* vcattn_attn_ex writing O with the row strides `so` (required; in elements
+ * of O's type, bf16 or f32).  lse2 stays a contiguous [B,H,N] array. */
+vcattn_status vcattn_attn_strided(const vcattn_shape* shape, const vcattn_prepped* in, float sm_scale,
+                                  int off, float tau8, int out_f32, const uint8_t* tile_mask, void* O,
+                                  const vcattn_strides* so, float* lse2, void* stream);
 
 /* One call = vcattn_prep into `ws` followed by vcattn_attn.  perm is the
  * output of vcattn_group (or of an earlier step, or NULL = identity). */

@@ -157,3 +157,23 @@ def test_group_warm_validation_without_gpu(lib):
                                  1 << 30, None) == 1
     assert lib.vcattn_group_warm(ctypes.byref(s), fake, 65, 1, fake, fake, fake, None, fake, 1 << 30,
                                  None) == 2
+
+
+def test_strided_validation_without_gpu(lib):
+    """The strided entry points need strides, and each stride must be a
+    positive multiple of 8 elements."""
+    from bit_smoothed_attention_gb300.vcattn import PreppedStruct, Strides
+    P = ctypes.c_void_p
+    s = _shape()
+    fake = P(1 << 20)
+    good = Strides(2 * 1000 * 128, 128, 2 * 128)
+    for bad in (Strides(0, 128, 256), Strides(2 * 1000 * 128, 100, 256), Strides(-8, 128, 256)):
+        assert lib.vcattn_group_strided(ctypes.byref(s), fake, ctypes.byref(bad), 8, 1, None, fake, fake,
+                                        None, fake, 1 << 30, None) == 1
+    assert lib.vcattn_group_strided(ctypes.byref(s), fake, None, 8, 1, None, fake, fake, None, fake,
+                                    1 << 30, None) == 1
+    pp = PreppedStruct()
+    assert lib.vcattn_prep_strided(ctypes.byref(s), fake, ctypes.byref(good), fake, None, fake,
+                                   ctypes.byref(good), None, ctypes.byref(pp), fake, 1 << 30, None) == 1
+    assert lib.vcattn_attn_strided(ctypes.byref(s), ctypes.byref(pp), ctypes.c_float(0.1), 8,
+                                   ctypes.c_float(6.0), 0, None, fake, None, None, None) == 1

@@ -344,6 +344,40 @@ def test_fwd_host_back_to_back_calls_share_the_workspace(vc):
     assert torch.equal(hO[0], refs[0]) and torch.equal(hO[1], refs[1])
 
 
+@pytest.mark.parametrize("B,H,N,masked", [(2, 3, 1000, False), (1, 4, 777, True)])
+def test_strided_bnhd_inputs_and_output(vc, B, H, N, masked):
+    """Q, K, V stored as (B, N, H, D) and passed as strided (B, H, N, D) views
+    give the labels, permutation, centroids, prepped bytes and output of
+    contiguous copies, bit for bit; O can be written back in the (B, N, H, D)
+    layout too (bf16 and f32)."""
+    k = 8
+    g = torch.Generator(device="cuda").manual_seed(800 + N)
+    x = [(torch.randn(B, N, H, 128, generator=g, device="cuda") * (1 + i)).to(torch.bfloat16)
+         for i in range(3)]
+    Qv, Kv, Vv = (t.transpose(1, 2) for t in x)          # strided views
+    Qc, Kc, Vc = (t.contiguous() for t in (Qv, Kv, Vv))
+    assert not Vv.is_contiguous()
+    l_v, p_v, c_v = vc.group(Vv, k, 3, centroids=True)
+    l_c, p_c, c_c = vc.group(Vc, k, 3, centroids=True)
+    assert torch.equal(l_v, l_c) and torch.equal(p_v, p_c) and torch.equal(c_v, c_c)
+    l_w, _, c_w = vc.group(Vv, k, 1, centroids=True, init=c_c)
+    l_w2, _, c_w2 = vc.group(Vc, k, 1, centroids=True, init=c_c)
+    assert torch.equal(l_w, l_w2) and torch.equal(c_w, c_w2)
+    pp_v = vc.prep(Qv, Kv, Vv, p_c)
+    pp_c = vc.prep(Qc, Kc, Vc, p_c)
+    for key, val in pp_c.views().items():
+        assert torch.equal(pp_v.views()[key], val), key
+    mask = W.make_tile_mask(B, H, N, 801, keep_frac=0.3).cuda() if masked else None
+    for out_f32 in (False, True):
+        dt = torch.float32 if out_f32 else torch.bfloat16
+        O_c, L_c = vc.attn(pp_c, SM, mask=mask, out_f32=out_f32)
+        O_bnhd = torch.zeros(B, N, H, 128, dtype=dt, device="cuda")
+        _, L_v = vc.attn(pp_c, SM, mask=mask, out_f32=out_f32, O=O_bnhd.transpose(1, 2))
+        torch.cuda.synchronize()
+        assert vc.last_device_error() == 0
+        assert torch.equal(O_bnhd.transpose(1, 2), O_c) and torch.equal(L_v, L_c)
+
+
 # ------------------------------------------------- the bench configuration
 def test_live_workload_sampled(vc, orc):
     """The 32,626-token workload in the launch configuration the benchmark
