@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int e = 0; e < 32; ++e)
             y[e] = __uint_as_float(o[e]) * p.v_scale[bh * D + 32 * c + e] * inv_l;
           if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + p.lo.head(bh) + row * p.lo.sn + 32 * c);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + p.lo.head(bh) + p.lo.row(row) + 32 * c);
 #pragma unroll
             for (int e = 0; e < 8; ++e) dst[e] = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
           } else {
@@ -738,7 +738,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const __nv_bfloat162 v2 = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
               pk[e] = *reinterpret_cast<const uint32_t*>(&v2);
             }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.O) + p.lo.head(bh) + row * p.lo.sn + 32 * c);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.O) + p.lo.head(bh) + p.lo.row(row) + 32 * c);
 #pragma unroll
             for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
           }
@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (row_ok && ntiles == 0) {
       const int nvec = p.out_f32 ? 32 : 16;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.O) +
-                                            (p.lo.head(bh) + row * p.lo.sn) * (p.out_f32 ? 4 : 2));
+                                            (p.lo.head(bh) + p.lo.row(row)) * (p.out_f32 ? 4 : 2));
       for (int e = 0; e < nvec; ++e) dst[e] = make_uint4(0, 0, 0, 0);
     }
     if (row_ok && p.lse2) {

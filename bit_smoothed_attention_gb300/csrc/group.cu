@@ -41,7 +41,7 @@ __global__ void km_init(const uint16_t* __restrict__ V, RowLayout lv, int64_t N,
   const int d = threadIdx.x;
   for (int c = 0; c < k; ++c) {
     const int64_t j = (static_cast<int64_t>(c) * N) / k;
-    cent[(bh * k + c) * D + d] = bf16f(V[lv.head(bh) + j * lv.sn + d]);
+    cent[(bh * k + c) * D + d] = bf16f(V[lv.head(bh) + lv.row(j) + d]);
   }
 }
 
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
   __syncthreads();
   // sums: clusters 4 cg .. 4 cg + 3, channels 8 q .. 8 q + 7
   const int cg = tid >> 4, q = tid & 15;
-  const uint16_t* vb = V + lv.head(bh) + j0 * lv.sn + 8 * q;
+  const uint16_t* vb = V + lv.head(bh) + lv.row(j0) + 8 * q;
   float* pg = part + (bh * nchunk + g) * static_cast<int64_t>(k) * D;
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
     for (; i + 8 <= i1; i += 8) {
       uint4 u[8];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) u[x] = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i + x]) * lv.sn);
+      for (int x = 0; x < 8; ++x) u[x] = *reinterpret_cast<const uint4*>(vb + lv.row(order[i + x]));
 #pragma unroll
       for (int x = 0; x < 8; ++x) {
         const uint32_t w4[4] = {u[x].x, u[x].y, u[x].z, u[x].w};
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
       }
     }
     for (; i < i1; ++i) {
-      const uint4 u = *reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(order[i]) * lv.sn);
+      const uint4 u = *reinterpret_cast<const uint4*>(vb + lv.row(order[i]));
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {

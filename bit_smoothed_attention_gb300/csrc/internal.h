@@ -23,12 +23,17 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 // Where the rows of a bf16 [B, H, N, D] tensor live: element strides of the
 // batch, head and token dimensions (channels contiguous).  Row (bh, n) starts
-// at head(bh) + n * sn, bh = b * H + h.
+// at head(bh) + row(n), bh = b * H + h.  The token stride is below 2^31 and
+// n below 2^30, so row(n) is one 32 x 32 -> 64-bit multiply.
 struct RowLayout {
-  int64_t sb, sh, sn, H;
+  int64_t sb, sh, H;
+  int32_t sn, pad;
   __host__ __device__ int64_t head(int64_t bh) const { return (bh / H) * sb + (bh % H) * sh; }
+  __host__ __device__ int64_t row(int64_t n) const {
+    return static_cast<int64_t>(static_cast<int32_t>(n)) * static_cast<int64_t>(sn);
+  }
 };
-inline RowLayout contiguous_rows(int64_t H, int64_t N) { return RowLayout{H * N * D, N * D, D, H}; }
+inline RowLayout contiguous_rows(int64_t H, int64_t N) { return RowLayout{H * N * D, N * D, H, D, 0}; }
 
 // ---- grouping (group.cu) ----
 // A token whose assignment the tensor-core filter left open: its flat index

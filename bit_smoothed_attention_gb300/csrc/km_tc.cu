@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, 
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const KmAmb a = amb[i];
     const int64_t bh = a.tok / N;
-    const uint16_t* vrow = V + lv.head(bh) + (a.tok - bh * N) * lv.sn;
+    const uint16_t* vrow = V + lv.head(bh) + lv.row(a.tok - bh * N);
     const float* cb = cent + bh * k * D;
     const float CM = head_cn[2 * bh], HM = head_cn[2 * bh + 1];
     const float* hh = head_h + bh * 64;

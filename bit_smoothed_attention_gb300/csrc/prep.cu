@@ -89,7 +89,7 @@ __device__ __forceinline__ Src4 load_src(const int32_t* perm, int64_t r0, int64_
   return s;
 }
 // rows src of the head at `base`, `sn` elements apart
-__device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, int64_t sn, const Src4& src4) {
+__device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, int32_t sn, const Src4& src4) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int piece = u * 256 + static_cast<int>(threadIdx.x);
@@ -98,7 +98,7 @@ __device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, 
     if (src4.r[u] >= 0) {
       const int64_t src = src4.r[u];
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                   "l"(base + src * sn + chunk * 8)
+                   "l"(base + static_cast<int64_t>(static_cast<int32_t>(src)) * sn + chunk * 8)
                    : "memory");
     } else {
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);

@@ -74,7 +74,8 @@ bool rows_of(const vcattn_shape* s, const vcattn_strides* st, vc::RowLayout* out
   const int64_t v[3] = {st->b, st->h, st->n};
   for (int64_t x : v)
     if (x <= 0 || (x & 7) != 0 || x > (int64_t(1) << 38)) return false;
-  *out = vc::RowLayout{st->b, st->h, st->n, s->H};
+  if (st->n >= (int64_t(1) << 31)) return false;
+  *out = vc::RowLayout{st->b, st->h, s->H, static_cast<int32_t>(st->n), 0};
   return true;
 }
 

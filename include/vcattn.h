@@ -62,8 +62,9 @@ typedef struct {
  * row (b, h, n) starts at element b*b_stride + h*h_stride + n*n_stride.  The
  * *_strided entry points take them, e.g. for the (B, N, H, D) layout of
  * many models: b = N*H*D, h = D, n = H*D.  Each must be a positive multiple
- * of 8 elements (every row 16-byte aligned) below 2^38; rows must not
- * overlap.  The other entry points take contiguous [B, H, N, D] tensors. */
+ * of 8 elements (every row 16-byte aligned) below 2^38, n below 2^31; rows
+ * must not overlap.  The other entry points take contiguous [B, H, N, D]
+ * tensors. */
 typedef struct {
   int64_t b, h, n;
 } vcattn_strides;
