@@ -825,13 +825,16 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   p.off = static_cast<float>(a.off);
   p.err = a.err;
   p.debug_flags = a.debug_flags;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory limit is a per-device attribute of each kernel
+  static bool attr_set[MAX_DEVICES] = {};
+  int dev = 0;
+  if (!current_device(&dev)) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_MASKED);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   const dim3 grid(static_cast<unsigned>(ceil_div(Np, CTA_ROWS)), static_cast<unsigned>(a.BH));
   if (p.mask)

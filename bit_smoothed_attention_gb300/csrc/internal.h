@@ -35,6 +35,13 @@ struct RowLayout {
 };
 inline RowLayout contiguous_rows(int64_t H, int64_t N) { return RowLayout{H * N * D, N * D, H, D, 0}; }
 
+// The current device, for per-device host state (function attributes and
+// SM counts are per device); false when it is not one of the first 64.
+constexpr int MAX_DEVICES = 64;
+inline bool current_device(int* dev) {
+  return cudaGetDevice(dev) == cudaSuccess && *dev >= 0 && *dev < MAX_DEVICES;
+}
+
 // ---- grouping (group.cu) ----
 // A token whose assignment the tensor-core filter left open: its flat index
 // b*H*N + h*N + j, the candidate clusters and its |v| bound.

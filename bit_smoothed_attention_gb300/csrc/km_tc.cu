@@ -451,22 +451,25 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t 
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // per device: the kernel's shared-memory limit and the SM count
+  static bool attr_set[MAX_DEVICES] = {};
+  static int slots_of[MAX_DEVICES] = {};
+  int dev = 0;
+  if (!current_device(&dev)) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(km_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, KT_SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   // Tiles per CTA: at most 16 (the per-CTA set-up is amortised over them),
   // chosen so that the CTAs fill whole waves of two CTAs per SM.
-  static int slots = 0;
-  if (!slots) {
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!slots_of[dev]) {
+    int sms = 0;
+    const cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    slots = 2 * (sms > 0 ? sms : 1);
+    slots_of[dev] = 2 * (sms > 0 ? sms : 1);
   }
+  const int slots = slots_of[dev];
   const int64_t ntile = (N + 127) / 128;
   const int64_t total = ntile * BH;
   const int64_t waves = (total + 16 * slots - 1) / (16 * slots);

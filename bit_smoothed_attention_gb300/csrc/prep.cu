@@ -481,13 +481,16 @@ cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* 
   const int nb = static_cast<int>(ceil_div(N, BLK));
   cudaError_t e = cudaMemsetAsync(ws.vamax, 0, static_cast<size_t>(BH) * D * 4, s);
   if (e != cudaSuccess) return e;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory limit is a per-device attribute of each kernel
+  static bool attr_set[MAX_DEVICES] = {};
+  int dev = 0;
+  if (!current_device(&dev)) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(prep_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, STATS_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prep_quant, cudaFuncAttributeMaxDynamicSharedMemorySize, QUANT_SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   prep_stats<<<dim3(static_cast<unsigned>(ceil_div(nb, STATS_BPC)), static_cast<unsigned>(BH)), 256,
                STATS_SMEM, s>>>(K, lk, V, lv, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax);
