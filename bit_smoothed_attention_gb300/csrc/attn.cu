@@ -20,7 +20,8 @@
 //
 // CTA = 256 query rows (two 128-row slots) of one (b, h).  Warps 0 and 1
 // issue the MMAs of slot 0 and slot 1 from one lane each (warp 0 also
-// allocates TMEM), warp 2 issues the TMA loads, warp 3 is idle, warps 4-7 run
+// allocates TMEM), warp 2 issues the TMA loads (with a tile mask: those of
+// slot 0, and warp 3 those of slot 1; dense, warp 3 is idle), warps 4-7 run
 // the softmax of slot 0 (thread = row = TMEM lane quarter warp & 3) and warps
 // 8-11 that of slot 1.  The issuing warps have the lowest warp numbers so that
 // the warp schedulers favour them over the softmax warps sharing their
@@ -50,12 +51,14 @@
 // done" implies that MEAN(t-2) is done.
 //
 // A KV tile is two 64-key blocks, one per 64-column half of S and P.  Dense,
-// tile t holds blocks 2t and 2t+1 (one 128-row TMA box of K and of V).  With
-// a tile mask, the CTA streams only the blocks that at least one of its four
-// query 64-tiles keeps, in ascending order, two per tile: K arrives as two
-// 64-row boxes, V as two 64-key boxes in the 64B-swizzled layout (each half
-// of the PV B operand has its own indicator row), and the mean tile as two
-// 2 KiB halves.
+// tile t holds blocks 2t and 2t+1 (one 128-row TMA box of K and of V) for
+// both slots, through one ring of NS stages.  With a tile mask, each slot
+// streams only the blocks that either of its two query 64-tiles keeps, in
+// ascending order, two per tile, through two stages of its own: K arrives as
+// two 64-row boxes, V as two 64-key boxes in the 64B-swizzled layout (each
+// half of the PV B operand has its own indicator row), and the mean tile as
+// two 2 KiB halves.  The slots then have different tile counts; S is taken
+// in turn while both have tiles, and the slot with more goes on alone.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -70,7 +73,7 @@ namespace vc {
 namespace {
 
 constexpr int NS = 4;          // K/V/mean pipeline stages
-constexpr int NTHREADS = 384;  // one MMA warp per slot, TMA warp, idle warp, 8 softmax warps
+constexpr int NTHREADS = 384;  // one MMA warp per slot, two TMA warps, 8 softmax warps
 constexpr int WARP_MMA = 0;    // + slot
 constexpr int WARP_TMA = 2;
 constexpr int WARP_SOFTMAX = 4;
