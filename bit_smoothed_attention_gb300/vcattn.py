@@ -274,7 +274,16 @@ def attn(pp, sm_scale, mask=None, off=8, tau8=6.0, out_f32=False, O=None, lse2=N
 
 
 def fwd(Q, K, V, perm, sm_scale, mask=None, O=None, lse2=None, ws=None, stream=None):
-    """vcattn_fwd: prep into a workspace + attention, one call."""
+    """vcattn_fwd: prep into a workspace + attention, one call (contiguous
+    tensors; strided ones go through prep() and attn())."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _req(t, torch.bfloat16, n)
+    if perm is not None:
+        _req(perm, torch.int32, "perm")
+    if mask is not None:
+        _req(mask, torch.uint8, "mask")
+    if O is not None:
+        _req(O, torch.bfloat16, "O")
     s = _shape(Q)
     nbytes = _lib().vcattn_fwd_workspace_bytes(ctypes.byref(s))
     if ws is None:
