@@ -262,6 +262,22 @@ def test_attn_mask_parity(vc, orc):
     assert np.all(g32[192:256] == 0) and np.all(np.isneginf(res[0][2][192:256]))
 
 
+def test_attn_mask_empty_slot(vc, orc):
+    """Both query tiles of one 128-row slot keep no block (that slot has no
+    KV tile at all) while the other slot of the same CTA, and other CTAs,
+    have work: the empty rows get O = 0 and lse2 = -inf, the rest matches
+    the oracle."""
+    N, H = 1000, 1
+    nq, nbp = (N + 63) // 64, vc.npad(N) // 64
+    mask = np.asarray(W.make_tile_mask(1, H, N, 404, keep_frac=0.3), np.uint8).copy()
+    mask[0, 0, 6:8, :] = 0                 # CTA 1, slot 1: query tiles 6 and 7
+    res = _attn_case(vc, orc, N, H, 8, 405, mask=mask)
+    _check_attn(res)
+    g32, gl = res[0][0], res[0][2]
+    assert np.all(g32[384:512] == 0) and np.all(np.isneginf(gl[384:512]))
+    assert np.all(np.isfinite(gl[256:384]))
+
+
 @pytest.mark.parametrize("kind", ["even", "odd", "one", "ones"])
 def test_attn_mask_structures(vc, orc, kind):
     """Masks whose kept blocks pair up differently from the dense tiles: every
