@@ -149,6 +149,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def workload_config(w, world):
+    """The `config` object of the JSON line (the same keys in both arms)."""
+    qkv_gb = 3 * w.B * w.H * w.N * 128 * 2 / 1e9
+    return {"workload": "%s: B=%d H=%d N=%d D=128, k-means k=%d x%d iters, 64-token blocks%s"
+                        % (w.name, w.B, w.H, w.N, w.k, w.iters, ", block-sparse" if w.sparse else ""),
+            "B": w.B, "H": w.H, "N": w.N, "D": 128, "k": w.k, "iters": w.iters,
+            "step": "vcattn_group + vcattn_prep + vcattn_attn",
+            "l2": "inputs (%.2f GB bf16 Q/K/V) exceed the 129 MB L2" % qkv_gb,
+            "parallelism": "heads split over %d rank(s), no collective in the path" % world}
+
+
 # --------------------------------------------------------------------- ours
 def run_ours(args):
     world, rank, local = dist_env()
@@ -247,7 +258,10 @@ def run_ours(args):
     flops_attn_local = 4.0 * N * N * 128 * Hl * B * kept_frac
     attn_tflops = flops_attn_local / (t_attn * 1e-3) / 1e12
     pk = peaks()
-    fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
+    # The attention launch (about 16 ms) runs at the full SM clock inside a
+    # sub-second timed region, so its denominator is the burst bf16 rate (the
+    # sustained rate was measured power-capped at a lower clock).
+    fp8_peak = pk["bf16"] * FP8_OVER_BF16
     Np = vcattn.npad(N)
     prep_bytes = B * Hl * (3 * N * 128 * 2 + 3 * Np * 128 + N * 4 * 2 + (Np // 64) * 128 * 4 +
                            (Np // 128) * 4096)
@@ -271,12 +285,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "e4m3",
         "data": "synthetic (seeded generator standing in for captured video-DiT Q/K/V)",
-        "config": {"workload": "%s: B=%d H=%d N=%d D=128, k-means k=%d x%d iters, 64-token blocks%s"
-                   % (w.name, B, w.H, N, w.k, w.iters, ", block-sparse" if w.sparse else ""),
-                   "B": B, "H": w.H, "N": N, "D": 128, "k": w.k, "iters": w.iters,
-                   "step": "vcattn_group + vcattn_prep + vcattn_attn",
-                   "l2": "inputs (%.2f GB bf16 Q/K/V) exceed the 129 MB L2" % (3 * Q.numel() * 2 / 1e9),
-                   "parallelism": "heads split over %d rank(s), no collective in the path" % world},
+        "config": workload_config(w, world),
         "breakdown_ms": {"group": round(t_group, 4), "prep": round(t_prep, 4), "attn": round(t_attn, 4)},
         "attn_tflops": round(attn_tflops, 2),
         "prep_gbs": round(prep_gbs, 1),
@@ -286,7 +295,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "kernel": "attn_fwd", "achieved": round(attn_tflops, 2),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(attn_tflops / fp8_peak, 4),
-                     "peak_source": "%s bf16 sustained x %.0f (nominal FP8/bf16 ratio)" % (pk["src"], FP8_OVER_BF16),
+                     "peak_source": "%s bf16 burst x %.0f (nominal FP8/bf16 ratio)" % (pk["src"], FP8_OVER_BF16),
                      "traffic": attn_traffic() if (args.workload == "live" and world == 1) else None,
                      "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "gpu_launches": launches_per_step * args.steps,
@@ -374,6 +383,13 @@ def cpu_baseline(w, budget_s=30.0):
 
 
 def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step is the bounded
+    sample `cpu_baseline` also times (as many heads as cores, grouped and
+    prepped in full, emulated attention of 64 evenly spaced queries per head).
+    `ms_per_step` is the measured time of that sample; `value` is the
+    oracle's attention throughput on the full workload, with the attention
+    time extrapolated from the sampled queries to all of them (the
+    extrapolated full-step time is reported beside it)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
@@ -381,26 +397,31 @@ def run_reference(args):
     oracle.build.build()
     w = W.WORKLOADS[args.workload]
     cores = oracle.threads()
-    heads = 1
-    nq = 16
+    heads = max(1, min(cores, w.H))
+    nq = 64
     for i in range(args.warmup):
         cpu_sample(w, heads, nq, seed_offset=i)
-    times, tg, ta = [], 0.0, 0.0
+    full, measured, tg, ta = [], [], 0.0, 0.0
     for i in range(args.steps):
         t_full, flops, g, a = cpu_sample(w, heads, nq, seed_offset=100 + i)
-        times.append(t_full)
+        full.append(t_full)
+        measured.append(g + a)
         tg += g
         ta += a
-    t = sum(times) / len(times)
-    value = 4.0 * w.N * w.N * 128 * heads / t / 1e12
-    sample = ("per step: 1 of %d heads, full k-means + sort + prep, emulated attention of %d evenly "
-              "spaced queries extrapolated to all %d queries" % (w.H, nq, w.N))
+    t_full = sum(full) / len(full)
+    t_meas = sum(measured) / len(measured)
+    value = 4.0 * w.N * w.N * 128 * heads / t_full / 1e12
+    sample = ("per step: %d of %d heads, full k-means + sort + prep (%.2f s), emulated attention of %d "
+              "evenly spaced queries per head (%.2f s); attention time extrapolated to all %d queries"
+              % (heads, w.H, tg / args.steps, nq, ta / args.steps, w.N))
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(t * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+           "ms_per_step": round(t_meas * 1e3, 2), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "e4m3 (emulated in software)", "data": "synthetic",
-           "config": {"workload": "%s: B=1 H=%d N=%d D=128, k-means k=%d x%d iters" %
-                      (w.name, w.H, w.N, w.k, w.iters)},
+           "config": workload_config(w, world),
+           "extrapolated": {"full_step_ms_for_sampled_heads": round(t_full * 1e3, 2),
+                            "heads": heads, "queries_run_per_head": nq,
+                            "note": "value = 4*N^2*D*heads / this extrapolated time"},
            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,

@@ -223,6 +223,28 @@ __device__ __forceinline__ uint32_t expcast4(float x0, float x1, float x2, float
               prmt(__float_as_uint(f23.x), __float_as_uint(f23.y), 0x0040u), 0x5410u);
 }
 
+// Test hook for the byte-level check of ExpCast: the bytes the attention
+// kernel writes for scores x with ExpCast coefficients A (per tile half) and
+// B = C - m (per tile), through the same expcast4 and the same treatment of
+// a key the kernel excludes (score -inf: cast as 0, byte cleared).  Thread g
+// casts the four scores x[4g..4g+3], which share A[g] and B[g].
+__global__ void expcast_probe(const float4* __restrict__ x, const float* __restrict__ A,
+                              const float* __restrict__ B, uint32_t* __restrict__ out, int64_t ngroups) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= ngroups) return;
+  const float4 v = x[g];
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float e[4] = {v.x, v.y, v.z, v.w};
+  float f[4];
+  uint32_t keep = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[i] = e[i] == NEG_INF ? 0.0f : e[i];
+    if (e[i] != NEG_INF) keep |= 0xFFu << (8 * i);
+  }
+  out[g] = expcast4(f[0], f[1], f[2], f[3], A[g] * 0.00390625f, B[g] * 0.00390625f) & keep;
+}
+
 // kMasked: the block-sparse instantiation (a tile mask is given: the union
 // bitmask, the block-pair walk, 64-key boxes); the dense one compiles
 // without them.
@@ -384,11 +406,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, h3, qb);
       }
       load_k(sb + SM_K + sbase * TILE_BYTES, pr, qb);
+      // Test hook: with debug_flags >> 8 = n > 0 the producer stops after n
+      // steps, as if its loads had stalled mid-stream.
+      const int stop_after = p.debug_flags >> 8;
+      // the last step that armed each of this producer's stages (-1: none)
+      int armed[SN];
+#pragma unroll
+      for (int u = 0; u < SN; ++u) armed[u] = -1;
       // Step j brings V(j) and its mean tile into stage sbase + j % SN and
       // K(j+1) into K stage sbase + (j+1) % SN, all on one barrier.  A K
       // stage is free again once the QKs that read it were done, a V stage
       // once the mean terms of its tile were issued (dense: both slots').
-      for (int j = 0; pr.x >= 0 && !*abort; ++j) {
+      for (int j = 0; pr.x >= 0 && !*abort && !(stop_after > 0 && j >= stop_after); ++j) {
         const int st = sbase + j % SN, stk = sbase + (j + 1) % SN;
         const int2 pn = next_pair(ps, pr);
         if (j >= SN && !mbar_wait(bar(B_VEMPTY + st), ((j / SN) - 1) & 1, abort, WAIT_NS)) {
@@ -403,8 +432,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive_expect_tx(bar(B_FULL + st), TILE_BYTES + MU_BYTES + (pn.x >= 0 ? TILE_BYTES : 0));
         load_v(st, pr, bar(B_FULL + st));
         if (pn.x >= 0) load_k(sb + SM_K + stk * TILE_BYTES, pn, bar(B_FULL + st));
+        armed[j % SN] = j;
         pr = pn;
       }
+      // Drain: every copy this producer issued has landed before the CTA can
+      // exit, also when a consumer gave up and never waited for it.  A stage
+      // is re-armed only after its previous fill was consumed, so waiting
+      // for the parity of its last fill is enough (time-bounded, ignoring
+      // the abort flag).
+      bool drained = mbar_wait_time(qb, 0, WAIT_NS);
+#pragma unroll
+      for (int u = 0; u < SN; ++u)
+        if (armed[u] >= 0)
+          drained &= mbar_wait_time(bar(B_FULL + sbase + u), (armed[u] / SN) & 1, WAIT_NS);
+      if (!drained) record_timeout(p, abort);
     }
   } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
     // ----------------------------------------------------------- MMA issue
@@ -490,9 +531,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_commit(bar(B_MDONE + s));
       }
       if (!ok) record_timeout(p, abort);
-      // Drain: every MMA of this lane has completed before TMEM is released.
+      // Drain: every MMA of this lane has completed before TMEM is released,
+      // also after an abort (the wait ignores the abort flag).
       mma_commit(bar(B_FIN + s));
-      if (!mbar_wait(bar(B_FIN + s), 0, abort, WAIT_NS) && !*abort) record_timeout(p, abort);
+      if (!mbar_wait_time(bar(B_FIN + s), 0, WAIT_NS)) record_timeout(p, abort);
     }
   } else if (warp >= WARP_SOFTMAX) {
     // ------------------------------------------------------ softmax warps
@@ -766,16 +808,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == WARP_MMA) tmem_dealloc(tmem, 512);
 }
 
+// The driver's tensor-map encoder (looked up once; a function-local static is
+// initialised thread-safely).
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     cudaDriverEntryPointQueryResult q;
     void* f = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -795,6 +839,15 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 }
 
 }  // namespace
+
+cudaError_t launch_expcast_probe(const float* x, const float* A, const float* B, uint8_t* codes, int64_t n,
+                                 cudaStream_t s) {
+  const int64_t ng = n / 4;
+  if (ng == 0) return cudaSuccess;
+  expcast_probe<<<static_cast<unsigned>((ng + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(x), A, B, reinterpret_cast<uint32_t*>(codes), ng);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   const int64_t Np = npad(a.N);
@@ -829,16 +882,15 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   p.err = a.err;
   p.debug_flags = a.debug_flags;
   // the shared-memory limit is a per-device attribute of each kernel
-  static bool attr_set[MAX_DEVICES] = {};
+  static PerDevice attr;
   int dev = 0;
-  if (!current_device(&dev)) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
+  const cudaError_t ea = per_device_setup(attr, &dev, [](int, int*) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_MASKED);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_MASKED);
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   const dim3 grid(static_cast<unsigned>(ceil_div(Np, CTA_ROWS)), static_cast<unsigned>(a.BH));
   if (p.mask)
     attn_fwd<true><<<grid, NTHREADS, SMEM_BYTES_MASKED, s>>>(mq, mk, mv, p);

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace vc {
 
@@ -16,6 +17,7 @@ constexpr float AMAX_FLOOR = 7.888609052210118e-31f;  // 2^-100
 // Device error word codes (bit flags, OR-ed by kernels).
 constexpr uint32_t ERR_TIMEOUT = 1u;
 constexpr uint32_t ERR_BAD_LABEL = 2u;
+constexpr uint32_t ERR_BAD_PERM = 4u;   // a permutation entry outside [0, N)
 
 __host__ __device__ inline int64_t npad(int64_t n) { return ((n + TILE - 1) / TILE) * TILE; }
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -40,6 +42,25 @@ inline RowLayout contiguous_rows(int64_t H, int64_t N) { return RowLayout{H * N 
 constexpr int MAX_DEVICES = 64;
 inline bool current_device(int* dev) {
   return cudaGetDevice(dev) == cudaSuccess && *dev >= 0 && *dev < MAX_DEVICES;
+}
+
+// Per-device host state (kernel attributes, SM counts) set up by the first
+// call on each device.  `setup(dev)` returns a cudaError_t; it runs under a
+// lock, so first calls from several host threads at once do not race, and a
+// failure is returned and retried by the next call.
+struct PerDevice {
+  std::mutex mu;
+  bool done[MAX_DEVICES] = {};
+  int value[MAX_DEVICES] = {};
+};
+template <class F>
+cudaError_t per_device_setup(PerDevice& pd, int* dev, F&& setup) {
+  if (!current_device(dev)) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(pd.mu);
+  if (pd.done[*dev]) return cudaSuccess;
+  const cudaError_t e = setup(*dev, &pd.value[*dev]);
+  if (e == cudaSuccess) pd.done[*dev] = true;
+  return e;
 }
 
 // ---- grouping (group.cu) ----
@@ -81,9 +102,10 @@ struct PrepWs {
   uint32_t* vamax;  // [BH, D] V residual amax (float bits)
 };
 size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws);
+// A perm entry outside [0, N) gathers a zero row and sets ERR_BAD_PERM in *err.
 cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* K, const RowLayout& lk,
                         const uint16_t* V, const RowLayout& lv, const int32_t* perm, int64_t BH, int64_t N,
-                        const PrepOut& out, const PrepWs& ws, cudaStream_t s);
+                        const PrepOut& out, const PrepWs& ws, uint32_t* err, cudaStream_t s);
 
 // ---- attention (attn.cu) ----
 struct AttnArgs {
@@ -99,8 +121,13 @@ struct AttnArgs {
   int off;
   float tau8;
   uint32_t* err;
-  int debug_flags;  // test hook: bit 0 = the TMA producer issues nothing
+  int debug_flags;  // test hook: bit 0 = the TMA producer issues nothing;
+                    // bits 8.. = n > 0: it stops after n steps
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+// Test hook: the attention kernel's ExpCast bytes for given scores (n a
+// multiple of 4; four consecutive scores share A[i/4] and B[i/4]).
+cudaError_t launch_expcast_probe(const float* x, const float* A, const float* B, uint8_t* codes, int64_t n,
+                                 cudaStream_t s);
 
 }  // namespace vc

@@ -416,16 +416,18 @@ __global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, 
   }
 }
 
+// The driver's tensor-map encoder (looked up once; a function-local static is
+// initialised thread-safely).
 PFN_cuTensorMapEncodeTiled_v12000 km_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     cudaDriverEntryPointQueryResult q;
     void* f = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -451,25 +453,21 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t 
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  // per device: the kernel's shared-memory limit and the SM count
-  static bool attr_set[MAX_DEVICES] = {};
-  static int slots_of[MAX_DEVICES] = {};
+  // per device: the kernel's shared-memory limit and the SM count (two CTA
+  // slots per SM)
+  static PerDevice setup;
   int dev = 0;
-  if (!current_device(&dev)) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(km_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, KT_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  const cudaError_t est = per_device_setup(setup, &dev, [](int d, int* slots_out) {
+    cudaError_t e = cudaFuncSetAttribute(km_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, KT_SMEM);
+    int sms = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+    if (e == cudaSuccess) *slots_out = 2 * (sms > 0 ? sms : 1);
+    return e;
+  });
+  if (est != cudaSuccess) return est;
   // Tiles per CTA: at most 16 (the per-CTA set-up is amortised over them),
   // chosen so that the CTAs fill whole waves of two CTAs per SM.
-  if (!slots_of[dev]) {
-    int sms = 0;
-    const cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    slots_of[dev] = 2 * (sms > 0 ? sms : 1);
-  }
-  const int slots = slots_of[dev];
+  const int slots = setup.value[dev];
   const int64_t ntile = (N + 127) / 128;
   const int64_t total = ntile * BH;
   const int64_t waves = (total + 16 * slots - 1) / (16 * slots);

@@ -79,12 +79,19 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 struct Src4 {
   int64_t r[4];
 };
-__device__ __forceinline__ Src4 load_src(const int32_t* perm, int64_t r0, int64_t N) {
+// A perm entry outside [0, N) is never dereferenced: its row is staged as
+// zeros and ERR_BAD_PERM is recorded in *err.
+__device__ __forceinline__ Src4 load_src(const int32_t* perm, int64_t r0, int64_t N, uint32_t* err) {
   Src4 s;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int64_t r = r0 + u * 16 + (static_cast<int>(threadIdx.x) >> 4);
-    s.r[u] = r < N ? (perm ? static_cast<int64_t>(perm[r]) : r) : -1;
+    int64_t src = r < N ? (perm ? static_cast<int64_t>(perm[r]) : r) : -1;
+    if (r < N && (src < 0 || src >= N)) {
+      atomicOr(err, ERR_BAD_PERM);
+      src = -1;
+    }
+    s.r[u] = src;
   }
   return s;
 }
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
                                                   const int32_t* __restrict__ perm, int64_t N,
                                                   int nb, int nbp, float* __restrict__ kbs,
                                                   float* __restrict__ v_mean,
-                                                  uint32_t* __restrict__ vamax) {
+                                                  uint32_t* __restrict__ vamax, uint32_t* err) {
   extern __shared__ __align__(128) uint8_t ssm[];
   const Map m = thread_map();
   const int64_t bh = blockIdx.y;
@@ -177,14 +184,14 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
   const uint16_t* Kh = K + lk.head(bh);
   const uint16_t* Vh = V + lv.head(bh);
   // gather indices of the next block to stage (one block ahead)
-  Src4 nk = load_src(nullptr, b0 * BLK, N), nv = load_src(ph, b0 * BLK, N);
+  Src4 nk = load_src(nullptr, b0 * BLK, N, err), nv = load_src(ph, b0 * BLK, N, err);
   auto stage = [&](int64_t b, int buf) {
     stage_rows(ssm + buf * 2 * TILE_SMEM, Kh, lk.sn, nk);
     stage_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, Vh, lv.sn, nv);
     cp_commit();
     if (b + 1 < b1) {
-      nk = load_src(nullptr, (b + 1) * BLK, N);
-      nv = load_src(ph, (b + 1) * BLK, N);
+      nk = load_src(nullptr, (b + 1) * BLK, N, err);
+      nv = load_src(ph, (b + 1) * BLK, N, err);
     }
   };
   stage(b0, 0);
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(256) prep_quant(
     const uint32_t* __restrict__ vamax, const float* __restrict__ k_mean,
     const float* __restrict__ v_scale, float* __restrict__ v_mean, uint8_t* __restrict__ q8,
     uint8_t* __restrict__ k8, uint8_t* __restrict__ r8t, float* __restrict__ q_scale,
-    float* __restrict__ k_scale, float* __restrict__ qmu, float* __restrict__ vmu_op) {
+    float* __restrict__ k_scale, float* __restrict__ qmu, float* __restrict__ vmu_op, uint32_t* err) {
   extern __shared__ __align__(128) uint8_t qsm[];
   uint8_t (*tb)[BLK + 16] = reinterpret_cast<uint8_t (*)[BLK + 16]>(qsm + 6 * TILE_SMEM);
   float* kmu = reinterpret_cast<float*>(qsm + 6 * TILE_SMEM + D * (BLK + 16));
@@ -313,7 +320,7 @@ __global__ void __launch_bounds__(256) prep_quant(
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * QUANT_BPC;
   const int64_t b1 = b0 + QUANT_BPC < nbp ? b0 + QUANT_BPC : nbp;
   const int32_t* ph = perm ? perm + bh * N : nullptr;
-  Src4 nq = load_src(nullptr, b0 * BLK, N), ng = load_src(ph, b0 * BLK, N);
+  Src4 nq = load_src(nullptr, b0 * BLK, N, err), ng = load_src(ph, b0 * BLK, N, err);
   auto stage = [&](int64_t b, int buf) {
     uint8_t* t = qsm + buf * 3 * TILE_SMEM;
     stage_rows(t, Q + lq.head(bh), lq.sn, nq);
@@ -321,8 +328,8 @@ __global__ void __launch_bounds__(256) prep_quant(
     stage_rows(t + 2 * TILE_SMEM, V + lv.head(bh), lv.sn, ng);
     cp_commit();
     if (b + 1 < b1) {
-      nq = load_src(nullptr, (b + 1) * BLK, N);
-      ng = load_src(ph, (b + 1) * BLK, N);
+      nq = load_src(nullptr, (b + 1) * BLK, N, err);
+      ng = load_src(ph, (b + 1) * BLK, N, err);
     }
   };
   stage(b0, 0);
@@ -475,31 +482,30 @@ size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws) {
 
 cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* K, const RowLayout& lk,
                         const uint16_t* V, const RowLayout& lv, const int32_t* perm, int64_t BH, int64_t N,
-                        const PrepOut& o, const PrepWs& ws, cudaStream_t s) {
+                        const PrepOut& o, const PrepWs& ws, uint32_t* err, cudaStream_t s) {
   const int64_t Np = npad(N);
   const int nbp = static_cast<int>(Np / BLK);
   const int nb = static_cast<int>(ceil_div(N, BLK));
   cudaError_t e = cudaMemsetAsync(ws.vamax, 0, static_cast<size_t>(BH) * D * 4, s);
   if (e != cudaSuccess) return e;
   // the shared-memory limit is a per-device attribute of each kernel
-  static bool attr_set[MAX_DEVICES] = {};
+  static PerDevice attr;
   int dev = 0;
-  if (!current_device(&dev)) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(prep_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, STATS_SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep_quant, cudaFuncAttributeMaxDynamicSharedMemorySize, QUANT_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  e = per_device_setup(attr, &dev, [](int, int*) {
+    cudaError_t r = cudaFuncSetAttribute(prep_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, STATS_SMEM);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(prep_quant, cudaFuncAttributeMaxDynamicSharedMemorySize, QUANT_SMEM);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   prep_stats<<<dim3(static_cast<unsigned>(ceil_div(nb, STATS_BPC)), static_cast<unsigned>(BH)), 256,
-               STATS_SMEM, s>>>(K, lk, V, lv, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax);
+               STATS_SMEM, s>>>(K, lk, V, lv, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax, err);
   prep_kmean<<<static_cast<unsigned>(BH), dim3(D, KM_SEG), 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp,
                                                                    o.k_mean, o.v_scale);
   prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH)), 256,
                QUANT_SMEM, s>>>(
       Q, lq, K, lk, V, lv, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
-      o.q_scale, o.k_scale, o.qmu, o.vmu_op);
+      o.q_scale, o.k_scale, o.qmu, o.vmu_op, err);
   return cudaGetLastError();
 }
 

@@ -32,7 +32,8 @@
 #include "internal.h"
 
 namespace vc {
-vcattn_status from_cuda(cudaError_t e);  // records e for vcattn_last_cuda_error
+vcattn_status from_cuda(cudaError_t e);             // records e for vcattn_last_cuda_error
+uint32_t* device_error_word(vcattn_status* st);      // the library's device error word
 }  // namespace vc
 
 namespace {
@@ -91,13 +92,15 @@ extern "C" vcattn_status vcattn_prep_noalloc(const vcattn_shape* s, const void* 
   vcattn_status st = VCATTN_OK;
   void* base = scratch_address(&st);
   if (!base) return st;
+  uint32_t* err = vc::device_error_word(&st);
+  if (!err) return st;
   vc::PrepWs w{};
   vc::prep_ws_layout(BH, s->N, base, &w);
   const vc::PrepOut o{out->q8, out->k8, out->r8t, out->q_scale, out->k_scale, out->v_scale,
                       out->k_mean, out->v_mean, out->qmu, out->vmu_op};
   const vc::RowLayout lc = vc::contiguous_rows(s->H, s->N);
   const cudaError_t e = vc::launch_prep(static_cast<const uint16_t*>(Q), lc, static_cast<const uint16_t*>(K), lc,
-                                        static_cast<const uint16_t*>(V), lc, perm, BH, s->N, o, w,
+                                        static_cast<const uint16_t*>(V), lc, perm, BH, s->N, o, w, err,
                                         static_cast<cudaStream_t>(stream));
   return vc::from_cuda(e);
 }

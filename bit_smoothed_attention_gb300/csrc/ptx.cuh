@@ -57,6 +57,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Waits for phase `parity` of `bar` bounded by wall-clock time only (the
+// abort flag is ignored): for draining work already issued (tcgen05 MMAs, TMA
+// copies) before a CTA releases TMEM or exits, which must happen even after
+// another thread has given up.
+__device__ __forceinline__ bool mbar_wait_time(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
                                             uint32_t bar) {

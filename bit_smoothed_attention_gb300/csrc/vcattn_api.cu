@@ -21,6 +21,16 @@ vcattn_status from_cuda(cudaError_t e) {
 using vc::from_cuda;
 
 namespace {
+uint32_t* err_word(vcattn_status* st);
+}  // namespace
+
+namespace vc {
+// The device error word of the current device (for the other translation
+// units of the library).
+uint32_t* device_error_word(vcattn_status* st) { return err_word(st); }
+}  // namespace vc
+
+namespace {
 
 using vc::D;
 
@@ -211,9 +221,11 @@ vcattn_status prep_impl(const vcattn_shape* s, const void* Q, const vcattn_strid
   const int64_t BH = s->B * s->H;
   vc::PrepWs w{};
   if (ws_bytes < vc::prep_ws_layout(BH, s->N, ws, &w)) return VCATTN_ERR_INVALID_ARG;
+  uint32_t* err = err_word(&st);
+  if (!err) return st;
   return from_cuda(vc::launch_prep(static_cast<const uint16_t*>(Q), lq, static_cast<const uint16_t*>(K), lk,
                                    static_cast<const uint16_t*>(V), lv, perm, BH, s->N,
-                                   to_prep_out(out), w, static_cast<cudaStream_t>(stream)));
+                                   to_prep_out(out), w, err, static_cast<cudaStream_t>(stream)));
 }
 }  // namespace
 
@@ -289,6 +301,22 @@ vcattn_status vcattn_attn_strided(const vcattn_shape* s, const vcattn_prepped* i
 vcattn_status vcattn_test_attn_stalled(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
                                        void* O, float* lse2, void* stream) {
   return attn_impl(s, in, sm_scale, 8, 6.0f, 0, nullptr, O, nullptr, lse2, stream, 1);
+}
+
+vcattn_status vcattn_test_attn_stalled_after(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
+                                             int steps, void* O, float* lse2, void* stream) {
+  if (steps < 1 || steps > (1 << 20)) return VCATTN_ERR_INVALID_ARG;
+  return attn_impl(s, in, sm_scale, 8, 6.0f, 0, nullptr, O, nullptr, lse2, stream, steps << 8);
+}
+
+vcattn_status vcattn_test_expcast(const float* x, const float* A, const float* B, uint8_t* codes, int64_t n,
+                                  void* stream) {
+  if (n < 0 || (n & 3) != 0) return VCATTN_ERR_INVALID_ARG;
+  if (n == 0) return VCATTN_OK;
+  if (!x || !A || !B || !codes || !aligned16(x) || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))
+    return VCATTN_ERR_INVALID_ARG;
+  return from_cuda(vc::launch_expcast_probe(x, A, B, codes, n, static_cast<cudaStream_t>(stream)));
 }
 
 vcattn_status vcattn_attn(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,

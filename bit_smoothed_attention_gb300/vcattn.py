@@ -364,6 +364,37 @@ def test_attn_stalled(pp, sm_scale, stream=None):
     return O, lse2
 
 
+def test_attn_stalled_after(pp, sm_scale, steps, stream=None):
+    """Failure-path test hook: the K/V loader stops after `steps` KV tiles, so
+    the kernel gives up with copies and MMAs already issued and must drain
+    them before it exits; last_device_error() then reports ERR_TIMEOUT."""
+    B, H, N = pp.shape.B, pp.shape.H, pp.shape.N
+    O = torch.empty(B, H, N, 128, dtype=torch.bfloat16, device=pp.buf.device)
+    lse2 = torch.empty(B, H, N, dtype=torch.float32, device=pp.buf.device)
+    f = _lib().vcattn_test_attn_stalled_after
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(PreppedStruct), ctypes.c_float, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    _check(f(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale), int(steps), _ptr(O), _ptr(lse2),
+             _stream(stream)), "vcattn_test_attn_stalled_after")
+    return O, lse2
+
+
+def test_expcast(x, A, B, stream=None):
+    """The attention kernel's ExpCast bytes (test hook): x f32 [n] (n a
+    multiple of 4), A and B f32 [n/4] on the GPU; returns uint8 [n]."""
+    for t, n in ((x, "x"), (A, "A"), (B, "B")):
+        _req(t, torch.float32, n)
+    if x.numel() % 4 or A.numel() != x.numel() // 4 or B.numel() != A.numel():
+        raise ValueError("x needs 4*m scores and A, B m values each")
+    codes = torch.empty(x.numel(), dtype=torch.uint8, device=x.device)
+    f = _lib().vcattn_test_expcast
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64, ctypes.c_void_p]
+    _check(f(_ptr(x), _ptr(A), _ptr(B), _ptr(codes), x.numel(), _stream(stream)), "vcattn_test_expcast")
+    return codes
+
+
 def last_device_error(stream=None):
     """Synchronise and return (and clear) the device error status."""
     return _lib().vcattn_last_device_error(_stream(stream))

@@ -146,7 +146,10 @@ vcattn_status vcattn_group_strided(const vcattn_shape* shape, const void* V, con
  * adjacent-pairing FP32 tree sums divided by the valid count.
  *   Q, K, V  bf16 [B,H,N,D] (device)
  *   perm     i32  [B,H,N] (device), nullable = identity; must be a
- *            permutation of [0, N) per head (not validated on the device)
+ *            permutation of [0, N) per head.  An entry outside [0, N) is
+ *            never dereferenced: its row is read as zeros and the device
+ *            error word reports VCATTN_ERR_DEVICE; a repeated entry is not
+ *            detected.
  *   out      the prepped buffers (device pointers inside a host struct)
  *   ws       device scratch of at least vcattn_prep_workspace_bytes(shape) */
 size_t vcattn_prepped_bytes(const vcattn_shape* shape);
@@ -286,6 +289,27 @@ const char* vcattn_status_string(vcattn_status s);
  * vcattn_attn (dense, no mask). */
 vcattn_status vcattn_test_attn_stalled(const vcattn_shape* shape, const vcattn_prepped* in,
                                        float sm_scale, void* O, float* lse2, void* stream);
+/* Test hook for the failure path while copies are in flight (not part of
+ * the method): as vcattn_test_attn_stalled, but the K/V loader stops after
+ * `steps` (>= 1) KV tiles, so the consumers give up part-way with loads and
+ * MMAs already issued; the kernel drains what it issued before it exits and
+ * records VCATTN_ERR_TIMEOUT. */
+vcattn_status vcattn_test_attn_stalled_after(const vcattn_shape* shape, const vcattn_prepped* in,
+                                             float sm_scale, int steps, void* O, float* lse2, void* stream);
+/* Test hook for the byte-level check of ExpCast-FP8 (VC-Attention, Key
+ * Contribution 2: the probability's E4M3 byte from one FMA and one integer
+ * rounding of the max-subtracted log2 score).  Runs the attention kernel's
+ * own ExpCast code on given scores: codes[i] is the byte the kernel writes
+ * for score x[i] with coefficient A[i/4] and constant B[i/4] = C - m, i.e.
+ * clip(rint(fmaf(x, A, B))) (rint: to nearest, ties to even) with codes
+ * below 8 flushed to 0; a score of -inf marks an excluded key (byte 0).  The
+ * kernel guarantees t = fmaf(x, A, B) <= C + tau8 < 126.5, so the clip at
+ * 126 never binds inside that domain; outside it the bytes are not
+ * specified.  x and codes hold n elements (n a multiple of 4, 16-byte
+ * aligned device pointers); A and B hold n/4 (device).  Enqueued on
+ * `stream`. */
+vcattn_status vcattn_test_expcast(const float* x, const float* A, const float* B, uint8_t* codes, int64_t n,
+                                  void* stream);
 /* Text of the CUDA error behind the calling thread's most recent
  * VCATTN_ERR_CUDA (host side: a failed launch, attribute, tensor-map or
  * copy call); "no error" if there was none.  The string is static. */

@@ -34,6 +34,7 @@ def _L():
         lib.orc_e4m3_is_tie.restype = i32
         lib.orc_expcast_cstar.restype = ctypes.c_double
         lib.orc_expcast_n.argtypes = [P, f32, f32, P, i64]
+        lib.orc_expcast_v.argtypes = [P, P, P, P, i64]
         lib.orc_tree_sum.argtypes = [P, i64]
         lib.orc_tree_sum.restype = f32
         lib.orc_kmeans.argtypes = [P, i64, i64, i32, i32, P, P]
@@ -97,6 +98,16 @@ def expcast(x, A, B):
     x = _c(x, np.float32)
     out = np.empty(x.shape, np.uint8)
     _L().orc_expcast_n(_p(x), float(A), float(B), _p(out), x.size)
+    return out
+
+
+def expcast_v(x, A, B):
+    """ExpCast bytes with a coefficient A[i] and constant B[i] per score."""
+    x, A, B = (_c(t, np.float32) for t in (x, A, B))
+    if not (x.shape == A.shape == B.shape):
+        raise ValueError("x, A and B must have one shape")
+    out = np.empty(x.shape, np.uint8)
+    _L().orc_expcast_v(_p(x), _p(A), _p(B), _p(out), x.size)
     return out
 
 

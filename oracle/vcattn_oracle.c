@@ -138,6 +138,10 @@ uint8_t orc_expcast_byte(float x, float A, float B) {
 void orc_expcast_n(const float* x, float A, float B, uint8_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_expcast_byte(x[i], A, B);
 }
+/* The same with a coefficient and a constant per element. */
+void orc_expcast_v(const float* x, const float* A, const float* B, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_expcast_byte(x[i], A[i], B[i]);
+}
 
 /* ------------------------------------------------------------------ */
 /* Pairwise tree sum (R6): adjacent pairing,                             */

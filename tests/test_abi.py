@@ -177,3 +177,23 @@ def test_strided_validation_without_gpu(lib):
                                    ctypes.byref(good), None, ctypes.byref(pp), fake, 1 << 30, None) == 1
     assert lib.vcattn_attn_strided(ctypes.byref(s), ctypes.byref(pp), ctypes.c_float(0.1), 8,
                                    ctypes.c_float(6.0), 0, None, fake, None, None, None) == 1
+
+
+def test_test_hooks_validation_without_gpu(lib):
+    """The test hooks reject bad sizes and pointers before any CUDA call."""
+    P = ctypes.c_void_p
+    f = lib.vcattn_test_expcast
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, ctypes.c_int64, P]
+    fake = P(1 << 20)
+    assert f(fake, fake, fake, fake, 6, None) == 1           # not a multiple of 4
+    assert f(fake, fake, fake, fake, -4, None) == 1
+    assert f(fake, fake, fake, fake, 0, None) == 0           # nothing to do
+    assert f(None, fake, fake, fake, 8, None) == 1
+    assert f(P((1 << 20) + 4), fake, fake, fake, 8, None) == 1
+    g = lib.vcattn_test_attn_stalled_after
+    g.restype = ctypes.c_int
+    from bit_smoothed_attention_gb300.vcattn import PreppedStruct
+    pp = PreppedStruct()
+    s = _shape()
+    assert g(ctypes.byref(s), ctypes.byref(pp), ctypes.c_float(0.1), 0, fake, None, None) == 1
