@@ -40,8 +40,7 @@
 
 #define ORC_D 128
 #define ORC_BLK 64        /* quantisation / mean block (tokens)            */
-#define ORC_TILE 128      /* KV tile of the online-softmax recurrence      */
-#define ORC_GROUP 128     /* query rows that share one sequence of KV tiles */
+#define ORC_TILE 128      /* KV step of the online-softmax recurrence       */
 #define ORC_UPD_CHUNK 512 /* token chunk of the centroid-sum order (R4)    */
 
 /* ------------------------------------------------------------------ */
@@ -442,12 +441,12 @@ int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int3
 /* selections, log2-LSE)]                                                */
 /* ------------------------------------------------------------------ */
 /* Per head, for each requested query i (original order), a sequence of KV
- * tiles of two permuted 64-key blocks (b_0, b_1) (R9): the query rows go in
- * groups of 128 (two 64-row tiles); a group's blocks are, in ascending
- * order, those that either of its two tiles keeps (all blocks when dense),
- * taken two per tile, and an odd last tile has no second block.  Dense, tile
- * t is (2t, 2t+1).  Per tile, with the keys of the blocks the row's own tile
- * keeps:
+ * steps of two permuted 64-key blocks (b_0, b_1) (R9): the blocks that the
+ * row's own query 64-tile keeps under the 64x64 tile mask [P2 Changes: the
+ * sparse forward visits the kept KV tiles of each query tile], in ascending
+ * order, two per step; an odd last step has no second block.  Without a mask
+ * every block is kept, so step t is (2t, 2t+1), and a mask that keeps
+ * everything is no mask.  Per step, with the keys of its blocks:
  *   x_ij  = sum_d dec(q8_id) dec(k8_jd), exact then rounded to FP32;
  *   a_i   = fl(c0 * q_scale[i/64]),  c0 = fl(8 log2(e) sm_scale);
  *   A_h   = fl(a_i * k_scale[b_h]),  h = half of the tile;
@@ -490,22 +489,16 @@ int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
     double l = 0.0;
     float m_run = -INFINITY;
     const float a_i = c0 * q_scale[i / ORC_BLK];
-    /* the blocks of the row's group, in ascending order */
-    int64_t* grp = (int64_t*)malloc((size_t)(nbp > 0 ? nbp : 1) * sizeof(int64_t));
-    int64_t ng = 0;
-    const int64_t qt0 = (i / ORC_GROUP) * (ORC_GROUP / ORC_BLK);
-    for (int64_t b = 0; b < nbp; ++b) {
-      int in = mask == NULL;
-      for (int64_t qt = qt0; qt < qt0 + ORC_GROUP / ORC_BLK && qt < nq64 && !in; ++qt)
-        in = mask[qt * nbp + b] != 0;
-      if (in) grp[ng++] = b;
-    }
-    for (int64_t t = 0; 2 * t < ng; ++t) {
-      const int64_t blk[2] = {grp[2 * t], 2 * t + 1 < ng ? grp[2 * t + 1] : -1};
+    /* the blocks the row's own query tile keeps, in ascending order */
+    int64_t* own = (int64_t*)malloc((size_t)(nbp > 0 ? nbp : 1) * sizeof(int64_t));
+    int64_t no = 0;
+    const int64_t qt = i / ORC_BLK;
+    for (int64_t b = 0; b < nbp; ++b)
+      if (mask == NULL || (qt < nq64 && mask[qt * nbp + b] != 0)) own[no++] = b;
+    for (int64_t t = 0; 2 * t < no; ++t) {
+      const int64_t blk[2] = {own[2 * t], 2 * t + 1 < no ? own[2 * t + 1] : -1};
       int kept[2];
-      for (int h = 0; h < 2; ++h)
-        kept[h] = blk[h] >= 0 && (mask ? mask[(i / ORC_BLK) * nbp + blk[h]] != 0 : 1);
-      if (!kept[0] && !kept[1]) continue;
+      for (int h = 0; h < 2; ++h) kept[h] = blk[h] >= 0;
       float A[2] = {0.0f, 0.0f}, mx[2] = {-INFINITY, -INFINITY};
       for (int h = 0; h < 2; ++h)
         if (kept[h]) A[h] = a_i * k_scale[blk[h]];
@@ -562,7 +555,7 @@ int orc_attn_emul(const uint8_t* q8, const uint8_t* k8, const uint8_t* r8t,
         }
       l += lh[0] + lh[1];
     }
-    free(grp);
+    free(own);
     if (l > 0.0) {
       for (int d = 0; d < ORC_D; ++d) O[qi * ORC_D + d] = acc[d] / l;
       lse2[qi] = (double)m_run / 8.0 - off + log2(l) + (double)qmu[i] * (double)sm_scale * 1.4426950408889634;

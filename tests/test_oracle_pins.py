@@ -474,60 +474,84 @@ def test_emul_mask_and_empty_rows(orc):
     assert np.allclose(lq[fin], lse2[fin], atol=1e-9)
 
 
+def _cut_down(pp, qt, steps, N):
+    """The prepped tensors of one head cut down to query tile qt and the KV
+    blocks of `steps`, laid out two per 128-key tile in step order (a step of
+    one block takes the first half of the last tile).  Only the last block of
+    the sequence may be partial, and only as the last block of the cut."""
+    blocks = [b for st in steps for b in st]
+    nkeys = [min(64, N - 64 * b) for b in blocks]
+    assert all(n == 64 for n in nkeys[:-1])
+    Nc = 64 * (len(blocks) - 1) + nkeys[-1]
+    Npc = ((Nc + 127) // 128) * 128
+    nbc = Npc // 64
+    rows = np.arange(64 * qt, min(64 * qt + 64, N))
+    cut = {"q8": np.zeros((1, Npc, 128), np.uint8), "k8": np.zeros((1, Npc, 128), np.uint8),
+           "r8t": np.zeros((1, 128, Npc), np.uint8), "q_scale": np.ones((1, nbc), np.float32),
+           "k_scale": np.ones((1, nbc), np.float32), "v_scale": pp["v_scale"].copy(),
+           "k_mean": pp["k_mean"].copy(), "v_mean": np.zeros((1, nbc, 128), np.float32),
+           "qmu": np.zeros((1, max(Nc, 64)), np.float32)}
+    cut["q8"][0, :rows.size] = pp["q8"][0, rows]
+    cut["q_scale"][0, 0] = pp["q_scale"][0, qt]
+    cut["qmu"][0, :rows.size] = pp["qmu"][0, rows]
+    for c, b in enumerate(blocks):
+        n = nkeys[c]
+        cut["k8"][0, 64 * c:64 * c + n] = pp["k8"][0, 64 * b:64 * b + n]
+        cut["r8t"][0, :, 64 * c:64 * c + n] = pp["r8t"][0, :, 64 * b:64 * b + n]
+        cut["k_scale"][0, c] = pp["k_scale"][0, b]
+        cut["v_mean"][0, c] = pp["v_mean"][0, b]
+    return cut, Nc, rows
+
+
 @pytest.mark.parametrize("tau8", [0.0, 6.0])
-def test_emul_mask_schedule_pairs_group_blocks(orc, tau8):
-    """With a mask, the rows of a 128-row group (two query tiles) visit the
-    blocks that either of the group's tiles keeps, two per KV tile in
-    ascending order.  When four tiles keep the same four blocks, their rows
-    equal the unmasked emulation of a 256-token problem cut down to those
-    blocks (whose tiles are then (S0, S1), (S2, S3)); the masks of other
-    groups do not matter, and a mask that keeps everything is no mask."""
-    N = 1024
+def test_emul_mask_steps_are_the_query_tiles_own_blocks(orc, tau8):
+    """With a 64x64 tile mask, a row's KV steps are the blocks its own query
+    tile keeps, in ascending order, two per step; only the last step of an
+    odd count has one block ("[perf] Add opt-in SM120 sparse attention
+    forward kernel for MiniMax-H3", Changes: the kept KV tiles of each query
+    tile are visited).  The expected steps of each case are written out
+    below, and the masked rows must equal the unmasked emulation of a
+    problem cut down to those steps' blocks, two per 128-key step.  A
+    different pairing of the same blocks gives different bytes, so the
+    comparison decides the steps; the masks of other query tiles do not
+    matter; a mask that keeps everything is no mask."""
+    N = 1000                                      # 16 blocks, the last has 40 keys
     Q, K, V = _small_inputs(N=N, H=1, seed=60)
     labels, _ = orc.kmeans(V, 4, 2)
     perm = orc.stable_sort(labels, 4)
     pp = orc.prep(Q, K, V, perm)
-    nq = nbp = N // 64
+    nq, nbp = (N + 63) // 64, orc.npad(N) // 64
     rng = np.random.default_rng(61)
     mask = (rng.random((nq, nbp)) < 0.3).astype(np.uint8)
-    S, g = [1, 4, 5, 9], 2
-    qt = np.arange(4 * g, 4 * g + 4)
-    mask[qt, :] = 0
-    mask[np.ix_(qt, S)] = 1
+    # query tile: (blocks it keeps, its KV steps written out by hand)
+    cases = {
+        3: ([1, 3, 4], [(1, 3), (4,)]),
+        4: ([0, 1, 2, 3], [(0, 1), (2, 3)]),
+        8: ([9], [(9,)]),
+        10: ([2, 7, 11, 15], [(2, 7), (11, 15)]),
+        11: ([2, 3, 7, 8, 15], [(2, 3), (7, 8), (15,)]),
+        15: ([0, 5, 6, 12, 13, 14], [(0, 5), (6, 12), (13, 14)]),
+    }
+    for qt, (blocks, _) in cases.items():
+        mask[qt, :] = 0
+        mask[qt, blocks] = 1
     O, L = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=mask)
-    rows = np.arange(256 * g, 256 * g + 256)
-    keys = np.concatenate([np.arange(64 * b, 64 * b + 64) for b in S])
-    sub = {"q8": pp["q8"][:, rows], "k8": pp["k8"][:, keys], "r8t": pp["r8t"][:, :, keys],
-           "q_scale": pp["q_scale"][:, qt], "k_scale": pp["k_scale"][:, S],
-           "v_scale": pp["v_scale"], "k_mean": pp["k_mean"], "v_mean": pp["v_mean"][:, S],
-           "qmu": pp["qmu"][:, rows]}
-    O2, L2 = orc.attn_emul(sub, 0, 256, SM, tau8=tau8)
-    assert np.array_equal(O[rows], O2) and np.array_equal(L[rows], L2)
-    # the tiles (2t, 2t+1) of the unmasked layout give a different answer
-    # here, so the comparison above decides the schedule
-    sub_cons = dict(sub, k8=pp["k8"][:, :256], r8t=pp["r8t"][:, :, :256])
-    assert not np.array_equal(O2, orc.attn_emul(sub_cons, 0, 256, SM, tau8=tau8)[0])
-    m3 = mask.copy()
-    m3[: 4 * g] = 1 - m3[: 4 * g]
-    O3, L3 = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=m3)
-    assert np.array_equal(O3[rows], O[rows]) and np.array_equal(L3[rows], L[rows])
-    # The grouping is by the group's union, not by each row's own blocks:
-    # tile 12 keeps {1, 4}; with tile 13 keeping {2, 7} the group's tiles are
-    # (1, 2), (4, 7), without it (1, 4), and tile 12's rows see the difference.
-    # Tile 14 is in the next 128-row group: what it keeps does not matter.
-    ma = mask.copy()
-    ma[12:16, :] = 0
-    ma[12, [1, 4]] = 1
-    mb = ma.copy()
-    mb[13, [2, 7]] = 1
-    mc = ma.copy()
-    mc[14, [2, 7]] = 1
-    ra = np.arange(12 * 64, 13 * 64)
-    Oa = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=ma, qidx=ra)[0]
-    Ob = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=mb, qidx=ra)[0]
-    Oc = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=mc, qidx=ra)[0]
-    assert not np.array_equal(Oa, Ob)
-    assert np.array_equal(Oa, Oc)
+    for qt, (blocks, steps) in cases.items():
+        assert [b for st in steps for b in st] == blocks
+        cut, Nc, rows = _cut_down(pp, qt, steps, N)
+        Oc, Lc = orc.attn_emul(cut, 0, Nc, SM, tau8=tau8, qidx=np.arange(rows.size))
+        assert np.array_equal(O[rows], Oc) and np.array_equal(L[rows], Lc), qt
+    # another pairing of the same blocks changes the output of tile 10
+    cut, Nc, rows = _cut_down(pp, 10, [(2, 11), (7, 15)], N)
+    assert not np.array_equal(O[rows], orc.attn_emul(cut, 0, Nc, SM, tau8=tau8, qidx=np.arange(rows.size))[0])
+    # what the other query tiles keep does not matter
+    m2 = 1 - mask
+    for qt, (blocks, _) in cases.items():
+        m2[qt] = mask[qt]
+    O2, L2 = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=m2)
+    for qt in cases:
+        r = np.arange(64 * qt, min(64 * qt + 64, N))
+        assert np.array_equal(O2[r], O[r]) and np.array_equal(L2[r], L[r])
     Of, Lf = orc.attn_emul(pp, 0, N, SM, tau8=tau8, mask=np.ones((nq, nbp), np.uint8))
     Od, Ld = orc.attn_emul(pp, 0, N, SM, tau8=tau8)
     assert np.array_equal(Of, Od) and np.array_equal(Lf, Ld)
