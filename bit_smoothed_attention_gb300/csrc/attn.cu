@@ -52,13 +52,16 @@
 //
 // A KV tile is two 64-key blocks, one per 64-column half of S and P.  Dense,
 // tile t holds blocks 2t and 2t+1 (one 128-row TMA box of K and of V) for
-// both slots, through one ring of NS stages.  With a tile mask, each slot
-// streams only the blocks that either of its two query 64-tiles keeps, in
-// ascending order, two per tile, through two stages of its own: K arrives as
-// two 64-row boxes, V as two 64-key boxes in the 64B-swizzled layout (each
-// half of the PV B operand has its own indicator row), and the mean tile as
-// two 2 KiB halves.  The slots then have different tile counts; S is taken
-// in turn while both have tiles, and the slot with more goes on alone.
+// both slots, through one ring of NS stages.  With a tile mask, each query
+// 64-tile has its own KV steps: the blocks it keeps, in ascending order, two
+// per step.  A slot (two query tiles) streams its first tile's step 0, its
+// second tile's step 0, the first tile's step 1, and so on, through two
+// stages of its own; only the rows of the tile whose step it is use it, the
+// other 64 rows treat it as absent (codes 0, no max, no row sum).  K arrives
+// as two 64-row boxes, V as two 64-key boxes in the 64B-swizzled layout
+// (each half of the PV B operand has its own indicator row), and the mean
+// tile as two 2 KiB halves.  The slots then have different tile counts; S is
+// taken in turn while both have tiles, and the slot with more goes on alone.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -112,12 +115,12 @@ constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
 constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
 constexpr uint32_t SM_END = SM_ABORT + 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;  // slack for 1024-byte alignment
-// Masked: per slot, one bit per 64-key block, set when either of the slot's
-// two query tiles keeps it (the first 32 * KEPT_WORDS blocks; later ones are
+// Masked: per query 64-tile of the CTA (four), one bit per 64-key block, set
+// when the tile keeps it (the first 32 * KEPT_WORDS blocks; later ones are
 // looked up in the mask itself).
 constexpr uint32_t SM_KEPT = SM_END;
-constexpr int KEPT_WORDS = 224;  // per slot
-constexpr uint32_t SMEM_BYTES_MASKED = SMEM_BYTES + 2 * 4 * KEPT_WORDS;
+constexpr int KEPT_WORDS = 112;  // per query tile
+constexpr uint32_t SMEM_BYTES_MASKED = SMEM_BYTES + 4 * 4 * KEPT_WORDS;
 static_assert(SMEM_BYTES_MASKED <= 232448, "shared memory per CTA");
 
 constexpr uint32_t IDESC_QK = idesc(FMT_E4M3, FMT_E4M3, 128, 128);
@@ -147,26 +150,31 @@ struct Params {
   int debug_flags;
 };
 
-// Does either of the query 64-tiles qa, qa + 1 keep 64-key block b?
-__device__ __forceinline__ bool block_kept(const Params& p, int64_t bh, int qa, int b) {
-  const uint8_t* mcol = p.mask + (bh * p.nq64) * p.nbp + b;
-  bool kept = false;
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int qt = qa + q;
-    kept |= qt < p.nq64 && mcol[static_cast<int64_t>(qt) * p.nbp] != 0;
-  }
-  return kept;
+// Does query 64-tile qt keep 64-key block b?
+__device__ __forceinline__ bool block_kept(const Params& p, int64_t bh, int qt, int b) {
+  return qt < p.nq64 && p.mask[(bh * p.nq64 + qt) * p.nbp + b] != 0;
 }
 
-// The first block at or after u that the query tiles qa, qa + 1 keep, read
-// from the mask itself (blocks beyond the shared-memory bitmask; out of line,
-// it is never hot), or -1.
-__device__ __noinline__ int next_kept_slow(const Params& p, int64_t bh, int qa, int u) {
+// The first block at or after u that query tile qt keeps, read from the mask
+// itself (blocks beyond the shared-memory bitmask; out of line, it is never
+// hot), or -1.
+__device__ __noinline__ int next_kept_slow(const Params& p, int64_t bh, int qt, int u) {
   for (; u < p.nbp; ++u)
-    if (block_kept(p, bh, qa, u)) return u;
+    if (block_kept(p, bh, qt, u)) return u;
   return -1;
 }
+
+// A slot's walk over its KV tiles.  Dense: tile t = blocks (2t, 2t + 1), for
+// all 128 rows.  Masked: each of the slot's two query tiles (A: rows 0-63, B:
+// rows 64-127) has its own steps, the blocks it keeps taken two by two in
+// ascending order (y = -1 in an odd last step); the slot's tiles are A's
+// step 0, B's step 0, A's step 1, ..., and once one tile has no steps left
+// the other goes on alone.  Only the owner's rows use a tile; the others
+// treat it as absent.  x = -1 past the last tile.
+struct Walk {
+  int2 pa, pb;  // the current steps of A and B (masked; dense: pa only)
+  int onB;      // masked: the current tile is B's step
+};
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort) {
   *abort = 1;
@@ -245,7 +253,7 @@ __global__ void expcast_probe(const float4* __restrict__ x, const float* __restr
   out[g] = expcast4(f[0], f[1], f[2], f[3], A[g] * 0.00390625f, B[g] * 0.00390625f) & keep;
 }
 
-// kMasked: the block-sparse instantiation (a tile mask is given: the union
+// kMasked: the block-sparse instantiation (a tile mask is given: the per-tile
 // bitmask, the block-pair walk, 64-key boxes); the dense one compiles
 // without them.
 template <bool kMasked>
@@ -305,16 +313,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           make_uint4(v, v, v, v);
     }
   }
-  // Masked: per slot, the bitmask of the blocks its two query tiles keep.
+  // Masked: per query tile of the CTA, the bitmask of the blocks it keeps.
   uint32_t* kept_w = reinterpret_cast<uint32_t*>(sm + SM_KEPT);
   const int nkw = (p.nbp + 31) >> 5;
   if (kMasked) {
     for (int w = warp; w < nkw && w < KEPT_WORDS; w += NTHREADS / 32) {
       const int b = 32 * w + lane;
 #pragma unroll
-      for (int sl = 0; sl < 2; ++sl) {
-        const uint32_t m = __ballot_sync(0xffffffffu, b < p.nbp && block_kept(p, bh, qt0 + 2 * sl, b));
-        if (lane == 0) kept_w[sl * KEPT_WORDS + w] = m;
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t m = __ballot_sync(0xffffffffu, b < p.nbp && block_kept(p, bh, qt0 + q, b));
+        if (lane == 0) kept_w[q * KEPT_WORDS + w] = m;
       }
     }
   }
@@ -325,41 +333,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TSLOT);
 
-  // KV tiles as block pairs (x, y): dense, (2t, 2t+1) for both slots;
-  // masked, each slot walks the blocks its query tiles keep, two by two,
-  // y = -1 for the empty second half of an odd last tile; x = -1 past the
-  // last tile.  Every role of a slot walks the same sequence.
+  // Every role of a slot walks the same sequence of tiles (see Walk).
   const int kept_lim = p.nbp < 32 * KEPT_WORDS ? p.nbp : 32 * KEPT_WORDS;
-  auto next_kept = [&](int sl, int b) {
-    const uint32_t* kw = kept_w + sl * KEPT_WORDS;
+  auto next_kept = [&](int q, int b) {  // the next block after b that query tile qt0 + q keeps
+    const uint32_t* kw = kept_w + q * KEPT_WORDS;
     int u = b + 1;
     for (; u < kept_lim; u = (u | 31) + 1) {  // bits past nbp are 0
       const uint32_t m = kw[u >> 5] >> (u & 31);
       if (m) return u + __ffs(static_cast<int>(m)) - 1;
     }
-    return u < p.nbp ? next_kept_slow(p, bh, qt0 + 2 * sl, u) : -1;
+    return u < p.nbp ? next_kept_slow(p, bh, qt0 + q, u) : -1;
   };
-  auto pair_after = [&](int sl, int b) -> int2 {  // the slot's tile that starts after block b
+  auto pair_after = [&](int q, int b) -> int2 {  // the step of query tile q that starts after block b
     if constexpr (kMasked) {
-      const int x = next_kept(sl, b);
-      return make_int2(x, x >= 0 ? next_kept(sl, x) : -1);
+      const int x = next_kept(q, b);
+      return make_int2(x, x >= 0 ? next_kept(q, x) : -1);
     } else {
       return b + 2 < p.nbp ? make_int2(b + 1, b + 2) : make_int2(-1, -1);
     }
   };
-  auto next_pair = [&](int sl, int2 pr) { return pr.y < 0 ? make_int2(-1, -1) : pair_after(sl, pr.y); };
+  auto next_pair = [&](int q, int2 pr) { return pr.y < 0 ? make_int2(-1, -1) : pair_after(q, pr.y); };
+  auto w_start = [&](int sl) -> Walk {
+    if constexpr (kMasked) return Walk{pair_after(2 * sl, -1), pair_after(2 * sl + 1, -1), 0};
+    else return Walk{pair_after(0, -1), make_int2(-1, -1), 0};
+  };
+  auto w_tile = [&](const Walk& w) -> int2 {
+    if constexpr (kMasked) return (w.onB || w.pa.x < 0) ? w.pb : w.pa;
+    else return w.pa;
+  };
+  // the tile's owner: 0 = the slot's first query tile, 1 = its second, 2 = both
+  auto w_owner = [&](const Walk& w) -> int {
+    if constexpr (kMasked) return (w.onB || w.pa.x < 0) ? 1 : 0;
+    else return 2;
+  };
+  auto w_next = [&](int sl, Walk w) -> Walk {
+    if constexpr (kMasked) {
+      if (!w.onB && w.pa.x >= 0) {      // A's step was the tile: B's step of the same index next
+        if (w.pb.x >= 0) w.onB = 1;
+        else w.pa = next_pair(2 * sl, w.pa);
+      } else {                          // B's step was the tile: both move on
+        w.onB = 0;
+        w.pa = next_pair(2 * sl, w.pa);
+        w.pb = next_pair(2 * sl + 1, w.pb);
+      }
+    } else {
+      w.pa = next_pair(0, w.pa);
+    }
+    return w;
+  };
 
   // Number of KV tiles of each slot (the same in every role).
   int nt0 = p.ntile, nt1 = p.ntile;
   if constexpr (kMasked) {
-    auto count = [&](int sl) {
+    auto steps = [&](int q) {
       int nb = 0;
-      for (int w = 0; w < nkw && w < KEPT_WORDS; ++w) nb += __popc(kept_w[sl * KEPT_WORDS + w]);
-      for (int u = 32 * KEPT_WORDS; u >= 0 && (u = next_kept_slow(p, bh, qt0 + 2 * sl, u)) >= 0; ++u) ++nb;
+      for (int w = 0; w < nkw && w < KEPT_WORDS; ++w) nb += __popc(kept_w[q * KEPT_WORDS + w]);
+      for (int u = 32 * KEPT_WORDS; u >= 0 && (u = next_kept_slow(p, bh, qt0 + q, u)) >= 0; ++u) ++nb;
       return (nb + 1) >> 1;
     };
-    nt0 = count(0);
-    nt1 = count(1);
+    nt0 = steps(0) + steps(1);
+    nt1 = steps(2) + steps(3);
   }
   auto nt = [&](int sl) { return sl ? nt1 : nt0; };
   // K/V/mean stages: dense, one ring of NS shared by both slots; masked, two
@@ -395,7 +428,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       };
       // Q and the first K tile
-      int2 pr = pair_after(ps, -1);
+      Walk wk = w_start(ps);
+      int2 pr = w_tile(wk);
       const uint32_t qb = bar(B_QFULL + ps);
       if constexpr (kMasked) {
         mbar_arrive_expect_tx(qb, 2 * TILE_BYTES);
@@ -419,7 +453,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // once the mean terms of its tile were issued (dense: both slots').
       for (int j = 0; pr.x >= 0 && !*abort && !(stop_after > 0 && j >= stop_after); ++j) {
         const int st = sbase + j % SN, stk = sbase + (j + 1) % SN;
-        const int2 pn = next_pair(ps, pr);
+        const Walk wn = w_next(ps, wk);
+        const int2 pn = w_tile(wn);
         if (j >= SN && !mbar_wait(bar(B_VEMPTY + st), ((j / SN) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
@@ -434,6 +469,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (pn.x >= 0) load_k(sb + SM_K + stk * TILE_BYTES, pn, bar(B_FULL + st));
         armed[j % SN] = j;
         pr = pn;
+        wk = wn;
       }
       // Drain: every copy this producer issued has landed before the CTA can
       // exit, also when a consumer gave up and never waited for it.  A stage
@@ -551,7 +587,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tO = tmem + lane_addr + COL_O + 160 * slot;
     const float qsc = p.q_scale[bh * p.nbp + (qt < p.nbp ? qt : p.nbp - 1)];
     const float a_i = p.c0 * qsc;
-    const uint8_t* mrow = (p.mask && qt < p.nq64) ? p.mask + (bh * p.nq64 + qt) * p.nbp : nullptr;
     uint8_t* Lrow = sm + SM_L + slot * MU_BYTES + (r >> 3) * 256 + (r & 7) * 16;
     const float* ksc = p.k_scale + bh * p.nbp;
     const float NEG_INF = -__int_as_float(0x7f800000);
@@ -580,24 +615,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float l = 0.0f;
     bool ok = true;
     int i = 0;
-    // block scales and mask bytes of a tile
+    // block scales of a tile
     auto pair_scales = [&](int2 pr) -> float2 {
       if (pr.x < 0) return make_float2(0.0f, 0.0f);
       if constexpr (kMasked) return make_float2(ksc[pr.x], pr.y >= 0 ? ksc[pr.y] : 0.0f);
       else return *reinterpret_cast<const float2*>(ksc + pr.x);
     };
-    auto mask_byte = [&](int b) -> uint8_t { return (kMasked && mrow && b >= 0) ? mrow[b] : 0; };
     const int ntiles = nt(slot);
-    int2 pr = pair_after(slot, -1);
+    const int my_tile = r >> 6;  // masked: the row's query tile within the slot (0 = A, 1 = B)
+    Walk wk = w_start(slot);
+    int2 pr = w_tile(wk);
+    int owner = w_owner(wk);
     // loaded one tile ahead
     float2 ks = pair_scales(pr);
-    uint8_t mk0 = mask_byte(pr.x), mk1 = mask_byte(pr.y);
     for (; pr.x >= 0; ++i) {
-      const int2 pn = next_pair(slot, pr);
+      const Walk wn = w_next(slot, wk);
+      const int2 pn = w_tile(wn);
+      const int owner_n = w_owner(wn);
       const float2 ks_n = pair_scales(pn);
-      const uint8_t mk0_n = mask_byte(pn.x), mk1_n = mask_byte(pn.y);
-      const bool keep0 = row_ok && (!kMasked || mk0 != 0);
-      const bool keep1 = row_ok && (!kMasked || mk1 != 0);
+      // a tile that another query tile owns is absent for this row
+      const bool mine = !kMasked || owner == my_tile;
+      const bool keep0 = row_ok && mine;
+      const bool keep1 = row_ok && mine && pr.y >= 0;
       // Score column j of the tile is a valid key iff j < lim_lo (first
       // half) or j < lim_hi (second half); dense, both are N - 128 t.
       const int n32 = static_cast<int>(p.N);
@@ -736,9 +775,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
       pr = pn;
+      wk = wn;
+      owner = owner_n;
       ks = ks_n;
-      mk0 = mk0_n;
-      mk1 = mk1_n;
     }
     // the last tile's row sums, then its mean term
     if (ok && ntiles > 0) {
