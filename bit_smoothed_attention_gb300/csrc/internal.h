@@ -103,9 +103,11 @@ struct PrepWs {
 };
 size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws);
 // A perm entry outside [0, N) gathers a zero row and sets ERR_BAD_PERM in *err.
+// flags: PREP_QK_HADAMARD rotates Q and centred K before their quantisers.
+constexpr int PREP_QK_HADAMARD = 1;
 cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* K, const RowLayout& lk,
                         const uint16_t* V, const RowLayout& lv, const int32_t* perm, int64_t BH, int64_t N,
-                        const PrepOut& out, const PrepWs& ws, uint32_t* err, cudaStream_t s);
+                        const PrepOut& out, const PrepWs& ws, uint32_t* err, int flags, cudaStream_t s);
 
 // ---- attention (attn.cu) ----
 struct AttnArgs {

@@ -161,6 +161,32 @@ __device__ __forceinline__ float2 block_max2(float a, float b, float* red) {
   return make_float2(ra, rb);
 }
 
+// The 128-point Hadamard butterfly of one row held by four consecutive lanes,
+// 32 channels each (lane & 3 = qq holds channels 32 qq ..): stages
+// h = 1, 2, ..., 64 in that order, each pair (x[i], x[i + h]) with i & h == 0
+// becoming (x[i] + x[i + h], x[i] - x[i + h]) in FP32.
+__device__ __forceinline__ void hadamard_row32(float (&x)[32], int qq) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((i & h) == 0) {
+        const float a = x[i], c = x[i + h];
+        x[i] = a + c;
+        x[i + h] = a - c;
+      }
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int lm = 1 << s;             // h = 32 (lane ^ 1), then h = 64 (lane ^ 2)
+    const bool hi = (qq & lm) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], lm);
+      x[i] = hi ? o - x[i] : x[i] + o;
+    }
+  }
+}
+
 // Stats: K block sums (original order), mean of each permuted V block, and
 // the per-channel amax of the V residual.  Each CTA handles STATS_BPC
 // consecutive blocks; block b+1 is staged while block b is reduced, and the
@@ -309,7 +335,8 @@ __global__ void __launch_bounds__(256) prep_quant(
     const uint32_t* __restrict__ vamax, const float* __restrict__ k_mean,
     const float* __restrict__ v_scale, float* __restrict__ v_mean, uint8_t* __restrict__ q8,
     uint8_t* __restrict__ k8, uint8_t* __restrict__ r8t, float* __restrict__ q_scale,
-    float* __restrict__ k_scale, float* __restrict__ qmu, float* __restrict__ vmu_op, uint32_t* err) {
+    float* __restrict__ k_scale, float* __restrict__ qmu, float* __restrict__ vmu_op, uint32_t* err,
+    int rot) {
   extern __shared__ __align__(128) uint8_t qsm[];
   uint8_t (*tb)[BLK + 16] = reinterpret_cast<uint8_t (*)[BLK + 16]>(qsm + 6 * TILE_SMEM);
   float* kmu = reinterpret_cast<float*>(qsm + 6 * TILE_SMEM + D * (BLK + 16));
@@ -365,32 +392,92 @@ __global__ void __launch_bounds__(256) prep_quant(
 
     // ---- Q (per 64-query block, original order) and K (gathered, centred,
     // per 64-key block): both block maxima in one reduction ----
-    float x[4][8], xk[4][8];
-    read_rows(tq, m.g, m.cc, x);
-    read_rows(tk, m.g, m.cc, xk);
-    float a = 0.0f, ak = 0.0f;
+    float2 am2;
+    if (!rot) {
+      float x[4][8], xk[4][8];
+      read_rows(tq, m.g, m.cc, x);
+      read_rows(tk, m.g, m.cc, xk);
+      float a = 0.0f, ak = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        a = fmaxf(a, fabsf(x[i][c]));
-        xk[i][c] = (r0 + i < N) ? xk[i][c] - kmu[8 * m.cc + c] : 0.0f;
-        ak = fmaxf(ak, fabsf(xk[i][c]));
+        for (int c = 0; c < 8; ++c) {
+          a = fmaxf(a, fabsf(x[i][c]));
+          xk[i][c] = (r0 + i < N) ? xk[i][c] - kmu[8 * m.cc + c] : 0.0f;
+          ak = fmaxf(ak, fabsf(xk[i][c]));
+        }
+      am2 = block_max2(a, ak, red);
+      const bool lq = am2.x >= AMAX_FLOOR, lk = am2.y >= AMAX_FLOOR;
+      const float iq = lq ? 448.0f / am2.x : 0.0f, ik = lk ? 448.0f / am2.y : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float y[8], z[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          y[c] = (lq && r0 + i < N) ? x[i][c] * iq : 0.0f;
+          z[c] = lk ? xk[i][c] * ik : 0.0f;
+        }
+        *reinterpret_cast<uint2*>(q8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
+        *reinterpret_cast<uint2*>(k8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(z);
       }
-    const float2 am2 = block_max2(a, ak, red);
-    float amax = am2.x;
-    bool live = amax >= AMAX_FLOOR;
-    float inv = live ? 448.0f / amax : 0.0f;
+    } else {
+      // QK Hadamard rotation before the quantisers: thread (row rr, quarter
+      // qq) holds channels 32 qq .. 32 qq + 31 of one row; butterfly stages
+      // h = 1..16 run in registers, h = 32 and 64 across the row's four
+      // lanes (lane ^ 1, lane ^ 2).  Q is scaled by 2^-4 and K by 2^-3
+      // afterwards (exact), so q' . k' = q . (k - mu_K).
+      const int rr = threadIdx.x >> 2, qq = threadIdx.x & 3;
+      const bool valid = b * BLK + rr < N;
+      float hq[32], hk[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float y[8];
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float t[8], u[8];
+        unpack8(*reinterpret_cast<const uint4*>(tq + swz(rr, 4 * qq + c4)), t);
+        unpack8(*reinterpret_cast<const uint4*>(tk + swz(rr, 4 * qq + c4)), u);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) y[c] = (live && r0 + i < N) ? x[i][c] * inv : 0.0f;
-      *reinterpret_cast<uint2*>(q8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
+        for (int e = 0; e < 8; ++e) {
+          hq[8 * c4 + e] = t[e];
+          hk[8 * c4 + e] = valid ? u[e] - kmu[32 * qq + 8 * c4 + e] : 0.0f;
+        }
+      }
+      hadamard_row32(hq, qq);
+      hadamard_row32(hk, qq);
+      float a = 0.0f, ak = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        hq[e] *= 0.0625f;
+        hk[e] *= 0.125f;
+        a = fmaxf(a, fabsf(hq[e]));
+        ak = fmaxf(ak, fabsf(hk[e]));
+      }
+      am2 = block_max2(a, ak, red);
+      const bool lq = am2.x >= AMAX_FLOOR, lk = am2.y >= AMAX_FLOOR;
+      const float iq = lq ? 448.0f / am2.x : 0.0f, ik = lk ? 448.0f / am2.y : 0.0f;
+      uint2 oq[4], ok[4];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float y[8], z[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          y[e] = (lq && valid) ? hq[8 * c4 + e] * iq : 0.0f;
+          z[e] = lk ? hk[8 * c4 + e] * ik : 0.0f;
+        }
+        oq[c4] = e4m3x8(y);
+        ok[c4] = e4m3x8(z);
+      }
+      uint4* dq = reinterpret_cast<uint4*>(q8 + (bh * Npad + b * BLK + rr) * D + 32 * qq);
+      uint4* dk = reinterpret_cast<uint4*>(k8 + (bh * Npad + b * BLK + rr) * D + 32 * qq);
+      dq[0] = make_uint4(oq[0].x, oq[0].y, oq[1].x, oq[1].y);
+      dq[1] = make_uint4(oq[2].x, oq[2].y, oq[3].x, oq[3].y);
+      dk[0] = make_uint4(ok[0].x, ok[0].y, ok[1].x, ok[1].y);
+      dk[1] = make_uint4(ok[2].x, ok[2].y, ok[3].x, ok[3].y);
     }
-    if (threadIdx.x == 0) q_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
+    if (threadIdx.x == 0) {
+      q_scale[bh * nbp + b] = am2.x >= AMAX_FLOOR ? am2.x / 448.0f : 1.0f;
+      k_scale[bh * nbp + b] = am2.y >= AMAX_FLOOR ? am2.y / 448.0f : 1.0f;
+    }
     if (threadIdx.x < BLK) {
-      // qmu = q . mu_K: one fmaf chain over d ascending
+      // qmu = q . mu_K (the unrotated q): one fmaf chain over d ascending
       const int rr = threadIdx.x;
       const int64_t r = b * BLK + rr;
       if (r < N) {
@@ -404,19 +491,9 @@ __global__ void __launch_bounds__(256) prep_quant(
         qmu[bh * N + r] = acc;
       }
     }
-    amax = am2.y;
-    live = amax >= AMAX_FLOOR;
-    inv = live ? 448.0f / amax : 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float y[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) y[c] = live ? xk[i][c] * inv : 0.0f;
-      *reinterpret_cast<uint2*>(k8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
-    }
-    if (threadIdx.x == 0) k_scale[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
 
     // ---- V: gathered, block-demeaned residual, per-channel scale, transposed ----
+    float x[4][8];
     read_rows(tv, m.g, m.cc, x);
     uint2 by[4];
 #pragma unroll
@@ -482,7 +559,7 @@ size_t prep_ws_layout(int64_t BH, int64_t N, void* base, PrepWs* ws) {
 
 cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* K, const RowLayout& lk,
                         const uint16_t* V, const RowLayout& lv, const int32_t* perm, int64_t BH, int64_t N,
-                        const PrepOut& o, const PrepWs& ws, uint32_t* err, cudaStream_t s) {
+                        const PrepOut& o, const PrepWs& ws, uint32_t* err, int flags, cudaStream_t s) {
   const int64_t Np = npad(N);
   const int nbp = static_cast<int>(Np / BLK);
   const int nb = static_cast<int>(ceil_div(N, BLK));
@@ -505,7 +582,7 @@ cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* 
   prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH)), 256,
                QUANT_SMEM, s>>>(
       Q, lq, K, lk, V, lv, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
-      o.q_scale, o.k_scale, o.qmu, o.vmu_op, err);
+      o.q_scale, o.k_scale, o.qmu, o.vmu_op, err, (flags & PREP_QK_HADAMARD) != 0);
   return cudaGetLastError();
 }
 

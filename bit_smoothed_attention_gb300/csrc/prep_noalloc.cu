@@ -100,7 +100,7 @@ extern "C" vcattn_status vcattn_prep_noalloc(const vcattn_shape* s, const void* 
                       out->k_mean, out->v_mean, out->qmu, out->vmu_op};
   const vc::RowLayout lc = vc::contiguous_rows(s->H, s->N);
   const cudaError_t e = vc::launch_prep(static_cast<const uint16_t*>(Q), lc, static_cast<const uint16_t*>(K), lc,
-                                        static_cast<const uint16_t*>(V), lc, perm, BH, s->N, o, w, err,
+                                        static_cast<const uint16_t*>(V), lc, perm, BH, s->N, o, w, err, 0,
                                         static_cast<cudaStream_t>(stream));
   return vc::from_cuda(e);
 }

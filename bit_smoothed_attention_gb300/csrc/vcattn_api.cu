@@ -209,9 +209,10 @@ size_t vcattn_prep_workspace_bytes(const vcattn_shape* s) {
 namespace {
 vcattn_status prep_impl(const vcattn_shape* s, const void* Q, const vcattn_strides* sq, const void* K,
                         const vcattn_strides* sk, const void* V, const vcattn_strides* sv, const int32_t* perm,
-                        const vcattn_prepped* out, void* ws, size_t ws_bytes, void* stream) {
+                        int flags, const vcattn_prepped* out, void* ws, size_t ws_bytes, void* stream) {
   vcattn_status st = check_shape(s);
   if (st != VCATTN_OK) return st;
+  if (flags & ~VCATTN_PREP_QK_HADAMARD) return VCATTN_ERR_INVALID_ARG;
   vc::RowLayout lq{}, lk{}, lv{};
   if (!rows_of(s, sq, &lq) || !rows_of(s, sk, &lk) || !rows_of(s, sv, &lv)) return VCATTN_ERR_INVALID_ARG;
   if (!Q || !K || !V || !out || !ws || !prepped_ok(out)) return VCATTN_ERR_INVALID_ARG;
@@ -225,7 +226,7 @@ vcattn_status prep_impl(const vcattn_shape* s, const void* Q, const vcattn_strid
   if (!err) return st;
   return from_cuda(vc::launch_prep(static_cast<const uint16_t*>(Q), lq, static_cast<const uint16_t*>(K), lk,
                                    static_cast<const uint16_t*>(V), lv, perm, BH, s->N,
-                                   to_prep_out(out), w, err, static_cast<cudaStream_t>(stream)));
+                                   to_prep_out(out), w, err, flags, static_cast<cudaStream_t>(stream)));
 }
 }  // namespace
 
@@ -234,7 +235,7 @@ extern "C" {
 vcattn_status vcattn_prep(const vcattn_shape* s, const void* Q, const void* K, const void* V,
                           const int32_t* perm, const vcattn_prepped* out, void* ws,
                           size_t ws_bytes, void* stream) {
-  return prep_impl(s, Q, nullptr, K, nullptr, V, nullptr, perm, out, ws, ws_bytes, stream);
+  return prep_impl(s, Q, nullptr, K, nullptr, V, nullptr, perm, 0, out, ws, ws_bytes, stream);
 }
 
 vcattn_status vcattn_prep_strided(const vcattn_shape* s, const void* Q, const vcattn_strides* sq,
@@ -242,7 +243,14 @@ vcattn_status vcattn_prep_strided(const vcattn_shape* s, const void* Q, const vc
                                   const vcattn_strides* sv, const int32_t* perm, const vcattn_prepped* out,
                                   void* ws, size_t ws_bytes, void* stream) {
   if (!sq || !sk || !sv) return VCATTN_ERR_INVALID_ARG;
-  return prep_impl(s, Q, sq, K, sk, V, sv, perm, out, ws, ws_bytes, stream);
+  return prep_impl(s, Q, sq, K, sk, V, sv, perm, 0, out, ws, ws_bytes, stream);
+}
+
+vcattn_status vcattn_prep_ex(const vcattn_shape* s, const void* Q, const vcattn_strides* sq, const void* K,
+                             const vcattn_strides* sk, const void* V, const vcattn_strides* sv,
+                             const int32_t* perm, int flags, const vcattn_prepped* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return prep_impl(s, Q, sq, K, sk, V, sv, perm, flags, out, ws, ws_bytes, stream);
 }
 
 namespace {

@@ -73,6 +73,9 @@ def _lib():
         lib.vcattn_attn_strided.restype = st
         lib.vcattn_attn_strided.argtypes = [SP, ctypes.POINTER(PreppedStruct), ctypes.c_float, ctypes.c_int,
                                             ctypes.c_float, ctypes.c_int, P, P, SS, P, P]
+        lib.vcattn_prep_ex.restype = st
+        lib.vcattn_prep_ex.argtypes = [SP, P, SS, P, SS, P, SS, P, ctypes.c_int, ctypes.POINTER(PreppedStruct),
+                                       P, sz, P]
         lib.vcattn_prepped_bytes.restype = sz
         lib.vcattn_prepped_bytes.argtypes = [SP]
         lib.vcattn_prepped_carve.restype = st
@@ -224,9 +227,14 @@ class Prepped:
             vmu_op=v("vmu_op", (B * H, nbp, 128, 4), torch.float32))
 
 
-def prep(Q, K, V, perm=None, out=None, stream=None):
+PREP_QK_HADAMARD = 1
+
+
+def prep(Q, K, V, perm=None, out=None, stream=None, hadamard=False):
     """Fused K mean, gather by perm, V block demean and Q/K/V quantisers.
-    Q, K, V may be strided views (channels contiguous)."""
+    Q, K, V may be strided views (channels contiguous).  hadamard=True
+    rotates Q and centred K by the 128-point Hadamard transform before their
+    quantisers (vcattn_prep_ex with VCATTN_PREP_QK_HADAMARD)."""
     rows = [_rows(t, torch.bfloat16, n) for t, n in ((Q, "Q"), (K, "K"), (V, "V"))]
     if perm is not None:
         _req(perm, torch.int32, "perm")
@@ -234,7 +242,12 @@ def prep(Q, K, V, perm=None, out=None, stream=None):
     s = _shape(Q)
     nbytes = _lib().vcattn_prep_workspace_bytes(ctypes.byref(s))
     ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
-    if all(r is None for r in rows):
+    if hadamard:
+        st = [None if r is None else ctypes.byref(r) for r in rows]
+        _check(_lib().vcattn_prep_ex(ctypes.byref(s), _ptr(Q), st[0], _ptr(K), st[1], _ptr(V), st[2],
+                                     _ptr(perm), PREP_QK_HADAMARD, ctypes.byref(pp.struct), _ptr(ws), nbytes,
+                                     _stream(stream)), "vcattn_prep_ex")
+    elif all(r is None for r in rows):
         _check(_lib().vcattn_prep(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(perm),
                                   ctypes.byref(pp.struct), _ptr(ws), nbytes, _stream(stream)),
                "vcattn_prep")

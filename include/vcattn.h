@@ -166,6 +166,31 @@ vcattn_status vcattn_prep_strided(const vcattn_shape* shape, const void* Q, cons
                                   const vcattn_strides* sv, const int32_t* perm,
                                   const vcattn_prepped* out, void* ws, size_t ws_bytes, void* stream);
 
+/* vcattn_prep with options (`flags`, a bitwise OR of the values below; 0 =
+ * vcattn_prep) and optional row strides (sq, sk, sv: NULL = contiguous).
+ *
+ * VCATTN_PREP_QK_HADAMARD: the QK Hadamard rotation of the fused
+ * preprocessing chain (VC-Attention, Key Contribution 3 and Methodology: the
+ * chain applies a Hadamard transform to Q and K after the means and the
+ * gather, before the quantisers).  Each row of Q, and of K after centring,
+ * is multiplied by the 128-point Sylvester-Hadamard matrix H (H[i][j] =
+ * (-1)^popcount(i & j)) through a fast butterfly in a fixed FP32 order
+ * (stages h = 1, 2, 4, ..., 64; each pair (x[i], x[i + h]) with i & h == 0
+ * becomes (x[i] + x[i + h], x[i] - x[i + h]), rounded to FP32), then scaled
+ * by 2^-4 (Q) and 2^-3 (K), so that q' . k' = q . (k - mu_K) exactly in
+ * exact arithmetic (H H^T = 128 I).  The quantisers then act on the rotated
+ * rows; the V side, k_mean and qmu (from the unrotated q) are unchanged, and
+ * vcattn_attn consumes the result as it is.  The rotation spreads outlier
+ * channels of Q and K over all 128 channels before their per-block E4M3
+ * scales are set.  Rotary position embedding, the other step of the
+ * pages' chain, is not included: the pages give neither its positions nor
+ * its frequencies. */
+#define VCATTN_PREP_QK_HADAMARD 1
+vcattn_status vcattn_prep_ex(const vcattn_shape* shape, const void* Q, const vcattn_strides* sq,
+                             const void* K, const vcattn_strides* sk, const void* V,
+                             const vcattn_strides* sv, const int32_t* perm, int flags,
+                             const vcattn_prepped* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Preprocessing without a caller-provided workspace.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot
  * allocate device memory when they call the preprocessing, such as a plugin

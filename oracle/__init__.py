@@ -42,6 +42,8 @@ def _L():
         lib.orc_kmeans_scores.argtypes = [P, i64, P, i32, P]
         lib.orc_stable_sort.argtypes = [P, i64, i64, i32, P]
         lib.orc_prep.argtypes = [P, P, P, P, i64, i64] + [P] * 9
+        lib.orc_prep_ex.argtypes = [P, P, P, P, i64, i64, i32] + [P] * 9
+        lib.orc_hadamard128.argtypes = [P, P, i64]
         lib.orc_attn_emul.argtypes = [P] * 8 + [i64, f32, i32, f32, P, P, i64, i32, P, P]
         lib.orc_attn_dense.argtypes = [P, P, P, i64, f32, P, P, P, i64, P, P]
         _lib = lib
@@ -150,10 +152,24 @@ def stable_sort(labels, k):
     return perm
 
 
-def prep(Q, K, V, perm=None):
+PREP_QK_HADAMARD = 1
+
+
+def hadamard128(x):
+    """The fixed-order FP32 butterfly of the QK rotation, row by row:
+    float32 [rows, 128] -> x H (H the 128-point Sylvester-Hadamard matrix)."""
+    x = _c(x, np.float32).reshape(-1, D)
+    y = np.empty_like(x)
+    _L().orc_hadamard128(_p(x), _p(y), x.shape[0])
+    return y
+
+
+def prep(Q, K, V, perm=None, flags=0):
     """Preprocessing of all heads.  Returns a dict of numpy arrays:
     q8, k8 [BH, Npad, 128] u8; r8t [BH, 128, Npad] u8; q_scale, k_scale
-    [BH, Npad/64]; v_scale, k_mean [BH, 128]; v_mean [BH, Npad/64, 128]; qmu [BH, N]."""
+    [BH, Npad/64]; v_scale, k_mean [BH, 128]; v_mean [BH, Npad/64, 128]; qmu [BH, N].
+    flags & PREP_QK_HADAMARD: Q and centred K rotated by the Hadamard transform
+    before their quantisers."""
     Q, K, V = (_c(t, np.uint16) for t in (Q, K, V))
     BH, N, _ = Q.shape
     Np = npad(N)
@@ -166,7 +182,7 @@ def prep(Q, K, V, perm=None):
         v_mean=np.empty((BH, nbp, D), np.float32), qmu=np.empty((BH, N), np.float32))
     if perm is not None:
         perm = _c(perm, np.int32)
-    rc = _L().orc_prep(_p(Q), _p(K), _p(V), _p(perm), BH, N,
+    rc = _L().orc_prep_ex(_p(Q), _p(K), _p(V), _p(perm), BH, N, int(flags),
                        _p(out["q8"]), _p(out["k8"]), _p(out["r8t"]),
                        _p(out["q_scale"]), _p(out["k_scale"]), _p(out["v_scale"]),
                        _p(out["k_mean"]), _p(out["v_mean"]), _p(out["qmu"]))

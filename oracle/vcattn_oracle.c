@@ -333,11 +333,40 @@ static void quant_block(const float* x, int64_t rows, int64_t stride, int64_t co
   *scale = amax / 448.0f;
 }
 
-int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
-             int64_t BH, int64_t N,
-             uint8_t* q8, uint8_t* k8, uint8_t* r8t,
-             float* q_scale, float* k_scale, float* v_scale,
-             float* k_mean, float* v_mean, float* qmu) {
+/* QK Hadamard rotation [P3 Key Contribution 3, Methodology: the fused
+ * preprocessing chain applies a Hadamard transform to Q and K after the means
+ * and the gather, before the quantisers].  Reading (R17): the 128-point
+ * Sylvester-Hadamard transform y = x H, H[i][j] = (-1)^popcount(i & j),
+ * computed as the fast butterfly in a fixed FP32 order -- stages h = 1, 2,
+ * 4, ..., 64, each replacing every pair (x[i], x[i + h]) with i & h == 0 by
+ * (x[i] + x[i + h], x[i] - x[i + h]), each result rounded to FP32.  Since
+ * H H^T = 128 I, the rotated rows are scaled by 2^-4 (Q) and 2^-3 (K)
+ * (exact) so that q' . k' = q . k in exact arithmetic; the attention itself
+ * is unchanged. */
+static void hadamard128_row(float* x) {
+  for (int h = 1; h < ORC_D; h <<= 1)
+    for (int i = 0; i < ORC_D; ++i)
+      if ((i & h) == 0) {
+        float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+}
+void orc_hadamard128(const float* x, float* y, int64_t rows) {
+  for (int64_t r = 0; r < rows; ++r) {
+    memcpy(y + r * ORC_D, x + r * ORC_D, ORC_D * sizeof(float));
+    hadamard128_row(y + r * ORC_D);
+  }
+}
+
+#define ORC_PREP_QK_HADAMARD 1
+
+int orc_prep_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+                int64_t BH, int64_t N, int flags,
+                uint8_t* q8, uint8_t* k8, uint8_t* r8t,
+                float* q_scale, float* k_scale, float* v_scale,
+                float* k_mean, float* v_mean, float* qmu) {
+  const int rot = (flags & ORC_PREP_QK_HADAMARD) != 0;
   if (N < 1) return 1;
   const int64_t Npad = ((N + ORC_TILE - 1) / ORC_TILE) * ORC_TILE;
   const int64_t nbp = Npad / ORC_BLK;
@@ -383,21 +412,31 @@ int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int3
     /* Q: per 64-query block, original order. */
     for (int64_t j = 0; j < N; ++j)
       for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] = bf16_to_f32(q[j * ORC_D + d]);
-    for (int64_t b = 0; b < nb; ++b) {
-      int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
-      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, Q8 + r0 * ORC_D, ORC_D, &qs[b]);
-    }
-    /* qmu_i = q_i . mu_K, fmaf chain over d ascending (used for the LSE). */
+    /* qmu_i = q_i . mu_K, fmaf chain over d ascending (used for the LSE);
+     * from the unrotated q. */
     for (int64_t j = 0; j < N; ++j) {
       float acc = 0.0f;
       for (int d = 0; d < ORC_D; ++d) acc = fmaf(xf[j * ORC_D + d], km[d], acc);
       qmu[bh * N + j] = acc;
     }
+    if (rot)
+      for (int64_t j = 0; j < N; ++j) {
+        hadamard128_row(xf + j * ORC_D);
+        for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] *= 0.0625f;
+      }
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
+      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, Q8 + r0 * ORC_D, ORC_D, &qs[b]);
+    }
 
-    /* K: gathered by perm, centred, per-block scale. */
+    /* K: gathered by perm, centred, (rotated,) per-block scale. */
     for (int64_t j = 0; j < N; ++j) {
       int64_t src = p ? p[j] : j;
       for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] = bf16_to_f32(kk[src * ORC_D + d]) - km[d];
+      if (rot) {
+        hadamard128_row(xf + j * ORC_D);
+        for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] *= 0.125f;
+      }
     }
     for (int64_t b = 0; b < nb; ++b) {
       int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
@@ -433,6 +472,14 @@ int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int3
     free(xf);
   }
   return 0;
+}
+
+int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+             int64_t BH, int64_t N,
+             uint8_t* q8, uint8_t* k8, uint8_t* r8t,
+             float* q_scale, float* k_scale, float* v_scale,
+             float* k_mean, float* v_mean, float* qmu) {
+  return orc_prep_ex(Q, K, V, perm, BH, N, 0, q8, k8, r8t, q_scale, k_scale, v_scale, k_mean, v_mean, qmu);
 }
 
 /* ------------------------------------------------------------------ */

@@ -147,6 +147,57 @@ def test_prep_bit_exact(vc, orc, N):
     assert vc.last_device_error() == 0
 
 
+@pytest.mark.parametrize("N", [1, 63, 65, 129, 777, 2049])
+def test_prep_hadamard_bit_exact(vc, orc, N):
+    """The QK Hadamard rotation (vcattn_prep_ex): every prepped tensor equal
+    to the oracle's rotated preprocessing, bit for bit (the butterfly's FP32
+    order is part of the definition), also for a strided (B, N, H, D) input."""
+    H = 2
+    Q, K, V = _inputs(1, H, N, 8, 220 + N)
+    _, perm = vc.group(V, 8, 2)
+    pp = vc.prep(Q, K, V, perm, hadamard=True)
+    torch.cuda.synchronize()
+    assert vc.last_device_error() == 0
+    op = perm.reshape(H, N).cpu().numpy()
+    ref = orc.prep(_bits(Q), _bits(K), _bits(V), op, flags=orc.PREP_QK_HADAMARD)
+    got = {k: v.cpu().numpy() for k, v in pp.views().items()}
+    for key in PREP_KEYS:
+        g, r = got[key], ref[key]
+        if g.dtype == np.float32:
+            g, r = g.view(np.uint32), r.view(np.uint32)
+        bad = np.nonzero(g != r)
+        assert bad[0].size == 0, "%s differs at %d places, first %s" % (key, bad[0].size,
+                                                                      [b[:3] for b in bad])
+    Qs, Ks, Vs = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (Q, K, V))
+    pps = vc.prep(Qs, Ks, Vs, perm, hadamard=True)
+    for key, val in pp.views().items():
+        assert torch.equal(pps.views()[key], val), key
+
+
+def test_attn_with_hadamard_prep(vc, orc):
+    """Attention on the rotated preprocessing meets both bars (against the
+    oracle's rotated pipeline and against exact attention on the inputs)."""
+    N, H, k = 1500, 2, 8
+    Q, K, V = _inputs(1, H, N, k, 230)
+    _, perm = vc.group(V, k, 5)
+    pp = vc.prep(Q, K, V, perm, hadamard=True)
+    O32, L = vc.attn(pp, SM, out_f32=True)
+    torch.cuda.synchronize()
+    assert vc.last_device_error() == 0
+    Qb, Kb, Vb = _bits(Q), _bits(K), _bits(V)
+    op = perm.reshape(H, N).cpu().numpy()
+    opp = orc.prep(Qb, Kb, Vb, op, flags=orc.PREP_QK_HADAMARD)
+    for h in range(H):
+        Oe, Le = orc.attn_emul(opp, h, N, SM, tau8=TAU8)
+        Od, _ = orc.attn_dense(Qb[h], Kb[h], Vb[h], SM)
+        g = O32[0, h].cpu().numpy()
+        rel, mx, _ = _metrics(g, Oe)
+        assert rel <= REL_EMUL and mx <= ABS_EMUL, (rel, mx)
+        assert np.abs(L[0, h].cpu().numpy() - Le).max() <= LSE_EMUL
+        rel_d, _, cos_d = _metrics(g, Od)
+        assert rel_d <= REL_DENSE and cos_d >= COS_DENSE, (rel_d, cos_d)
+
+
 def test_prep_out_of_range_perm_is_reported_not_read(vc):
     """Permutation entries outside [0, N) (a stale or corrupt perm) are never
     dereferenced: the preprocessing reads those rows as zeros and reports a

@@ -659,3 +659,93 @@ def test_emul_end_to_end_close_to_dense(orc):
         cos = (Oe * Od).sum() / (np.linalg.norm(Oe) * np.linalg.norm(Od))
         assert rel <= 0.05 and cos >= 0.998, (rel, cos)
         assert np.abs(Le - Ld).max() < 0.05
+
+
+# ------------------------------------------------------ QK Hadamard rotation
+def test_hadamard_butterfly_is_the_sylvester_matrix(orc):
+    """The butterfly maps the unit vectors to the rows of the 128-point
+    Sylvester-Hadamard matrix (scipy.linalg.hadamard), so it computes x H
+    with H H^T = 128 I."""
+    from scipy.linalg import hadamard
+    H = hadamard(128).astype(np.float64)
+    Y = orc.hadamard128(np.eye(128, dtype=np.float32)).astype(np.float64)
+    assert np.array_equal(Y, H)
+    assert np.array_equal(Y @ Y.T, 128.0 * np.eye(128))
+
+
+def test_hadamard_butterfly_fp32_error_bound(orc):
+    """Seven stages of FP32 additions: each output is within 7 u sum|x| of
+    the exact x H (u = 2^-24), and a row of powers of two with no
+    cancellation is exact."""
+    from scipy.linalg import hadamard
+    H = hadamard(128).astype(np.float64)
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((2000, 128)) * np.exp(rng.uniform(-8, 8, (2000, 1)))).astype(np.float32)
+    x[::7, 3] *= 1000.0                        # outlier channels
+    y = orc.hadamard128(x).astype(np.float64)
+    exact = x.astype(np.float64) @ H
+    bound = 7 * 2.0 ** -24 * np.abs(x).astype(np.float64).sum(1, keepdims=True)
+    assert np.all(np.abs(y - exact) <= bound + 1e-30)
+    assert not np.array_equal(y, exact)       # FP32 rounding does happen
+    e = np.zeros((1, 128), np.float32)
+    e[0, :] = 2.0 ** -3
+    assert np.array_equal(orc.hadamard128(e)[0].astype(np.float64), e[0].astype(np.float64) @ H)
+
+
+def test_prep_hadamard_rotates_only_q_and_k(orc):
+    """With the rotation, the V side, the K mean and qmu are those of the
+    plain preprocessing; Q8 and K8 quantise x H / 16 and (k - mu_K) H / 8,
+    so the dequantised scores still approximate q . (k - mu_K) (the
+    rotation is orthogonal up to the power-of-two scaling), and on inputs
+    with outlier channels more closely than without the rotation."""
+    Q, K, V = _small_inputs(N=700, H=1, seed=71)
+    # a few outlier channels in Q and K (bf16 bit patterns scaled by 2^5)
+    Qo, Ko = Q.copy(), K.copy()
+    for t in (Qo, Ko):
+        t[..., 5] = ((t[..., 5].astype(np.uint32) + (5 << 7)) & 0xFFFF).astype(np.uint16)
+    labels, _ = orc.kmeans(V, 8, 2)
+    perm = orc.stable_sort(labels, 8)
+    for q, k in ((Q, K), (Qo, Ko)):
+        p0 = orc.prep(q, k, V, perm)
+        p1 = orc.prep(q, k, V, perm, flags=orc.PREP_QK_HADAMARD)
+        for key in ("r8t", "v_scale", "v_mean", "k_mean", "qmu"):
+            assert np.array_equal(p0[key], p1[key]), key
+        assert not np.array_equal(p0["q8"], p1["q8"]) and not np.array_equal(p0["k8"], p1["k8"])
+    N = Q.shape[1]
+
+    def scores(pp, q, k):
+        qd = orc.e4m3_decode(pp["q8"][0, :N]) * np.repeat(pp["q_scale"][0], 64)[:N, None]
+        kd = orc.e4m3_decode(pp["k8"][0, :N]) * np.repeat(pp["k_scale"][0], 64)[:N, None]
+        qf = (q[0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        kf = (k[0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)[perm[0]]
+        kc = kf - pp["k_mean"][0].astype(np.float64)
+        exact = qf @ kc.T
+        return np.linalg.norm(qd @ kd.T - exact) / np.linalg.norm(exact)
+
+    e_plain = scores(orc.prep(Qo, Ko, V, perm), Qo, Ko)
+    e_rot = scores(orc.prep(Qo, Ko, V, perm, flags=orc.PREP_QK_HADAMARD), Qo, Ko)
+    assert e_rot < 0.05 and e_plain < 0.2
+    assert e_rot < e_plain, (e_rot, e_plain)
+
+
+def test_emul_with_hadamard_close_to_dense(orc):
+    """The whole pipeline with the QK rotation meets the same bar against
+    exact attention (rel-L2 <= 0.05, cosine >= 0.998); with the exact
+    exponential it is softmax attention of the dequantised rotated tensors."""
+    w = W.WORKLOADS["tiny"]
+    Q, K, V = (W.bf16_bits(t)[0] for t in W.make_workload(w))
+    labels, _ = orc.kmeans(V, w.k, w.iters)
+    perm = orc.stable_sort(labels, w.k)
+    pp = orc.prep(Q, K, V, perm, flags=orc.PREP_QK_HADAMARD)
+    qidx = np.arange(0, w.N, 3)
+    for h in range(w.H):
+        Oe, Le = orc.attn_emul(pp, h, w.N, SM, qidx=qidx, tau8=6.0)
+        Od, Ld = orc.attn_dense(Q[h], K[h], V[h], SM, qidx=qidx)
+        rel = np.linalg.norm(Oe - Od) / np.linalg.norm(Od)
+        cos = (Oe * Od).sum() / (np.linalg.norm(Oe) * np.linalg.norm(Od))
+        assert rel <= 0.05 and cos >= 0.998, (rel, cos)
+        assert np.abs(Le - Ld).max() < 0.05
+    O1, L1 = orc.attn_emul(pp, 0, w.N, SM, flags=1)
+    q, k, v = _deq(orc, pp, 0, w.N)
+    o, lse2 = _softmax_attn(q, k, v, SM)
+    assert np.allclose(O1, o, rtol=1e-10, atol=1e-10)
