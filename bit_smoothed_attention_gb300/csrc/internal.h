@@ -85,9 +85,11 @@ struct GroupWs {
 size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws);
 // Tensor-core k-means assignment with an exact FP32 fallback (km_tc.cu);
 // 1 <= k <= 64.
+// tdump (test hook, nullable): [BH, N, 65] f32, the tensor-core scores T_c
+// (c < 64) and the token's filter bound E, written for every token.
 cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k,
                                 const float* cent, int32_t* labels, const GroupWs& ws, int iter,
-                                uint32_t* err, cudaStream_t s);
+                                uint32_t* err, cudaStream_t s, float* tdump = nullptr);
 cudaError_t launch_group(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k, int iters,
                          const float* init, int32_t* labels, int32_t* perm, float* centroids_out,
                          const GroupWs& ws, uint32_t* err, cudaStream_t s);

@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     km_assign_tc(const __grid_constant__ CUtensorMap tmv, int64_t N, int64_t H, int k, int tpc,
                  const float* __restrict__ cent,
                  int32_t* __restrict__ labels, KmAmb* __restrict__ amb, uint32_t* __restrict__ amb_count,
-                 float* __restrict__ head_cn, float* __restrict__ head_h, uint32_t* __restrict__ err) {
+                 float* __restrict__ head_cn, float* __restrict__ head_h, uint32_t* __restrict__ err,
+                 float* __restrict__ tdump) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -301,6 +302,12 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
         uint64_t cand = 0;  // bit c: cluster c can still win
 #pragma unroll
         for (int q = 0; q < 8; ++q) cand |= static_cast<uint64_t>(cm8[q]) << (8 * q);
+        if (tdump) {  // test hook: the tensor-core scores T_c and the token's bound E
+          float* td = tdump + (bh * N + j) * 65;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) td[c] = T[c];
+          td[64] = E;
+        }
         const int best = __ffsll(static_cast<long long>(cand)) - 1;
         if (cand & (cand - 1)) {  // left open: km_fixup decides
           const uint32_t slot = atomicAdd(amb_count, 1u);
@@ -438,7 +445,7 @@ PFN_cuTensorMapEncodeTiled_v12000 km_encoder() {
 cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k,
                                 const float* cent,
                                 int32_t* labels, const GroupWs& ws, int iter, uint32_t* err,
-                                cudaStream_t s) {
+                                cudaStream_t s, float* tdump) {
   if (k < 1 || k > 64) return cudaErrorInvalidValue;
   auto enc = km_encoder();
   if (!enc) return cudaErrorInvalidValue;
@@ -477,7 +484,7 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t 
   // before the first iteration, then by the previous fix-up).
   uint32_t* cnt = ws.amb_count + (iter & 1);
   km_assign_tc<<<grid, KT_THREADS, KT_SMEM, s>>>(m, N, lv.H, k, static_cast<int>(tpc), cent, labels, ws.amb, cnt,
-                                                 ws.head_cn, ws.head_h, err);
+                                                 ws.head_cn, ws.head_h, err, tdump);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   km_fixup<<<static_cast<unsigned>(slots * 2), 128, 0, s>>>(V, lv, N, k, cent, labels, ws.amb, cnt,

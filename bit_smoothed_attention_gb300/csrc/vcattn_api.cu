@@ -317,6 +317,27 @@ vcattn_status vcattn_test_attn_stalled_after(const vcattn_shape* s, const vcattn
   return attn_impl(s, in, sm_scale, 8, 6.0f, 0, nullptr, O, nullptr, lse2, stream, steps << 8);
 }
 
+vcattn_status vcattn_test_km_scores(const vcattn_shape* s, const void* V, int k, const float* centroids,
+                                    int32_t* labels, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  vcattn_status st = check_shape(s);
+  if (st != VCATTN_OK) return st;
+  if (k < 1 || k > vc::KMAX) return VCATTN_ERR_UNSUPPORTED;
+  if (!V || !centroids || !labels || !scores || !ws || !aligned16(V) || !aligned16(centroids) ||
+      !aligned16(labels) || !aligned16(scores) || !aligned16(ws))
+    return VCATTN_ERR_INVALID_ARG;
+  const int64_t BH = s->B * s->H;
+  vc::GroupWs w{};
+  if (ws_bytes < vc::group_ws_layout(BH, s->N, k, ws, &w)) return VCATTN_ERR_INVALID_ARG;
+  uint32_t* err = err_word(&st);
+  if (!err) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(w.amb_count, 0, 2 * sizeof(uint32_t), cs);
+  if (e == cudaSuccess)
+    e = vc::launch_km_assign_tc(static_cast<const uint16_t*>(V), vc::contiguous_rows(s->H, s->N), BH, s->N, k,
+                                centroids, labels, w, 0, err, cs, scores);
+  return from_cuda(e);
+}
+
 vcattn_status vcattn_test_expcast(const float* x, const float* A, const float* B, uint8_t* codes, int64_t n,
                                   void* stream) {
   if (n < 0 || (n & 3) != 0) return VCATTN_ERR_INVALID_ARG;

@@ -321,6 +321,20 @@ vcattn_status vcattn_test_attn_stalled(const vcattn_shape* shape, const vcattn_p
  * records VCATTN_ERR_TIMEOUT. */
 vcattn_status vcattn_test_attn_stalled_after(const vcattn_shape* shape, const vcattn_prepped* in,
                                              float sm_scale, int steps, void* O, float* lse2, void* stream);
+/* Test hook for the k-means assignment's tensor-core filter (not part of the
+ * method): one assign step of vcattn_group from the given centroids, with
+ * the filter's inputs written out.  The tensor core computes an
+ * approximation T_c of each token's FP32 score v . c_c - |c_c|^2 / 2; the
+ * filter keeps the clusters within a bound E of the largest T_c and exact
+ * FP32 chains decide among them, which is exact if |T_c - score_c| <= E / 2.
+ *   V          bf16 [B,H,N,D] (device)
+ *   centroids  f32 [B,H,k,D] (device), the centroids of the step
+ *   labels     i32 [B,H,N] (device) out: the labels of this one step
+ *   scores     f32 [B,H,N,65] (device) out: T_c for c < 64 (-inf for c >= k)
+ *              and E at index 64, for every token
+ *   ws         scratch of vcattn_group_workspace_bytes(shape, k) */
+vcattn_status vcattn_test_km_scores(const vcattn_shape* shape, const void* V, int k, const float* centroids,
+                                    int32_t* labels, float* scores, void* ws, size_t ws_bytes, void* stream);
 /* Test hook for the byte-level check of ExpCast-FP8 (VC-Attention, Key
  * Contribution 2: the probability's E4M3 byte from one FMA and one integer
  * rounding of the max-subtracted log2 score).  Runs the attention kernel's

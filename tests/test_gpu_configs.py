@@ -90,7 +90,9 @@ def test_schedule_regroup_then_reuse(vc, orc):
     late in the schedule the inputs carry drift of up to 2.45 standard
     deviations, the logits grow accordingly and the method itself (the
     emulating oracle) moves away from exact attention, so there the GPU's
-    error against exact attention must equal the oracle's."""
+    error against exact attention must equal the oracle's; the oracle grouped
+    afresh on the late step does only slightly better than the frozen
+    permutation."""
     w = W.WORKLOADS["schedule"]
     sm = float(np.float32(w.sm_scale))
     Q0, K0, V0 = W.make_workload(w, device="cuda")
@@ -136,6 +138,17 @@ def test_schedule_regroup_then_reuse(vc, orc):
                 assert rel_d <= REL_DENSE and cos_d >= COS_DENSE, (t, h, rel_d, cos_d)
             else:
                 assert abs(rel_d - rel_m) <= 0.1 * rel_m + 1e-3, (t, h, rel_d, rel_m)
+                # The same pipeline grouped afresh on this step's V: its
+                # error against exact attention is nearly as large, so most
+                # of the late loss comes from the drifted inputs (larger
+                # logits), and at most 30% from the permutation frozen at
+                # step 12.
+                fl, _ = orc.kmeans(Vb, w.k, w.iters)
+                fpp = orc.prep(Qb, Kb, Vb, orc.stable_sort(fl, w.k))
+                Of, _ = orc.attn_emul(fpp, 0, w.N, sm, qidx=qidx, tau8=TAU8)
+                rel_f, _, _ = _metrics(Of, Od)
+                print("schedule step %2d head %2d: oracle with a fresh grouping %.4f" % (t, h, rel_f))
+                assert rel_f >= 0.7 * rel_m, (t, h, rel_m, rel_f)
     print("schedule: attention ms per step, median %.3f (min %.3f, max %.3f)"
           % (float(np.median(times[1:])), min(times[1:]), max(times[1:])))
 
