@@ -77,23 +77,26 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // r0 (rows r0 + threadIdx.x / 16 + 16 u); loaded one block ahead so that the
 // gather index is in a register when the copy is issued.
 struct Src4 {
-  int64_t r[4];
+  int32_t r[4];
 };
 // A perm entry outside [0, N) is never dereferenced: its row is staged as
-// zeros and ERR_BAD_PERM is recorded in *err.
-__device__ __forceinline__ Src4 load_src(const int32_t* perm, int64_t r0, int64_t N, uint32_t* err) {
+// zeros and `bad` is set (the kernel reports it once, at its end, through
+// report_bad_perm; an atomic here would slow every load).
+__device__ __forceinline__ Src4 load_src(const int32_t* perm, int64_t r0, int64_t N, bool& bad) {
   Src4 s;
+  const int32_t n32 = static_cast<int32_t>(N);  // N < 2^30
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    const int64_t r = r0 + u * 16 + (static_cast<int>(threadIdx.x) >> 4);
-    int64_t src = r < N ? (perm ? static_cast<int64_t>(perm[r]) : r) : -1;
-    if (r < N && (src < 0 || src >= N)) {
-      atomicOr(err, ERR_BAD_PERM);
-      src = -1;
-    }
-    s.r[u] = src;
+    const int32_t r = static_cast<int32_t>(r0) + u * 16 + (static_cast<int>(threadIdx.x) >> 4);
+    const int32_t src = r < n32 ? (perm ? perm[r] : r) : -1;
+    const bool out = r < n32 && static_cast<uint32_t>(src) >= static_cast<uint32_t>(n32);
+    bad |= out;
+    s.r[u] = out ? -1 : src;
   }
   return s;
+}
+__device__ __forceinline__ void report_bad_perm(bool bad, uint32_t* err) {
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(err, ERR_BAD_PERM);
 }
 // rows src of the head at `base`, `sn` elements apart
 __device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, int32_t sn, const Src4& src4) {
@@ -103,7 +106,7 @@ __device__ __forceinline__ void stage_rows(uint8_t* tile, const uint16_t* base, 
     const int row = piece >> 4, chunk = piece & 15;
     uint8_t* dst = tile + swz(row, chunk);
     if (src4.r[u] >= 0) {
-      const int64_t src = src4.r[u];
+      const int32_t src = src4.r[u];
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                    "l"(base + static_cast<int64_t>(static_cast<int32_t>(src)) * sn + chunk * 8)
                    : "memory");
@@ -210,14 +213,15 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
   const uint16_t* Kh = K + lk.head(bh);
   const uint16_t* Vh = V + lv.head(bh);
   // gather indices of the next block to stage (one block ahead)
-  Src4 nk = load_src(nullptr, b0 * BLK, N, err), nv = load_src(ph, b0 * BLK, N, err);
+  bool bad = false;
+  Src4 nk = load_src(nullptr, b0 * BLK, N, bad), nv = load_src(ph, b0 * BLK, N, bad);
   auto stage = [&](int64_t b, int buf) {
     stage_rows(ssm + buf * 2 * TILE_SMEM, Kh, lk.sn, nk);
     stage_rows(ssm + buf * 2 * TILE_SMEM + TILE_SMEM, Vh, lv.sn, nv);
     cp_commit();
     if (b + 1 < b1) {
-      nk = load_src(nullptr, (b + 1) * BLK, N, err);
-      nv = load_src(ph, (b + 1) * BLK, N, err);
+      nk = load_src(nullptr, (b + 1) * BLK, N, bad);
+      nv = load_src(ph, (b + 1) * BLK, N, bad);
     }
   };
   stage(b0, 0);
@@ -258,6 +262,7 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
     }
     __syncthreads();  // this stage may be restaged next iteration
   }
+  report_bad_perm(bad, err);
 #pragma unroll
   for (int c = 0; c < 8; ++c) am[c] = max16(am[c]);
   if (m.g == 0)
@@ -321,14 +326,47 @@ __global__ void __launch_bounds__(D * KM_SEG) prep_kmean(const float* __restrict
   }
 }
 
-// Quantisers.  Each CTA handles QUANT_BPC consecutive blocks; the next
-// block's Q, K (gathered) and V (gathered) rows are staged while the current
-// one is quantised.  grid (ceil(nbp / QUANT_BPC), BH), block 256, dynamic
-// shared memory QUANT_SMEM: two stages of the three tiles, the transposed
-// residual bytes and small reduction buffers.
-constexpr int QUANT_BPC = 4;
-constexpr int QUANT_SMEM = 2 * 3 * TILE_SMEM + D * (BLK + 16) + D * 4 + 64;
-__global__ void __launch_bounds__(256) prep_quant(
+// Quantisers, one tensor per CTA (blockIdx.z: 0 = Q, 1 = K, 2 = V).  Each CTA
+// handles QUANT_BPC consecutive 64-token blocks of one (b, h) through a ring
+// of QUANT_NST staged tiles (16 KiB each, all rows of a tile in flight at
+// once), so QUANT_NST - 1 blocks load while one is quantised.  One tensor per
+// CTA keeps the per-thread state small (32 values), so three CTAs fit on an
+// SM, and lets each path do only its own arithmetic:
+//   Q: block amax from the bf16 bits (|x| as an integer max of the bit
+//      patterns, exact), q8 = E4M3(fl(x * inv)), q_scale, and qmu (one fmaf
+//      chain per row, warps 0-1);
+//   K: gathered, centred (fl(k - mu_K)), block amax, k8, k_scale;
+//   V: gathered, fl(fl(v - mu_b) * vinv_d) transposed to r8t, the mean
+//      operand of the block, zero means for padding blocks.
+// The FP32 operations and their order are those of the per-element
+// definition (packed f32x2 instructions round each lane as the scalar ones
+// do).  With the QK Hadamard flag the Q and K paths rotate first (four lanes
+// per row, as in hadamard_row32).  grid (ceil(nbp / QUANT_BPC), BH, 3),
+// block 256, dynamic shared memory QUANT_SMEM.
+constexpr int QUANT_BPC = 8;
+constexpr int QUANT_NST = 3;
+constexpr int QUANT_SMEM = QUANT_NST * TILE_SMEM + D * (BLK + 16) + D * 4 + 64;
+
+__device__ __forceinline__ float2 bf2f(uint32_t w) {  // (low, high) bf16 of a word as floats
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t e4m3x4(float2 a, float2 b) {
+  return e4m3x2(a.x, a.y) | (e4m3x2(b.x, b.y) << 16);
+}
+// Block max over all 256 threads (one barrier; `red` is reused after the
+// caller's next barrier).
+__device__ __forceinline__ float block_max1(float a, float* red) {
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+__global__ void __launch_bounds__(256, 3) prep_quant(
     const uint16_t* __restrict__ Q, RowLayout lq, const uint16_t* __restrict__ K, RowLayout lk,
     const uint16_t* __restrict__ V, RowLayout lv,
     const int32_t* __restrict__ perm, int64_t N, int64_t Npad, int nbp,
@@ -338,145 +376,210 @@ __global__ void __launch_bounds__(256) prep_quant(
     float* __restrict__ k_scale, float* __restrict__ qmu, float* __restrict__ vmu_op, uint32_t* err,
     int rot) {
   extern __shared__ __align__(128) uint8_t qsm[];
-  uint8_t (*tb)[BLK + 16] = reinterpret_cast<uint8_t (*)[BLK + 16]>(qsm + 6 * TILE_SMEM);
-  float* kmu = reinterpret_cast<float*>(qsm + 6 * TILE_SMEM + D * (BLK + 16));
+  uint8_t (*tb)[BLK + 16] = reinterpret_cast<uint8_t (*)[BLK + 16]>(qsm + QUANT_NST * TILE_SMEM);
+  float* kmu = reinterpret_cast<float*>(qsm + QUANT_NST * TILE_SMEM + D * (BLK + 16));
   float* red = kmu + D;
   const Map m = thread_map();
   const int64_t bh = blockIdx.y;
+  const int z = blockIdx.z;  // 0 = Q, 1 = K, 2 = V
   const int64_t nb = ceil_div(N, BLK);
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * QUANT_BPC;
   const int64_t b1 = b0 + QUANT_BPC < nbp ? b0 + QUANT_BPC : nbp;
-  const int32_t* ph = perm ? perm + bh * N : nullptr;
-  Src4 nq = load_src(nullptr, b0 * BLK, N, err), ng = load_src(ph, b0 * BLK, N, err);
-  auto stage = [&](int64_t b, int buf) {
-    uint8_t* t = qsm + buf * 3 * TILE_SMEM;
-    stage_rows(t, Q + lq.head(bh), lq.sn, nq);
-    stage_rows(t + TILE_SMEM, K + lk.head(bh), lk.sn, ng);
-    stage_rows(t + 2 * TILE_SMEM, V + lv.head(bh), lv.sn, ng);
-    cp_commit();
-    if (b + 1 < b1) {
-      nq = load_src(nullptr, (b + 1) * BLK, N, err);
-      ng = load_src(ph, (b + 1) * BLK, N, err);
+  const int32_t* ph = (perm && z > 0) ? perm + bh * N : nullptr;
+  const uint16_t* src = z == 0 ? Q + lq.head(bh) : z == 1 ? K + lk.head(bh) : V + lv.head(bh);
+  const int32_t sn = z == 0 ? lq.sn : z == 1 ? lk.sn : lv.sn;
+  // the ring: block b in stage (b - b0) % QUANT_NST; the gather indices of
+  // the next block to stage are loaded one staging ahead
+  bool bad = false;
+  Src4 nxt = load_src(ph, b0 * BLK, N, bad);
+  int64_t bs = b0;  // next block to stage
+  auto stage_next = [&]() {
+    if (bs < b1) {
+      stage_rows(qsm + ((bs - b0) % QUANT_NST) * TILE_SMEM, src, sn, nxt);
+      ++bs;
+      if (bs < b1) nxt = load_src(ph, bs * BLK, N, bad);
     }
+    cp_commit();  // one group per call, empty past the last block
   };
-  stage(b0, 0);
-  if (threadIdx.x < D) kmu[threadIdx.x] = k_mean[bh * D + threadIdx.x];
-  // per-channel inverse scales of the V residual (the same for every block)
-  float vinv[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const float am = __uint_as_float(vamax[bh * D + 8 * m.cc + c]);
-    vinv[c] = am >= AMAX_FLOOR ? 448.0f / am : 0.0f;
+  for (int u = 0; u < QUANT_NST - 1; ++u) stage_next();
+  if (z < 2 && threadIdx.x < D) kmu[threadIdx.x] = k_mean[bh * D + threadIdx.x];
+  float vinv[8];
+  if (z == 2) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float am = __uint_as_float(vamax[bh * D + 8 * m.cc + c]);
+      vinv[c] = am >= AMAX_FLOOR ? 448.0f / am : 0.0f;
+    }
   }
 
   for (int64_t b = b0; b < b1; ++b) {
-    const int buf = static_cast<int>((b - b0) & 1);
-    if (b + 1 < b1) {
-      stage(b + 1, buf ^ 1);
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
-    __syncthreads();
-    const uint8_t* tq = qsm + buf * 3 * TILE_SMEM;
-    const uint8_t* tk = tq + TILE_SMEM;
-    const uint8_t* tv = tq + 2 * TILE_SMEM;
+    cp_wait<QUANT_NST - 2>();
+    __syncthreads();  // block b has landed everywhere; the stage of b - 1 is free
+    stage_next();
+    const uint8_t* t = qsm + ((b - b0) % QUANT_NST) * TILE_SMEM;
     const int64_t r0 = b * BLK + 4 * m.g;
+    const bool tail = b * BLK + BLK > N;  // the block holds rows past N
     const bool pad_block = b >= nb;
 
-    // the block's V means, needed below (loaded early to hide the latency)
-    const int64_t mo = (bh * nbp + b) * D + 8 * m.cc;
-    float mu[8];
+    if (z == 2) {
+      // ---- V: gathered, block-demeaned residual, per-channel scale, transposed ----
+      const int64_t mo = (bh * nbp + b) * D + 8 * m.cc;
+      float mu[8];
+      if (pad_block) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) mu[c] = pad_block ? 0.0f : v_mean[mo + c];
-
-    // ---- Q (per 64-query block, original order) and K (gathered, centred,
-    // per 64-key block): both block maxima in one reduction ----
-    float2 am2;
-    if (!rot) {
-      float x[4][8], xk[4][8];
-      read_rows(tq, m.g, m.cc, x);
-      read_rows(tk, m.g, m.cc, xk);
-      float a = 0.0f, ak = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          a = fmaxf(a, fabsf(x[i][c]));
-          xk[i][c] = (r0 + i < N) ? xk[i][c] - kmu[8 * m.cc + c] : 0.0f;
-          ak = fmaxf(ak, fabsf(xk[i][c]));
-        }
-      am2 = block_max2(a, ak, red);
-      const bool lq = am2.x >= AMAX_FLOOR, lk = am2.y >= AMAX_FLOOR;
-      const float iq = lq ? 448.0f / am2.x : 0.0f, ik = lk ? 448.0f / am2.y : 0.0f;
+        for (int c = 0; c < 8; ++c) mu[c] = 0.0f;
+      } else {
+        const float4 a0 = *reinterpret_cast<const float4*>(v_mean + mo);
+        const float4 a1 = *reinterpret_cast<const float4*>(v_mean + mo + 4);
+        mu[0] = a0.x; mu[1] = a0.y; mu[2] = a0.z; mu[3] = a0.w;
+        mu[4] = a1.x; mu[5] = a1.y; mu[6] = a1.z; mu[7] = a1.w;
+      }
+      const float2 nmu[4] = {make_float2(-mu[0], -mu[1]), make_float2(-mu[2], -mu[3]),
+                             make_float2(-mu[4], -mu[5]), make_float2(-mu[6], -mu[7])};
+      const float2 vi[4] = {make_float2(vinv[0], vinv[1]), make_float2(vinv[2], vinv[3]),
+                            make_float2(vinv[4], vinv[5]), make_float2(vinv[6], vinv[7])};
+      uint2 by[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float y[8], z[8];
+        const uint4 u = *reinterpret_cast<const uint4*>(t + swz(4 * m.g + i, m.cc));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float2 y[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          y[c] = (lq && r0 + i < N) ? x[i][c] * iq : 0.0f;
-          z[c] = lk ? xk[i][c] * ik : 0.0f;
+        for (int e = 0; e < 4; ++e) y[e] = __fmul2_rn(__fadd2_rn(bf2f(w[e]), nmu[e]), vi[e]);
+        if (tail && r0 + i >= N) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) y[e] = make_float2(0.0f, 0.0f);
         }
-        *reinterpret_cast<uint2*>(q8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(y);
-        *reinterpret_cast<uint2*>(k8 + (bh * Npad + r0 + i) * D + 8 * m.cc) = e4m3x8(z);
+        by[i] = make_uint2(e4m3x4(y[0], y[1]), e4m3x4(y[2], y[3]));
       }
+      // channel c's bytes of the thread's 4 rows -> one 32-bit word of tb[d][4g..4g+3]
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t sel = static_cast<uint32_t>((c & 3) | ((4 + (c & 3)) << 4));
+        const uint32_t w01 = c < 4 ? __byte_perm(by[0].x, by[1].x, sel) : __byte_perm(by[0].y, by[1].y, sel);
+        const uint32_t w23 = c < 4 ? __byte_perm(by[2].x, by[3].x, sel) : __byte_perm(by[2].y, by[3].y, sel);
+        *reinterpret_cast<uint32_t*>(&tb[8 * m.cc + c][4 * m.g]) = __byte_perm(w01, w23, 0x5410);
+      }
+      if (pad_block && m.g == 0) {
+        *reinterpret_cast<float4*>(v_mean + mo) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(v_mean + mo + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      // the mean operand of the rank-one restoration MMA: one 16-byte row
+      // per channel d, (hi, hi, lo, 0) of mu_b[d] / v_scale[d] (2 KiB per
+      // block, so the mean tile of any two blocks is two contiguous copies)
+      if (threadIdx.x < D) {
+        const int d = threadIdx.x;
+        const float mud = pad_block ? 0.0f : v_mean[(bh * nbp + b) * D + d];
+        const float uq = mud / v_scale[bh * D + d];
+        const float hi = to_tf32(uq);
+        const float lo = to_tf32(uq - hi);
+        reinterpret_cast<float4*>(vmu_op + (bh * nbp + b) * (4 * D))[d] = make_float4(hi, hi, lo, 0.0f);
+      }
+      __syncthreads();
+      {
+        const int d = threadIdx.x >> 1, h = threadIdx.x & 1;
+        const uint4* s4 = reinterpret_cast<const uint4*>(&tb[d][32 * h]);
+        uint4* dst = reinterpret_cast<uint4*>(r8t + (bh * D + d) * Npad + b * BLK + 32 * h);
+        dst[0] = s4[0];
+        dst[1] = s4[1];
+      }
+    } else if (!rot) {
+      // ---- Q (original order) or K (gathered, centred): per 64-row block ----
+      uint8_t* out = z == 0 ? q8 : k8;
+      uint32_t w[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = *reinterpret_cast<const uint4*>(t + swz(4 * m.g + i, m.cc));
+        w[i][0] = u.x; w[i][1] = u.y; w[i][2] = u.z; w[i][3] = u.w;
+      }
+      float2 x[4][4];
+      float a;
+      if (z == 0) {
+        // |x| of bf16 as the integer max of the sign-cleared bit patterns
+        uint32_t mb = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mb = __vmaxu2(mb, w[i][e] & 0x7FFF7FFFu);
+        a = __uint_as_float(((mb >> 16) > (mb & 0xFFFFu) ? (mb >> 16) : (mb & 0xFFFFu)) << 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[i][e] = bf2f(w[i][e]);  // rows past N are staged as +0
+      } else {
+        const float* km = kmu + 8 * m.cc;
+        const float2 nk[4] = {make_float2(-km[0], -km[1]), make_float2(-km[2], -km[3]),
+                              make_float2(-km[4], -km[5]), make_float2(-km[6], -km[7])};
+        a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[i][e] = __fadd2_rn(bf2f(w[i][e]), nk[e]);
+          if (tail && r0 + i >= N) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[i][e] = make_float2(0.0f, 0.0f);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a = fmaxf(a, fmaxf(fabsf(x[i][e].x), fabsf(x[i][e].y)));
+        }
+      }
+      const float amax = block_max1(a, red);
+      const bool live = amax >= AMAX_FLOOR;
+      const float inv = live ? 448.0f / amax : 0.0f;
+      const float2 iv = make_float2(inv, inv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint2 o = make_uint2(0u, 0u);
+        if (live) {
+          float2 y[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) y[e] = __fmul2_rn(x[i][e], iv);
+          o = make_uint2(e4m3x4(y[0], y[1]), e4m3x4(y[2], y[3]));
+        }
+        *reinterpret_cast<uint2*>(out + (bh * Npad + r0 + i) * D + 8 * m.cc) = o;
+      }
+      if (threadIdx.x == 0) (z == 0 ? q_scale : k_scale)[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
     } else {
-      // QK Hadamard rotation before the quantisers: thread (row rr, quarter
-      // qq) holds channels 32 qq .. 32 qq + 31 of one row; butterfly stages
-      // h = 1..16 run in registers, h = 32 and 64 across the row's four
-      // lanes (lane ^ 1, lane ^ 2).  Q is scaled by 2^-4 and K by 2^-3
-      // afterwards (exact), so q' . k' = q . (k - mu_K).
+      // ---- Q or centred K with the Hadamard rotation: thread (row rr,
+      // quarter qq) holds channels 32 qq .. 32 qq + 31 of one row ----
+      uint8_t* out = z == 0 ? q8 : k8;
       const int rr = threadIdx.x >> 2, qq = threadIdx.x & 3;
       const bool valid = b * BLK + rr < N;
-      float hq[32], hk[32];
+      float hx[32];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        float t[8], u[8];
-        unpack8(*reinterpret_cast<const uint4*>(tq + swz(rr, 4 * qq + c4)), t);
-        unpack8(*reinterpret_cast<const uint4*>(tk + swz(rr, 4 * qq + c4)), u);
+        float tv[8];
+        unpack8(*reinterpret_cast<const uint4*>(t + swz(rr, 4 * qq + c4)), tv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          hq[8 * c4 + e] = t[e];
-          hk[8 * c4 + e] = valid ? u[e] - kmu[32 * qq + 8 * c4 + e] : 0.0f;
-        }
+        for (int e = 0; e < 8; ++e)
+          hx[8 * c4 + e] = z == 0 ? tv[e] : (valid ? tv[e] - kmu[32 * qq + 8 * c4 + e] : 0.0f);
       }
-      hadamard_row32(hq, qq);
-      hadamard_row32(hk, qq);
-      float a = 0.0f, ak = 0.0f;
+      hadamard_row32(hx, qq);
+      const float sc = z == 0 ? 0.0625f : 0.125f;
+      float a = 0.0f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        hq[e] *= 0.0625f;
-        hk[e] *= 0.125f;
-        a = fmaxf(a, fabsf(hq[e]));
-        ak = fmaxf(ak, fabsf(hk[e]));
+        hx[e] *= sc;
+        a = fmaxf(a, fabsf(hx[e]));
       }
-      am2 = block_max2(a, ak, red);
-      const bool lq = am2.x >= AMAX_FLOOR, lk = am2.y >= AMAX_FLOOR;
-      const float iq = lq ? 448.0f / am2.x : 0.0f, ik = lk ? 448.0f / am2.y : 0.0f;
-      uint2 oq[4], ok[4];
+      const float amax = block_max1(a, red);
+      const bool live = amax >= AMAX_FLOOR;
+      const float inv = live ? 448.0f / amax : 0.0f;
+      uint2 o4[4];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        float y[8], z[8];
+        float y[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          y[e] = (lq && valid) ? hq[8 * c4 + e] * iq : 0.0f;
-          z[e] = lk ? hk[8 * c4 + e] * ik : 0.0f;
-        }
-        oq[c4] = e4m3x8(y);
-        ok[c4] = e4m3x8(z);
+        for (int e = 0; e < 8; ++e) y[e] = (live && valid) ? hx[8 * c4 + e] * inv : 0.0f;
+        o4[c4] = e4m3x8(y);
       }
-      uint4* dq = reinterpret_cast<uint4*>(q8 + (bh * Npad + b * BLK + rr) * D + 32 * qq);
-      uint4* dk = reinterpret_cast<uint4*>(k8 + (bh * Npad + b * BLK + rr) * D + 32 * qq);
-      dq[0] = make_uint4(oq[0].x, oq[0].y, oq[1].x, oq[1].y);
-      dq[1] = make_uint4(oq[2].x, oq[2].y, oq[3].x, oq[3].y);
-      dk[0] = make_uint4(ok[0].x, ok[0].y, ok[1].x, ok[1].y);
-      dk[1] = make_uint4(ok[2].x, ok[2].y, ok[3].x, ok[3].y);
+      uint4* dst = reinterpret_cast<uint4*>(out + (bh * Npad + b * BLK + rr) * D + 32 * qq);
+      dst[0] = make_uint4(o4[0].x, o4[0].y, o4[1].x, o4[1].y);
+      dst[1] = make_uint4(o4[2].x, o4[2].y, o4[3].x, o4[3].y);
+      if (threadIdx.x == 0) (z == 0 ? q_scale : k_scale)[bh * nbp + b] = live ? amax / 448.0f : 1.0f;
     }
-    if (threadIdx.x == 0) {
-      q_scale[bh * nbp + b] = am2.x >= AMAX_FLOOR ? am2.x / 448.0f : 1.0f;
-      k_scale[bh * nbp + b] = am2.y >= AMAX_FLOOR ? am2.y / 448.0f : 1.0f;
-    }
-    if (threadIdx.x < BLK) {
+    if (z == 0 && threadIdx.x < BLK) {
       // qmu = q . mu_K (the unrotated q): one fmaf chain over d ascending
       const int rr = threadIdx.x;
       const int64_t r = b * BLK + rr;
@@ -484,60 +587,15 @@ __global__ void __launch_bounds__(256) prep_quant(
         float acc = 0.0f;
         for (int cc = 0; cc < 16; ++cc) {
           float qv[8];
-          unpack8(*reinterpret_cast<const uint4*>(tq + swz(rr, cc)), qv);
+          unpack8(*reinterpret_cast<const uint4*>(t + swz(rr, cc)), qv);
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc = __fmaf_rn(qv[e], kmu[8 * cc + e], acc);
         }
         qmu[bh * N + r] = acc;
       }
     }
-
-    // ---- V: gathered, block-demeaned residual, per-channel scale, transposed ----
-    float x[4][8];
-    read_rows(tv, m.g, m.cc, x);
-    uint2 by[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float y[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) y[c] = (r0 + i < N) ? (x[i][c] - mu[c]) * vinv[c] : 0.0f;
-      by[i] = e4m3x8(y);
-    }
-    // channel c's bytes of the thread's 4 rows -> one 32-bit word of tb[d][4g..4g+3]
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t sel = static_cast<uint32_t>((c & 3) | ((4 + (c & 3)) << 4));
-      const uint32_t w01 = c < 4 ? __byte_perm(by[0].x, by[1].x, sel) : __byte_perm(by[0].y, by[1].y, sel);
-      const uint32_t w23 = c < 4 ? __byte_perm(by[2].x, by[3].x, sel) : __byte_perm(by[2].y, by[3].y, sel);
-      *reinterpret_cast<uint32_t*>(&tb[8 * m.cc + c][4 * m.g]) = __byte_perm(w01, w23, 0x5410);
-    }
-    if (pad_block && m.g == 0) {
-      *reinterpret_cast<float4*>(v_mean + mo) = make_float4(0.f, 0.f, 0.f, 0.f);
-      *reinterpret_cast<float4*>(v_mean + mo + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-    {
-      const int d = threadIdx.x >> 1, h = threadIdx.x & 1;
-      const uint4* src = reinterpret_cast<const uint4*>(&tb[d][32 * h]);
-      uint4* dst = reinterpret_cast<uint4*>(r8t + (bh * D + d) * Npad + b * BLK + 32 * h);
-      dst[0] = src[0];
-      dst[1] = src[1];
-    }
-    // ---- mean operand of the rank-one restoration MMA ----
-    // One 16-byte row per channel d: (hi, hi, lo, 0) of mu_b[d] / v_scale[d],
-    // K-slots 0..3 of the [K = 8] x [N = 128] tf32 B operand for whichever
-    // half of a 128-key tile the block lands in (2 KiB per block, so the
-    // mean tile of any two blocks is two contiguous copies).
-    if (threadIdx.x < D) {
-      const int d = threadIdx.x;
-      const float mud = pad_block ? 0.0f : v_mean[(bh * nbp + b) * D + d];
-      const float u = mud / v_scale[bh * D + d];
-      const float hi = to_tf32(u);
-      const float lo = to_tf32(u - hi);
-      reinterpret_cast<float4*>(vmu_op + (bh * nbp + b) * (4 * D))[d] = make_float4(hi, hi, lo, 0.0f);
-    }
-    __syncthreads();  // tb and this stage are reused by the next block
   }
+  report_bad_perm(bad, err);
 }
 
 }  // namespace
@@ -579,7 +637,7 @@ cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* 
                STATS_SMEM, s>>>(K, lk, V, lv, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax, err);
   prep_kmean<<<static_cast<unsigned>(BH), dim3(D, KM_SEG), 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp,
                                                                    o.k_mean, o.v_scale);
-  prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH)), 256,
+  prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH), 3), 256,
                QUANT_SMEM, s>>>(
       Q, lq, K, lk, V, lv, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
       o.q_scale, o.k_scale, o.qmu, o.vmu_op, err, (flags & PREP_QK_HADAMARD) != 0);
