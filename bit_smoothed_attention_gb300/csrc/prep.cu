@@ -198,7 +198,7 @@ __device__ __forceinline__ void hadamard_row32(float (&x)[32], int qq) {
 // 256, dynamic shared memory STATS_SMEM (two stages of K and V tiles).
 constexpr int STATS_BPC = 8;
 constexpr int STATS_SMEM = 2 * 2 * TILE_SMEM;
-__global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K, RowLayout lk,
+__global__ void __launch_bounds__(256, 3) prep_stats(const uint16_t* __restrict__ K, RowLayout lk,
                                                   const uint16_t* __restrict__ V, RowLayout lv,
                                                   const int32_t* __restrict__ perm, int64_t N,
                                                   int nb, int nbp, float* __restrict__ kbs,
@@ -246,8 +246,15 @@ __global__ void __launch_bounds__(256) prep_stats(const uint16_t* __restrict__ K
     block_tree(vx, vs);
     const int64_t nvalid = N - b * BLK < BLK ? N - b * BLK : BLK;
     const float fn = static_cast<float>(nvalid);
+    // x / 64 is x * 2^-6 exactly (both correctly round the same value), so
+    // full blocks multiply; only the last, partial block divides.
+    if (nvalid == BLK) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) mu[c] = vs[c] / fn;
+      for (int c = 0; c < 8; ++c) mu[c] = vs[c] * 0.015625f;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mu[c] = vs[c] / fn;
+    }
 #pragma unroll
     for (int c = 0; c < 8; ++c)
 #pragma unroll
