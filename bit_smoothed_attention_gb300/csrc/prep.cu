@@ -63,6 +63,17 @@ __device__ __forceinline__ Map thread_map() {
   m.cc = 2 * m.warp + (m.lane >> 4);     // channel chunk (8 channels)
   return m;
 }
+// The quantisers' mapping: the 16 lanes of a half-warp take the 16 channel
+// chunks of the same 4 rows, so each of their 8-byte stores of a row is one
+// contiguous 128-byte line.
+__device__ __forceinline__ Map quant_map() {
+  Map m;
+  m.warp = threadIdx.x >> 5;
+  m.lane = threadIdx.x & 31;
+  m.cc = m.lane & 15;                    // channel chunk (8 channels)
+  m.g = 2 * m.warp + (m.lane >> 4);      // token group (4 tokens)
+  return m;
+}
 
 // A block's 64 rows are staged in shared memory with cp.async (all loads in
 // flight at once): [64 rows][16 chunks of 16 bytes], the chunk index XOR-ed
@@ -386,9 +397,11 @@ __global__ void __launch_bounds__(256, 3) prep_quant(
   uint8_t (*tb)[BLK + 16] = reinterpret_cast<uint8_t (*)[BLK + 16]>(qsm + QUANT_NST * TILE_SMEM);
   float* kmu = reinterpret_cast<float*>(qsm + QUANT_NST * TILE_SMEM + D * (BLK + 16));
   float* red = kmu + D;
-  const Map m = thread_map();
-  const int64_t bh = blockIdx.y;
   const int z = blockIdx.z;  // 0 = Q, 1 = K, 2 = V
+  // V keeps the token-group lanes (its transposed bytes go to shared memory
+  // without bank conflicts); Q and K take the coalescing mapping
+  const Map m = z == 2 ? thread_map() : quant_map();
+  const int64_t bh = blockIdx.y;
   const int64_t nb = ceil_div(N, BLK);
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * QUANT_BPC;
   const int64_t b1 = b0 + QUANT_BPC < nbp ? b0 + QUANT_BPC : nbp;
