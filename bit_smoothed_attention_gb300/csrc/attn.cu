@@ -261,8 +261,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned, derived from the shared array itself so that the
+  // compiler keeps every access through it in the shared state space
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
   auto bar = [&](int i) { return sb + SM_BAR + 8u * static_cast<uint32_t>(i); };
   volatile int* abort = reinterpret_cast<volatile int*>(sm + SM_ABORT);
