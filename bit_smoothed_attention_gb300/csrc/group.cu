@@ -34,15 +34,13 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
   }
 }
 
-// Init: c_c = v[floor(c*N/k)].  grid (BH), block D.
+// Init: c_c = v[floor(c*N/k)].  grid (k, BH), block D.
 __global__ void km_init(const uint16_t* __restrict__ V, RowLayout lv, int64_t N, int k,
                         float* __restrict__ cent) {
-  const int64_t bh = blockIdx.x;
-  const int d = threadIdx.x;
-  for (int c = 0; c < k; ++c) {
-    const int64_t j = (static_cast<int64_t>(c) * N) / k;
-    cent[(bh * k + c) * D + d] = bf16f(V[lv.head(bh) + lv.row(j) + d]);
-  }
+  const int64_t bh = blockIdx.y;
+  const int c = blockIdx.x, d = threadIdx.x;
+  const int64_t j = (static_cast<int64_t>(c) * N) / k;
+  cent[(bh * k + c) * D + d] = bf16f(V[lv.head(bh) + lv.row(j) + d]);
 }
 
 // Chunk partial sums.  The chunk's tokens are first listed cluster by
@@ -247,6 +245,7 @@ size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws) {
   w.amb_count = reinterpret_cast<uint32_t*>(take(8));
   w.head_cn = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * 2 * 4));
   w.head_h = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * KMAX * 4));
+  w.vnorm = reinterpret_cast<float*>(take(static_cast<size_t>(BH) * N * 4));
   if (ws) *ws = w;
   return off;
 }
@@ -258,7 +257,7 @@ cudaError_t launch_group(const uint16_t* V, const RowLayout& lv, int64_t BH, int
   float* cent = centroids_out ? centroids_out : ws.cent;
   cudaError_t e = cudaSuccess;
   if (!init) {
-    km_init<<<static_cast<unsigned>(BH), D, 0, s>>>(V, lv, N, k, cent);
+    km_init<<<dim3(k, static_cast<unsigned>(BH)), D, 0, s>>>(V, lv, N, k, cent);
     e = cudaGetLastError();
   } else if (init != cent) {
     // warm start: the iterations begin from the given centroids

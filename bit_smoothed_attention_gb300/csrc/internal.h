@@ -81,10 +81,13 @@ struct GroupWs {
   uint32_t* amb_count; // [2]: how many, for even and odd iterations
   float* head_cn;      // [BH, 2]: max |c| and max |h| bounds of each head
   float* head_h;       // [BH, 64]: h_c of each head
+  float* vnorm;        // [BH, N]: |v| bound of each token (stored by the first iteration)
 };
 size_t group_ws_layout(int64_t BH, int64_t N, int k, void* base, GroupWs* ws);
 // Tensor-core k-means assignment with an exact FP32 fallback (km_tc.cu);
 // 1 <= k <= 64.
+// Iteration `iter` = 0 computes the tokens' |v| bounds into ws.vnorm, later
+// iterations read them.
 // tdump (test hook, nullable): [BH, N, 65] f32, the tensor-core scores T_c
 // (c < 64) and the token's filter bound E, written for every token.
 cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t BH, int64_t N, int k,

@@ -88,11 +88,12 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     km_assign_tc(const __grid_constant__ CUtensorMap tmv, int64_t N, int64_t H, int k, int tpc,
                  const float* __restrict__ cent,
                  int32_t* __restrict__ labels, KmAmb* __restrict__ amb, uint32_t* __restrict__ amb_count,
-                 float* __restrict__ head_cn, float* __restrict__ head_h, uint32_t* __restrict__ err,
-                 float* __restrict__ tdump) {
+                 float* __restrict__ head_cn, float* __restrict__ head_h, float* __restrict__ vnorm,
+                 int vnorm_ready, uint32_t* __restrict__ err, float* __restrict__ tdump) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned, derived from the shared array itself so that the
+  // compiler keeps every access through it in the shared state space
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
   auto bar = [&](int i) { return sb + SM_BAR + 8u * static_cast<uint32_t>(i); };
   volatile int* abort = reinterpret_cast<volatile int*>(sm + SM_ABORT);
@@ -246,6 +247,33 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     for (int t = 0; t < ntl; ++t) {
       const int s = t % KT_NS, b = t & 1;
       bool ok = __all_sync(FULLM, mbar_wait(bar(KB_FULL + s), (t / KT_NS) & 1, abort, KT_WAIT_NS));
+      const uint8_t* vt = sm + SM_V + s * V_STAGE;
+      const int64_t j = (tile0 + t) * 128 + r;
+      // |v|: an upper bound (the sum's relative error is far below the
+      // factor); it depends on V alone, so the first iteration stores it and
+      // the others read it back
+      float vn = 0.0f;
+      if (ok && j < N) {
+        if (vnorm_ready) {
+          vn = vnorm[bh * N + j];
+        } else {
+          float2 q2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 u = *reinterpret_cast<const uint4*>(vt + kc * V_HALF + sw128(r, 8 * ch));
+              const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 v2 = make_float2(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xFFFF0000u));
+                q2 = __ffma2_rn(v2, v2, q2);
+              }
+            }
+          vn = sqrtf(q2.x + q2.y) * 1.0000153f;
+          vnorm[bh * N + j] = vn;
+        }
+      }
       ok = ok && __all_sync(FULLM, mbar_wait(bar(KB_DFULL + b), (t >> 1) & 1, abort, KT_WAIT_NS));
       if (!ok) {
         if (lane == 0) atomicOr(err, ERR_TIMEOUT);
@@ -265,25 +293,7 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(KB_DEMPTY + b));
 
-      const uint8_t* vt = sm + SM_V + s * V_STAGE;
-      const int64_t j = (tile0 + t) * 128 + r;
       if (j < N) {
-        // |v| from the staged row (an upper bound: the sum's relative error
-        // is far below the factor)
-        float2 q2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint4 u = *reinterpret_cast<const uint4*>(vt + kc * V_HALF + sw128(r, 8 * ch));
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 v2 = make_float2(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xFFFF0000u));
-              q2 = __ffma2_rn(v2, v2, q2);
-            }
-          }
-        const float vn = sqrtf(q2.x + q2.y) * 1.0000153f;
         const float E = EA * vn + EB;
         // m = max_c T_c (eight independent chains), then the candidates
         float m8[8];
@@ -484,7 +494,7 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t 
   // before the first iteration, then by the previous fix-up).
   uint32_t* cnt = ws.amb_count + (iter & 1);
   km_assign_tc<<<grid, KT_THREADS, KT_SMEM, s>>>(m, N, lv.H, k, static_cast<int>(tpc), cent, labels, ws.amb, cnt,
-                                                 ws.head_cn, ws.head_h, err, tdump);
+                                                 ws.head_cn, ws.head_h, ws.vnorm, iter > 0 ? 1 : 0, err, tdump);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   km_fixup<<<static_cast<unsigned>(slots * 2), 128, 0, s>>>(V, lv, N, k, cent, labels, ws.amb, cnt,

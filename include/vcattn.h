@@ -109,7 +109,11 @@ int64_t vcattn_npad(int64_t N);
  *                             sorted by (label, token index)
  *   centroids f32  [B,H,k,D] out, nullable: centroids after the last update
  *   ws        device scratch of at least vcattn_group_workspace_bytes(shape, k)
- * k in [1, 64], iters >= 1.  Results are bit-for-bit deterministic. */
+ * k in [1, 64], iters >= 1.  Results are bit-for-bit deterministic.
+ * V must be finite: a token whose scores cannot be compared (a NaN or an
+ * infinity in its row or in a centroid) gets label -1 and sets the device
+ * error word (vcattn_last_device_error returns VCATTN_ERR_DEVICE); perm is
+ * then not a permutation. */
 size_t vcattn_group_workspace_bytes(const vcattn_shape* shape, int k);
 vcattn_status vcattn_group(const vcattn_shape* shape, const void* V, int k, int iters,
                            int32_t* labels, int32_t* perm, float* centroids,
