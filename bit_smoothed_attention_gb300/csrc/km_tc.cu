@@ -23,14 +23,14 @@
 // win.
 // When one cluster is left it is the label.  Otherwise (0.6% of the tokens
 // on the live workload) the token goes on a list, and km_fixup, launched
-// right after, resolves every listed token with one thread each: a second
-// filter computes the candidates' FP32 dot products in eight interleaved
-// partial sums and drops those more than E2 = 2^-15 (|v| max|c| + max|h|)
-// below the best of them (the same argument with a tighter bound); the
-// exact chains of what is left decide, lowest index first on ties.  (Done in
-// place, these few tokens held their whole warp on a chain of global loads:
-// a third of the assignment time.)  The labels are those of the FP32
-// definition, bit for bit, whatever the data.
+// right after, resolves every listed token with one warp: a second filter
+// computes the candidates' FP32 dot products (lanes over candidates and
+// channel groups) and drops those more than E2 = 2^-15 (|v| max|c| +
+// max|h|) below the best of them (the same argument with a tighter bound);
+// the exact chains of what is left decide, lowest index first on ties.
+// (Done in place, these few tokens held their whole warp on a chain of
+// global loads: a third of the assignment time.)  The labels are those of
+// the FP32 definition, bit for bit, whatever the data.
 //
 // CTA: up to KT_TPC consecutive 128-token tiles of one (b, h).  Warps 0-3:
 // one thread per token (= TMEM lane) for the selection; warp 4: TMA; warp 5:
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < KT_NS; ++s) {
       mbar_init(bar(KB_FULL + s), 1);
-      mbar_init(bar(KB_EMPTY + s), 5);  // the MMA lane's commit + the 4 selection warps
+      mbar_init(bar(KB_EMPTY + s), 5);  // the MMA lane's commit + the 4 selection warps (after |v|)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(KB_DFULL + b), 1);
@@ -274,6 +274,11 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
           vnorm[bh * N + j] = vn;
         }
       }
+      // The selection reads nothing else from the V stage: it is free once
+      // the tensor core is done with it.  (Waiting for FULL first keeps this
+      // arrival in the stage's current phase.)
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(bar(KB_EMPTY + s));
       ok = ok && __all_sync(FULLM, mbar_wait(bar(KB_DFULL + b), (t >> 1) & 1, abort, KT_WAIT_NS));
       if (!ok) {
         if (lane == 0) atomicOr(err, ERR_TIMEOUT);
@@ -325,8 +330,6 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
         }
         labels[bh * N + j] = best;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(KB_EMPTY + s));  // done reading this V stage
     }
   }
   tc_fence_before();
@@ -335,10 +338,18 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
   if (warp == KT_WARP_MMA) tmem_dealloc(tmem, 128);
 }
 
-// The assignments the tensor-core filter left open, one thread each: the
-// second filter (at most four candidates), then the exact chains.  v comes
+// The assignments the tensor-core filter left open, one warp each.  v comes
 // from the bf16 row in global memory, h_c as km_assign_tc computed it.
-__global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, RowLayout lv, int64_t N, int k,
+//  - Second filter (at most four candidates): lanes (q, g) = (lane >> 3,
+//    lane & 7) form candidate q's dot product over channels 16g .. 16g+15
+//    (an fmaf chain), then a three-level tree over g.  Against the exact
+//    chain this errs by at most (128 + 16 + 3) 2^-24 |v| |c| < 2^-16.7 |v| |c|,
+//    so E2 = 2^-15 (|v| max|c| + max|h|) is again at least twice the
+//    difference of the scores, and candidates more than E2 below the best
+//    cannot win.
+//  - If two or more are left: lane i runs the exact chain of the i-th
+//    candidate; the best score wins, the lower cluster on ties.
+__global__ void __launch_bounds__(256) km_fixup(const uint16_t* __restrict__ V, RowLayout lv, int64_t N, int k,
                                                 const float* __restrict__ cent, int32_t* __restrict__ labels,
                                                 const KmAmb* __restrict__ amb, const uint32_t* __restrict__ count,
                                                 uint32_t* __restrict__ next_count,
@@ -346,90 +357,100 @@ __global__ void __launch_bounds__(128) km_fixup(const uint16_t* __restrict__ V, 
                                                 const float* __restrict__ head_h) {
   const uint32_t n = *count;
   if (blockIdx.x == 0 && threadIdx.x == 0) *next_count = 0;  // for the next iteration's assign
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t FULLM = 0xffffffffu;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += nwarps) {
     const KmAmb a = amb[i];
     const int64_t bh = a.tok / N;
     const uint16_t* vrow = V + lv.head(bh) + lv.row(a.tok - bh * N);
     const float* cb = cent + bh * k * D;
-    const float CM = head_cn[2 * bh], HM = head_cn[2 * bh + 1];
     const float* hh = head_h + bh * 64;
     uint64_t cand = a.cand;
-    int best = __ffsll(static_cast<long long>(cand)) - 1;
     if (__popcll(cand) <= 4) {
-      // Second filter: FP32 dot products of the (at most four) candidates in
-      // eight interleaved partial sums; their error vs the chain is
-      // <= (128 + 19) 2^-24 |v| |c| < 2^-16.7 |v| |c|, so E2 = 2^-15 (|v|
-      // max|c| + max|h|) is again at least twice the difference of the scores.
-      float st[4];
-      int cl[4];
-      float m2 = -__int_as_float(0x7f800000);
+      const int q = lane >> 3, g = lane & 7;
+      // the q-th candidate (or none)
       uint64_t rest = cand;
+      for (int x = 0; x < q && rest; ++x) rest &= rest - 1;
+      const int cl = rest ? __ffsll(static_cast<long long>(rest)) - 1 : -1;
+      float part = 0.0f;
+      if (cl >= 0) {
+        const uint4 u0 = *reinterpret_cast<const uint4*>(vrow + 16 * g);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(vrow + 16 * g + 8);
+        const float4* c4 = reinterpret_cast<const float4*>(cb + cl * D + 16 * g);
+        const float4 c0 = c4[0], c1 = c4[1], c2 = c4[2], c3 = c4[3];
+        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        const float cc[16] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w,
+                              c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        cl[q] = rest ? __ffsll(static_cast<long long>(rest)) - 1 : -1;
-        rest = rest ? rest & (rest - 1) : 0;
-        st[q] = -__int_as_float(0x7f800000);
-        if (cl[q] >= 0) {
-          float a8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-          const float* crow = cb + cl[q] * D;
+        for (int e = 0; e < 8; ++e) {
+          part = __fmaf_rn(__uint_as_float(w[e] << 16), cc[2 * e], part);
+          part = __fmaf_rn(__uint_as_float(w[e] & 0xFFFF0000u), cc[2 * e + 1], part);
+        }
+      }
+#pragma unroll
+      for (int m = 4; m >= 1; m >>= 1) part = part + __shfl_xor_sync(FULLM, part, m);
+      const float st = cl >= 0 ? part - hh[cl] : -__int_as_float(0x7f800000);
+      float m2 = st;
+      m2 = fmaxf(m2, __shfl_xor_sync(FULLM, m2, 8));
+      m2 = fmaxf(m2, __shfl_xor_sync(FULLM, m2, 16));
+      const float thr2 = m2 - 3.0517578125e-5f * (a.vn * head_cn[2 * bh] + head_cn[2 * bh + 1]);
+      const bool keep = g == 0 && cl >= 0 && st >= thr2;
+      uint64_t c2 = 0;
+      const uint32_t kb = __ballot_sync(FULLM, keep);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        if ((kb >> (8 * qq)) & 1u) c2 |= 1ull << __shfl_sync(FULLM, cl, 8 * qq);
+      cand = c2;
+    }
+    int best = __ffsll(static_cast<long long>(cand)) - 1;
+    if (cand & (cand - 1)) {
+      // exact chains: lane l takes the l-th, (l+32)-th, ... candidate
+      float bs = -__int_as_float(0x7f800000);
+      int bc = 64;
+      uint64_t rest = cand;
+      while (rest) {
+        uint64_t mine = rest;
+        for (int x = 0; x < lane && mine; ++x) mine &= mine - 1;
+        if (mine) {
+          const int c = __ffsll(static_cast<long long>(mine)) - 1;
+          const float* crow = cb + c * D;
+          float acc = 0.0f;
 #pragma unroll 4
-          for (int ch = 0; ch < 16; ++ch) {
+          for (int ch = 0; ch < 16; ++ch) {  // d = 8 ch .. 8 ch + 7, in order
             const uint4 u = *reinterpret_cast<const uint4*>(vrow + 8 * ch);
             const float4 c0 = *reinterpret_cast<const float4*>(crow + 8 * ch);
             const float4 c1 = *reinterpret_cast<const float4*>(crow + 8 * ch + 4);
-            a8[0] = __fmaf_rn(__uint_as_float(u.x << 16), c0.x, a8[0]);
-            a8[1] = __fmaf_rn(__uint_as_float(u.x & 0xFFFF0000u), c0.y, a8[1]);
-            a8[2] = __fmaf_rn(__uint_as_float(u.y << 16), c0.z, a8[2]);
-            a8[3] = __fmaf_rn(__uint_as_float(u.y & 0xFFFF0000u), c0.w, a8[3]);
-            a8[4] = __fmaf_rn(__uint_as_float(u.z << 16), c1.x, a8[4]);
-            a8[5] = __fmaf_rn(__uint_as_float(u.z & 0xFFFF0000u), c1.y, a8[5]);
-            a8[6] = __fmaf_rn(__uint_as_float(u.w << 16), c1.z, a8[6]);
-            a8[7] = __fmaf_rn(__uint_as_float(u.w & 0xFFFF0000u), c1.w, a8[7]);
+            acc = __fmaf_rn(__uint_as_float(u.x << 16), c0.x, acc);
+            acc = __fmaf_rn(__uint_as_float(u.x & 0xFFFF0000u), c0.y, acc);
+            acc = __fmaf_rn(__uint_as_float(u.y << 16), c0.z, acc);
+            acc = __fmaf_rn(__uint_as_float(u.y & 0xFFFF0000u), c0.w, acc);
+            acc = __fmaf_rn(__uint_as_float(u.z << 16), c1.x, acc);
+            acc = __fmaf_rn(__uint_as_float(u.z & 0xFFFF0000u), c1.y, acc);
+            acc = __fmaf_rn(__uint_as_float(u.w << 16), c1.z, acc);
+            acc = __fmaf_rn(__uint_as_float(u.w & 0xFFFF0000u), c1.w, acc);
           }
-          st[q] = (((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]))) - hh[cl[q]];
-          m2 = fmaxf(m2, st[q]);
+          const float e = acc - hh[c];
+          if (e > bs || (e == bs && c < bc)) {
+            bs = e;
+            bc = c;
+          }
         }
+        for (int x = 0; x < 32 && rest; ++x) rest &= rest - 1;
       }
-      const float thr2 = m2 - 3.0517578125e-5f * (a.vn * CM + HM);
-      uint64_t c2 = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (cl[q] >= 0 && st[q] >= thr2) c2 |= 1ull << cl[q];
-      cand = c2;
-      best = __ffsll(static_cast<long long>(cand)) - 1;
-    }
-    if (cand & (cand - 1)) {
-      // exact chains of the candidates in ascending cluster order; the
-      // lowest index is kept on ties
-      float bs = 0.0f;
-      bool have = false;
-      for (uint64_t rest = cand; rest; rest &= rest - 1) {
-        const int c = __ffsll(static_cast<long long>(rest)) - 1;
-        const float* crow = cb + c * D;
-        float acc = 0.0f;
-#pragma unroll 4
-        for (int ch = 0; ch < 16; ++ch) {  // d = 8 ch .. 8 ch + 7, in order
-          const uint4 u = *reinterpret_cast<const uint4*>(vrow + 8 * ch);
-          const float4 c0 = *reinterpret_cast<const float4*>(crow + 8 * ch);
-          const float4 c1 = *reinterpret_cast<const float4*>(crow + 8 * ch + 4);
-          acc = __fmaf_rn(__uint_as_float(u.x << 16), c0.x, acc);
-          acc = __fmaf_rn(__uint_as_float(u.x & 0xFFFF0000u), c0.y, acc);
-          acc = __fmaf_rn(__uint_as_float(u.y << 16), c0.z, acc);
-          acc = __fmaf_rn(__uint_as_float(u.y & 0xFFFF0000u), c0.w, acc);
-          acc = __fmaf_rn(__uint_as_float(u.z << 16), c1.x, acc);
-          acc = __fmaf_rn(__uint_as_float(u.z & 0xFFFF0000u), c1.y, acc);
-          acc = __fmaf_rn(__uint_as_float(u.w << 16), c1.z, acc);
-          acc = __fmaf_rn(__uint_as_float(u.w & 0xFFFF0000u), c1.w, acc);
-        }
-        const float e = acc - hh[c];
-        if (!have || e > bs) {
-          bs = e;
-          best = c;
-          have = true;
+      for (int m = 16; m >= 1; m >>= 1) {
+        const float os = __shfl_xor_sync(FULLM, bs, m);
+        const int oc = __shfl_xor_sync(FULLM, bc, m);
+        if (os > bs || (os == bs && oc < bc)) {
+          bs = os;
+          bc = oc;
         }
       }
+      // (bc = 64 only if every score is NaN: the first candidate then)
+      best = bc < 64 ? bc : best;
     }
-    labels[a.tok] = best;
+    if (lane == 0) labels[a.tok] = best;
   }
 }
 
@@ -497,7 +518,7 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t 
                                                  ws.head_cn, ws.head_h, ws.vnorm, iter > 0 ? 1 : 0, err, tdump);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  km_fixup<<<static_cast<unsigned>(slots * 2), 128, 0, s>>>(V, lv, N, k, cent, labels, ws.amb, cnt,
+  km_fixup<<<static_cast<unsigned>(slots * 2), 256, 0, s>>>(V, lv, N, k, cent, labels, ws.amb, cnt,
                                                             ws.amb_count + ((iter + 1) & 1), ws.head_cn,
                                                             ws.head_h);
   return cudaGetLastError();
