@@ -32,7 +32,7 @@
 // global loads: a third of the assignment time.)  The labels are those of
 // the FP32 definition, bit for bit, whatever the data.
 //
-// CTA: up to KT_TPC consecutive 128-token tiles of one (b, h).  Warps 0-3:
+// CTA: a run of consecutive 128-token tiles of one (b, h).  Warps 0-3:
 // one thread per token (= TMEM lane) for the selection; warp 4: TMA; warp 5:
 // MMA lane.  V tiles (bf16, two 64-channel K chunks, 128B swizzle) through a
 // ring of KT_NS stages; the scores T in two TMEM buffers of 64 columns.
@@ -119,19 +119,22 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     *abort = 0;
     mbar_fence_init();
   }
-  // The FP32 centroids, staged in V stage 0 (not yet in use) with 16-byte
-  // loads, all in flight at once.
+  // The FP32 centroids, staged in the V stages (not yet in use) with
+  // 16-byte loads, all in flight at once; rows CS floats apart, so that the
+  // h_c chains below (thread c reads row c) spread over the banks.
+  constexpr int CS = D + 4;
+  static_assert(64 * CS * 4 <= KT_NS * V_STAGE, "centroid staging");
   float* cs = reinterpret_cast<float*>(sm + SM_V);
   for (int i = threadIdx.x; i < 64 * D / 4; i += KT_THREADS) {
     const int c = i >> 5;
-    *reinterpret_cast<float4*>(cs + 4 * i) =
+    *reinterpret_cast<float4*>(cs + c * CS + 4 * (i & 31)) =
         c < k ? *reinterpret_cast<const float4*>(cb + 4 * i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   }
   __syncthreads();
   // B operand: the centroids as bf16 high and low parts (clusters >= k are 0)
   for (int i = threadIdx.x; i < 64 * D; i += KT_THREADS) {
     const int c = i >> 7, d = i & (D - 1);
-    const float x = cs[i];
+    const float x = cs[c * CS + d];
     const __nv_bfloat16 hi = __float2bfloat16_rn(x);
     const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
     const int kc = d >> 6, e = d & 63;
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     float acc = 0.0f;
     if (c < k)
 #pragma unroll 16
-      for (int d = 0; d < D; ++d) acc = __fmaf_rn(cs[c * D + d], cs[c * D + d], acc);
+      for (int d = 0; d < D; ++d) acc = __fmaf_rn(cs[c * CS + d], cs[c * CS + d], acc);
     const float h = 0.5f * acc;
     hs[c] = h;
     // B of the bias step: -h in three bf16 parts; clusters >= k get -inf
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
   }
   fence_proxy_async_smem();
   if (warp == KT_WARP_MMA) tmem_alloc(sb + SM_TSLOT, 128);
-  // (V stage 0 is overwritten by TMA only after this barrier)
+  // (the V stages are overwritten by TMA only after this barrier)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -503,13 +506,20 @@ cudaError_t launch_km_assign_tc(const uint16_t* V, const RowLayout& lv, int64_t 
     return e;
   });
   if (est != cudaSuccess) return est;
-  // Tiles per CTA: at most 16 (the per-CTA set-up is amortised over them),
-  // chosen so that the CTAs fill whole waves of two CTAs per SM.
+  // Tiles per CTA (all of one head): the count that minimises the waves of
+  // two CTAs per SM times the tiles of a CTA plus its set-up (about six
+  // tiles' worth: the centroid operands and the h_c chains).
   const int slots = setup.value[dev];
   const int64_t ntile = (N + 127) / 128;
-  const int64_t total = ntile * BH;
-  const int64_t waves = (total + 16 * slots - 1) / (16 * slots);
-  const int64_t tpc = (total + slots * waves - 1) / (slots * waves);
+  int64_t tpc = 1, best_cost = -1;
+  for (int64_t c = 1; c <= ntile; ++c) {
+    const int64_t waves = ceil_div(BH * ceil_div(ntile, c), slots);
+    const int64_t cost = waves * (c + 6);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      tpc = c;
+    }
+  }
   const dim3 grid(static_cast<unsigned>((ntile + tpc - 1) / tpc), static_cast<unsigned>(BH));
   // The open-assignment counter of this iteration starts at 0 (cleared
   // before the first iteration, then by the previous fix-up).
