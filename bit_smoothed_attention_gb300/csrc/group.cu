@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
   // sums: clusters 4 cg .. 4 cg + 3, channels 8 q .. 8 q + 7
   const int cg = tid >> 4, q = tid & 15;
   const uint16_t* vb = V + lv.head(bh) + lv.row(j0) + 8 * q;
-  float* pg = part + (bh * nchunk + g) * static_cast<int64_t>(k) * D;
+  // partials [BH, k, nchunk, D]: a cluster's chunks side by side
+  float* pg = part + (bh * k * static_cast<int64_t>(nchunk) + g) * D;
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
     const int c = 4 * cg + cc;
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
         acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(w4[e] & 0xFFFF0000u);
       }
     }
-    float* dst = pg + c * D + 8 * q;
+    float* dst = pg + static_cast<int64_t>(c) * nchunk * D + 8 * q;
     *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     if (q == 0) cnt[(bh * nchunk + g) * k + c] = i1 - cstart[c];
@@ -160,10 +161,10 @@ __global__ void __launch_bounds__(D) km_finalize(const float* __restrict__ part,
   const int d = threadIdx.x;
   float total = 0.0f;
   int count = 0;
+  const float* pc = part + (bh * k + c) * static_cast<int64_t>(nchunk) * D + d;
   for (int g = 0; g < nchunk; ++g) {
-    const int64_t o = (bh * nchunk + g) * k + c;
-    total = total + part[o * D + d];
-    count += cnt[o];
+    total = total + pc[static_cast<int64_t>(g) * D];
+    count += cnt[(bh * nchunk + g) * k + c];
   }
   if (count > 0) cent[(bh * k + c) * D + d] = total / static_cast<float>(count);
 }

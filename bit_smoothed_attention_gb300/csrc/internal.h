@@ -74,7 +74,7 @@ struct KmAmb {
 };
 struct GroupWs {
   float* cent;         // [BH, k, D]
-  float* part;         // [BH, nchunk, k, D]
+  float* part;         // [BH, k, nchunk, D]
   int32_t* cnt;        // [BH, nchunk, k]
   int32_t* offs;       // [BH, nchunk, k]
   KmAmb* amb;          // [BH * N] open assignments of one iteration

@@ -247,6 +247,10 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
     const float EB = (1.220703125e-4f + 4.76837158e-7f) * HM;
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t FULLM = 0xffffffffu;
+    // |v| of this thread's token in the next tile, loaded a tile ahead (once
+    // the first iteration has stored them)
+    float vn_next = 0.0f;
+    if (vnorm_ready && tile0 * 128 + r < N) vn_next = vnorm[bh * N + tile0 * 128 + r];
     for (int t = 0; t < ntl; ++t) {
       const int s = t % KT_NS, b = t & 1;
       bool ok = __all_sync(FULLM, mbar_wait(bar(KB_FULL + s), (t / KT_NS) & 1, abort, KT_WAIT_NS));
@@ -255,11 +259,10 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
       // |v|: an upper bound (the sum's relative error is far below the
       // factor); it depends on V alone, so the first iteration stores it and
       // the others read it back
-      float vn = 0.0f;
+      float vn = vn_next;
+      if (vnorm_ready && t + 1 < ntl && j + 128 < N) vn_next = vnorm[bh * N + j + 128];  // the next tile's
       if (ok && j < N) {
-        if (vnorm_ready) {
-          vn = vnorm[bh * N + j];
-        } else {
+        if (!vnorm_ready) {
           float2 q2 = make_float2(0.0f, 0.0f);
 #pragma unroll
           for (int kc = 0; kc < 2; ++kc)
