@@ -93,6 +93,45 @@ def test_group_degenerate_inputs(vc, orc):
         assert np.array_equal(labels.reshape(1, 300).cpu().numpy(), ol)
 
 
+def test_group_all_clusters_tied(vc, orc):
+    """The seeds are 64 sign patterns of one bf16 vector u, so every h_c is
+    the same float (the squares come in the same order), and a third of the
+    tokens are zero: their 64 scores are one value, every cluster stays a
+    candidate through both filters (two rounds of exact chains), and the
+    lowest index must win.  Other tokens are small multiples of the seeds
+    and random rows.  Bit-exact after one and two iterations."""
+    H, N, k = 2, 4096, 64
+    g = torch.Generator(device="cpu")
+    g.manual_seed(777)
+    V = (torch.randn(1, H, N, 128, generator=g) * 0.5).to(torch.bfloat16)
+    u = (torch.rand(128, generator=g) + 0.5).to(torch.bfloat16)
+    sign = torch.randint(0, 2, (k, 128), generator=g).to(torch.bool)
+    seeds = [(c * N) // k for c in range(k)]
+    zero = torch.rand(N, generator=g) < 0.33
+    for h in range(H):
+        V[0, h, zero] = 0.0
+        for c, j in enumerate(seeds):
+            V[0, h, j] = torch.where(sign[c], -u, u)
+        for c, j in enumerate(seeds):       # a few scaled copies next to each seed
+            if j + 1 < N and (j + 1) not in seeds:
+                V[0, h, j + 1] = (torch.where(sign[c], -u, u).float() * 0.5).to(torch.bfloat16)
+    V = V.cuda()
+    for iters in (1, 2):
+        labels, perm, cent = vc.group(V, k, iters, centroids=True)
+        torch.cuda.synchronize()
+        ol, oc = orc.kmeans(_bits(V), k, iters)
+        op = orc.stable_sort(ol, k)
+        assert np.array_equal(labels.reshape(H, N).cpu().numpy(), ol)
+        assert np.array_equal(cent.reshape(H, k, 128).cpu().numpy().view(np.uint32), oc.view(np.uint32))
+        assert np.array_equal(perm.reshape(H, N).cpu().numpy(), op)
+        if iters == 1:   # the zero tokens all went to cluster 0
+            z = zero.numpy().copy()
+            z[seeds] = False
+            z[[j + 1 for j in seeds if j + 1 < N]] = False
+            assert z.sum() > 1000 and np.all(ol[:, z] == 0)
+    assert vc.last_device_error() == 0
+
+
 def test_group_near_ties(vc, orc):
     """Pairs of initial centroids one bf16 ulp apart in one channel, and
     tokens repeated from them: most scores of the first iterations differ in
