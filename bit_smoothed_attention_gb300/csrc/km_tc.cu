@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
 
   if (warp == KT_WARP_TMA) {
     if (lane == 0) {
+      int issued = 0;
       for (int t = 0; t < ntl && !*abort; ++t) {
         const int s = t % KT_NS;
         if (t >= KT_NS && !mbar_wait(bar(KB_EMPTY + s), ((t / KT_NS) - 1) & 1, abort, KT_WAIT_NS)) {
@@ -198,7 +199,13 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
         const int hh = static_cast<int>(bh % H), bb = static_cast<int>(bh / H);
         tma_load_4d(sb + SM_V + s * V_STAGE, &tmv, 0, row, hh, bb, bar(KB_FULL + s));
         tma_load_4d(sb + SM_V + s * V_STAGE + V_HALF, &tmv, 64, row, hh, bb, bar(KB_FULL + s));
+        issued = t + 1;
       }
+      // Copies still in flight land before the CTA exits (possible only after
+      // an abort; otherwise the consumers have waited for every one).  The
+      // wait is bounded by time alone.
+      for (int t = issued > KT_NS ? issued - KT_NS : 0; t < issued; ++t)
+        if (!mbar_wait_time(bar(KB_FULL + t % KT_NS), (t / KT_NS) & 1, KT_WAIT_NS)) atomicOr(err, ERR_TIMEOUT);
     }
   } else if (warp == KT_WARP_MMA) {
     if (lane == 0) {
@@ -228,8 +235,10 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
         *abort = 1;
         atomicOr(err, ERR_TIMEOUT);
       }
+      // every MMA of this lane completes before TMEM is released, also after
+      // an abort (the wait ignores the abort flag)
       mma_commit(bar(KB_FIN));
-      if (!mbar_wait(bar(KB_FIN), 0, abort, KT_WAIT_NS) && !*abort) atomicOr(err, ERR_TIMEOUT);
+      if (!mbar_wait_time(bar(KB_FIN), 0, KT_WAIT_NS)) atomicOr(err, ERR_TIMEOUT);
     }
   } else {
     // ---------------------------------------------------- selection warps
