@@ -178,25 +178,42 @@ __device__ __forceinline__ float2 block_max2(float a, float b, float* red) {
 // The 128-point Hadamard butterfly of one row held by four consecutive lanes,
 // 32 channels each (lane & 3 = qq holds channels 32 qq ..): stages
 // h = 1, 2, ..., 64 in that order, each pair (x[i], x[i + h]) with i & h == 0
-// becoming (x[i] + x[i + h], x[i] - x[i + h]) in FP32.
+// becoming (x[i] + x[i + h], x[i] - x[i + h]) in FP32.  From h = 2 on, two
+// neighbouring pairs go through one packed f32x2 instruction each, and the
+// difference is fma(x[i + h], -1, x[i]): one rounding of the same exact
+// value.  In the two cross-lane stages the lane holding the upper half takes
+// fma(own, -1, partner) = partner - own, the other fma(own, 1, partner).
 __device__ __forceinline__ void hadamard_row32(float (&x)[32], int qq) {
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1)
+  for (int i = 0; i < 32; i += 2) {  // h = 1
+    const float a = x[i], c = x[i + 1];
+    x[i] = a + c;
+    x[i + 1] = a - c;
+  }
+  const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+  for (int h = 2; h < 32; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; i += 2)
       if ((i & h) == 0) {
-        const float a = x[i], c = x[i + h];
-        x[i] = a + c;
-        x[i + h] = a - c;
+        const float2 a = make_float2(x[i], x[i + 1]), c = make_float2(x[i + h], x[i + h + 1]);
+        const float2 sum = __fadd2_rn(a, c), dif = __ffma2_rn(c, m1, a);
+        x[i] = sum.x;
+        x[i + 1] = sum.y;
+        x[i + h] = dif.x;
+        x[i + h + 1] = dif.y;
       }
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const int lm = 1 << s;             // h = 32 (lane ^ 1), then h = 64 (lane ^ 2)
-    const bool hi = (qq & lm) != 0;
+    const float sg = (qq & lm) != 0 ? -1.0f : 1.0f;
+    const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, x[i], lm);
-      x[i] = hi ? o - x[i] : x[i] + o;
+    for (int i = 0; i < 32; i += 2) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[i], lm), __shfl_xor_sync(0xffffffffu, x[i + 1], lm));
+      const float2 r = __ffma2_rn(make_float2(x[i], x[i + 1]), sg2, o);
+      x[i] = r.x;
+      x[i + 1] = r.y;
     }
   }
 }
