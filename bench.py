@@ -430,9 +430,10 @@ def run_reference(args):
 
 
 def profile_case(workload):
-    """One grouping, one preprocessing and two attention calls on `workload`,
-    untimed: the launch sequence the committed ncu summaries capture
-    (``-k regex:<kernel> -s <n> -c <m>``)."""
+    """One grouping, one preprocessing and two attention calls on `workload`
+    (with the bench's tile mask if it is block-sparse), untimed: the launch
+    sequence the committed ncu summaries capture (``-k regex:<kernel> -s <n>
+    -c <m>``)."""
     from bit_smoothed_attention_gb300 import build, vcattn
     build.build()
     w = W.WORKLOADS[workload]
@@ -441,8 +442,10 @@ def profile_case(workload):
     pp = vcattn.prep(Q, K, V, perm)
     pp = vcattn.prep(Q, K, V, perm, out=pp)
     sm = float(np.float32(w.sm_scale))
-    O, L = vcattn.attn(pp, sm)
-    vcattn.attn(pp, sm, O=O, lse2=L)
+    # the bench's mask for a block-sparse workload
+    mask = W.make_tile_mask(w.B, w.H, w.N, w.seed + 7).to(Q.device) if w.sparse else None
+    O, L = vcattn.attn(pp, sm, mask=mask)
+    vcattn.attn(pp, sm, mask=mask, O=O, lse2=L)
     torch.cuda.synchronize()
     st = vcattn.last_device_error()
     if st != 0:

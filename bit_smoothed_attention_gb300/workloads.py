@@ -53,6 +53,9 @@ WORKLOADS = {
     "live_h8": Workload("live_h8", 1, 8, 32626, 64, 64, seed=1002),
     "schedule": Workload("schedule", 1, 40, 32760, 64, 64, steps=50, seed=1003),
     "sparse": Workload("sparse", 1, 56, 115328, 64, 64, sparse=True, seed=1004),
+    # 4 of the sparse workload's heads: the size the masked kernel's profile
+    # is captured at
+    "sparse_h4": Workload("sparse_h4", 1, 4, 115328, 64, 64, sparse=True, seed=1004),
 }
 
 
