@@ -312,9 +312,10 @@ vcattn_status vcattn_test_attn_stalled(const vcattn_shape* s, const vcattn_prepp
 }
 
 vcattn_status vcattn_test_attn_stalled_after(const vcattn_shape* s, const vcattn_prepped* in, float sm_scale,
-                                             int steps, void* O, float* lse2, void* stream) {
+                                             const uint8_t* tile_mask, int steps, void* O, float* lse2,
+                                             void* stream) {
   if (steps < 1 || steps > (1 << 20)) return VCATTN_ERR_INVALID_ARG;
-  return attn_impl(s, in, sm_scale, 8, 6.0f, 0, nullptr, O, nullptr, lse2, stream, steps << 8);
+  return attn_impl(s, in, sm_scale, 8, 6.0f, 0, tile_mask, O, nullptr, lse2, stream, steps << 8);
 }
 
 vcattn_status vcattn_test_km_scores(const vcattn_shape* s, const void* V, int k, const float* centroids,

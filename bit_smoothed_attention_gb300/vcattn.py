@@ -137,6 +137,14 @@ def _req(x, dtype, name):
         raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
 
 
+def _req_mask(mask, B, H, N):
+    """A tile mask is u8 [B, H, ceil(N/64), Npad/64] on the GPU, contiguous."""
+    _req(mask, torch.uint8, "mask")
+    want = (int(B), int(H), (int(N) + 63) // 64, npad(int(N)) // 64)
+    if tuple(mask.shape) != want:
+        raise ValueError("mask must have shape %s, got %s" % (want, tuple(mask.shape)))
+
+
 def _rows(x, dtype, name):
     """None for a contiguous [B,H,N,128] tensor, else its Strides (channels
     contiguous, e.g. a (B,N,H,D) tensor viewed as (B,H,N,D) by transpose(1, 2))."""
@@ -272,7 +280,7 @@ def attn(pp, sm_scale, mask=None, off=8, tau8=6.0, out_f32=False, O=None, lse2=N
     if lse2 is None and want_lse:
         lse2 = torch.empty(B, H, N, dtype=torch.float32, device=dev)
     if mask is not None:
-        _req(mask, torch.uint8, "mask")
+        _req_mask(mask, B, H, N)
     so = _rows(O, torch.float32 if out_f32 else torch.bfloat16, "O")
     if so is None:
         _check(_lib().vcattn_attn_ex(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale),
@@ -293,11 +301,11 @@ def fwd(Q, K, V, perm, sm_scale, mask=None, O=None, lse2=None, ws=None, stream=N
         _req(t, torch.bfloat16, n)
     if perm is not None:
         _req(perm, torch.int32, "perm")
-    if mask is not None:
-        _req(mask, torch.uint8, "mask")
     if O is not None:
         _req(O, torch.bfloat16, "O")
     s = _shape(Q)
+    if mask is not None:
+        _req_mask(mask, s.B, s.H, s.N)
     nbytes = _lib().vcattn_fwd_workspace_bytes(ctypes.byref(s))
     if ws is None:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
@@ -342,7 +350,7 @@ class HostPipeline:
         if hO is None:
             hO = torch.empty(hQ.shape, dtype=torch.bfloat16, pin_memory=True)
         if mask is not None:
-            _req(mask, torch.uint8, "mask")
+            _req_mask(mask, self.shape.B, self.shape.H, self.shape.N)
         # the compute streams start after the caller's pending work
         for s in self.streams[:2]:
             s.wait_stream(torch.cuda.current_stream(self.device))
@@ -377,19 +385,23 @@ def test_attn_stalled(pp, sm_scale, stream=None):
     return O, lse2
 
 
-def test_attn_stalled_after(pp, sm_scale, steps, stream=None):
+def test_attn_stalled_after(pp, sm_scale, steps, mask=None, stream=None):
     """Failure-path test hook: the K/V loader stops after `steps` KV tiles, so
     the kernel gives up with copies and MMAs already issued and must drain
-    them before it exits; last_device_error() then reports ERR_TIMEOUT."""
+    them before it exits; last_device_error() then reports ERR_TIMEOUT.
+    `mask` (u8 [B,H,ceil(N/64),Npad/64], as for attn) selects the block-sparse
+    kernel."""
     B, H, N = pp.shape.B, pp.shape.H, pp.shape.N
+    if mask is not None:
+        _req_mask(mask, B, H, N)
     O = torch.empty(B, H, N, 128, dtype=torch.bfloat16, device=pp.buf.device)
     lse2 = torch.empty(B, H, N, dtype=torch.float32, device=pp.buf.device)
     f = _lib().vcattn_test_attn_stalled_after
     f.restype = ctypes.c_int
-    f.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(PreppedStruct), ctypes.c_float, ctypes.c_int,
-                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
-    _check(f(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale), int(steps), _ptr(O), _ptr(lse2),
-             _stream(stream)), "vcattn_test_attn_stalled_after")
+    f.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(PreppedStruct), ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    _check(f(ctypes.byref(pp.shape), ctypes.byref(pp.struct), float(sm_scale), _ptr(mask), int(steps), _ptr(O),
+             _ptr(lse2), _stream(stream)), "vcattn_test_attn_stalled_after")
     return O, lse2
 
 

@@ -322,9 +322,12 @@ vcattn_status vcattn_test_attn_stalled(const vcattn_shape* shape, const vcattn_p
  * the method): as vcattn_test_attn_stalled, but the K/V loader stops after
  * `steps` (>= 1) KV tiles, so the consumers give up part-way with loads and
  * MMAs already issued; the kernel drains what it issued before it exits and
- * records VCATTN_ERR_TIMEOUT. */
+ * records VCATTN_ERR_TIMEOUT.  tile_mask as for vcattn_attn (NULL: dense;
+ * otherwise the block-sparse kernel, whose loaders walk each slot's own
+ * tiles). */
 vcattn_status vcattn_test_attn_stalled_after(const vcattn_shape* shape, const vcattn_prepped* in,
-                                             float sm_scale, int steps, void* O, float* lse2, void* stream);
+                                             float sm_scale, const uint8_t* tile_mask, int steps, void* O,
+                                             float* lse2, void* stream);
 /* Test hook for the k-means assignment's tensor-core filter (not part of the
  * method): one assign step of vcattn_group from the given centroids, with
  * the filter's inputs written out.  The tensor core computes an

@@ -196,4 +196,4 @@ def test_test_hooks_validation_without_gpu(lib):
     from bit_smoothed_attention_gb300.vcattn import PreppedStruct
     pp = PreppedStruct()
     s = _shape()
-    assert g(ctypes.byref(s), ctypes.byref(pp), ctypes.c_float(0.1), 0, fake, None, None) == 1
+    assert g(ctypes.byref(s), ctypes.byref(pp), ctypes.c_float(0.1), None, 0, fake, None, None) == 1
