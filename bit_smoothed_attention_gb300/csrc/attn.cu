@@ -848,6 +848,549 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == WARP_MMA) tmem_dealloc(tmem, 512);
 }
 
+// ------------------------------------------------------------- block-sparse
+// With a tile mask: one 128-row slot per CTA, its two query 64-tiles A (rows
+// 0-63) and B (rows 64-127) each walking their own KV steps (the blocks they
+// keep, two per step, in ascending order).  Step t of the slot is A's step t
+// and B's step t at once, as one block-diagonal 256-key step:
+//   S = Q8 [K_a0; K_a1; K_b0; K_b1]^T (N = 256): A's rows read columns
+//       0-127 (their own two blocks), B's rows columns 128-255;
+//   [O | l] += [P_A 0; 0 P_B] [R8_a0; R8_a1; R8_b0; R8_b1 | indicators]
+//       (K = 256, N = 144): P's off-diagonal quadrants stay zero, so each
+//       row accumulates only its own blocks, and the indicator rows give the
+//       row sums of the four blocks (A's in columns 128-129 of O, B's in
+//       130-131);
+//   two tf32 mean MMAs restore A's and B's block means.
+// Once one tile has no steps left, the other goes on alone: the finished
+// tile's blocks are replaced by a block of the step that is present (finite
+// bytes) and its rows cast nothing.  An odd last step has an empty second
+// block, filled the same way.  The arithmetic of each row is that of its own
+// query tile's steps, as in the two-slot kernel; the tensor cores do no work
+// for another tile's rows beyond the zero quadrants of P.
+//
+// Warp 0 issues the MMAs from one lane and allocates TMEM (512 columns: S
+// [0,256), O [256,400)); warp 1 issues the TMA loads through two stages
+// (stage j: V(j), its mean tiles and K(j+1), on one barrier); warps 4-7 run
+// the softmax, thread = row = TMEM lane.  The single S buffer is taken by
+// the next QK as soon as the softmax holds S in registers.
+namespace sp {
+constexpr int NTHREADS = 256;
+constexpr int WARP_MMA = 0, WARP_TMA = 1, WARP_SOFTMAX = 4;
+constexpr int NS = 2;
+constexpr uint32_t COL_S = 0;
+constexpr uint32_t COL_O = 256;
+constexpr uint32_t KBOX = 8192;              // 64 keys x 128 channels, 128B swizzle
+constexpr uint32_t K_STAGE = 4 * KBOX;
+constexpr uint32_t V_HALF = 9216;            // 144 x 64 keys, 64B swizzle (rows 128-143: indicators)
+constexpr uint32_t V_STAGE = 4 * V_HALF;
+constexpr uint32_t MU_HALF = 2048;           // mean operand of one block
+constexpr uint32_t MU_STAGE = 4 * MU_HALF;
+constexpr uint32_t L_BYTES = 4096;           // tf32 A operand of one mean MMA
+constexpr uint32_t SM_Q = 0;
+constexpr uint32_t SM_K = SM_Q + TILE_BYTES;
+constexpr uint32_t SM_V = SM_K + NS * K_STAGE;
+constexpr uint32_t SM_MU = SM_V + NS * V_STAGE;
+constexpr uint32_t SM_L = SM_MU + NS * MU_STAGE;
+constexpr uint32_t SM_P = SM_L + 2 * L_BYTES;      // P tile 0 (keys of A), P tile 1 (keys of B)
+constexpr uint32_t SM_KEPT = SM_P + 2 * TILE_BYTES;
+constexpr uint32_t SM_BAR = SM_KEPT + 2 * 4 * KEPT_WORDS;
+enum {
+  B_QFULL = 0,
+  B_FULL,
+  B_KEMPTY = B_FULL + NS,
+  B_VEMPTY = B_KEMPTY + NS,
+  B_SFULL = B_VEMPTY + NS,
+  B_STAKEN,
+  B_PFULL,
+  B_ODONE,
+  B_MDONE,
+  B_FIN,
+  NBAR
+};
+constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
+constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
+constexpr uint32_t SMEM_BYTES = SM_ABORT + 8 + 1024;  // slack for 1024-byte alignment
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(SM_K % 1024 == 0 && SM_V % 1024 == 0 && SM_P % 1024 == 0, "swizzle atoms");
+constexpr uint32_t IDESC_QK = idesc(FMT_E4M3, FMT_E4M3, 128, 256);
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_sparse(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(sm);
+  auto bar = [&](int i) { return sb + SM_BAR + 8u * static_cast<uint32_t>(i); };
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + SM_ABORT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t bh = blockIdx.y;
+  const int q0 = blockIdx.x * TILE;
+  const int qt0 = q0 / BLK;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
+    }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_STAKEN), 4);
+    mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_MDONE), 1);
+    mbar_init(bar(B_FIN), 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  // Indicator rows 128..143 of each 64-key quarter of a V stage: row 128 + h
+  // is 1.0 on quarter h's keys (64B swizzle; the rows are uniform, so the
+  // swizzle does not move them).
+  const uint32_t one4 = 0x38383838u;  // four E4M3 1.0 bytes
+  for (int c = threadIdx.x; c < NS * 4 * 16 * 4; c += NTHREADS) {
+    const int st = c >> 8, h = (c >> 6) & 3, n = (c >> 2) & 15, k = c & 3;  // stage, quarter, row, chunk
+    const uint32_t v = n == h ? one4 : 0u;
+    *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + h * V_HALF + 8192 + n * 64 + k * 16) =
+        make_uint4(v, v, v, v);
+  }
+  // The off-diagonal quadrants of P (rows 64-127 of P tile 0, rows 0-63 of
+  // P tile 1) and of the mean operand (B's rows of A's, A's rows of B's)
+  // stay zero: each row writes only its own tile's part.
+  for (int c = threadIdx.x; c < 2 * 512; c += NTHREADS) {  // 16-byte chunks: 2 x 8 KB
+    const int t = c >> 9, o = (c & 511) << 4;
+    *reinterpret_cast<uint4*>(sm + SM_P + t * TILE_BYTES + (t ? 0 : 8192) + o) = make_uint4(0, 0, 0, 0);
+  }
+  for (int c = threadIdx.x; c < 2 * 128; c += NTHREADS) {  // 16-byte chunks: 2 x 2 KB
+    const int t = c >> 7, o = (c & 127) << 4;
+    *reinterpret_cast<uint4*>(sm + SM_L + t * L_BYTES + (t ? 0 : 2048) + o) = make_uint4(0, 0, 0, 0);
+  }
+  // per query tile of the CTA (two), the bitmask of the blocks it keeps
+  uint32_t* kept_w = reinterpret_cast<uint32_t*>(sm + SM_KEPT);
+  const int nkw = (p.nbp + 31) >> 5;
+  for (int w = warp; w < nkw && w < KEPT_WORDS; w += NTHREADS / 32) {
+    const int b = 32 * w + lane;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t m = __ballot_sync(0xffffffffu, b < p.nbp && block_kept(p, bh, qt0 + q, b));
+      if (lane == 0) kept_w[q * KEPT_WORDS + w] = m;
+    }
+  }
+  fence_proxy_async_smem();
+  if (warp == WARP_MMA) tmem_alloc(sb + SM_TSLOT, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TSLOT);
+
+  // Each query tile's steps, the same in every role.
+  const int kept_lim = p.nbp < 32 * KEPT_WORDS ? p.nbp : 32 * KEPT_WORDS;
+  auto next_kept = [&](int q, int b) {  // the next block after b that query tile qt0 + q keeps
+    const uint32_t* kw = kept_w + q * KEPT_WORDS;
+    int u = b + 1;
+    for (; u < kept_lim; u = (u | 31) + 1) {  // bits past nbp are 0
+      const uint32_t m = kw[u >> 5] >> (u & 31);
+      if (m) return u + __ffs(static_cast<int>(m)) - 1;
+    }
+    return u < p.nbp ? next_kept_slow(p, bh, qt0 + q, u) : -1;
+  };
+  auto pair_after = [&](int q, int b) -> int2 {  // the step of query tile q that starts after block b
+    const int x = next_kept(q, b);
+    return make_int2(x, x >= 0 ? next_kept(q, x) : -1);
+  };
+  auto next_pair = [&](int q, int2 pr) { return pr.y < 0 ? make_int2(-1, -1) : pair_after(q, pr.y); };
+  int nst = 0;  // steps of the slot: the larger of the two tiles' counts
+  {
+    int nb[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      nb[q] = 0;
+      for (int w = 0; w < nkw && w < KEPT_WORDS; ++w) nb[q] += __popc(kept_w[q * KEPT_WORDS + w]);
+      for (int u = 32 * KEPT_WORDS; u >= 0 && (u = next_kept_slow(p, bh, qt0 + q, u)) >= 0; ++u) ++nb[q];
+    }
+    nst = max((nb[0] + 1) >> 1, (nb[1] + 1) >> 1);
+  }
+
+  if (warp == WARP_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && !(p.debug_flags & 1) && nst > 0) {
+      const int h3 = static_cast<int>(bh);
+      const float* mu = p.vmu_op + bh * p.nbp * (4 * D);  // 2 KiB per block
+      // the four blocks of a step (A's two, B's two); an absent one is
+      // replaced by a present block of the step, so every byte is finite
+      auto quad = [](int2 pa, int2 pb) {
+        const int f = pa.x >= 0 ? pa.x : pb.x;
+        const int a0 = pa.x >= 0 ? pa.x : f, b0 = pb.x >= 0 ? pb.x : f;
+        return make_int4(a0, pa.y >= 0 ? pa.y : a0, b0, pb.y >= 0 ? pb.y : b0);
+      };
+      auto load_k = [&](int st, int4 q4, uint32_t b) {
+        const uint32_t dk = sb + SM_K + st * K_STAGE;
+        tma_load_3d(dk, &tmk, 0, q4.x * BLK, h3, b);
+        tma_load_3d(dk + KBOX, &tmk, 0, q4.y * BLK, h3, b);
+        tma_load_3d(dk + 2 * KBOX, &tmk, 0, q4.z * BLK, h3, b);
+        tma_load_3d(dk + 3 * KBOX, &tmk, 0, q4.w * BLK, h3, b);
+      };
+      auto load_v = [&](int st, int4 q4, uint32_t b) {
+        const uint32_t dv = sb + SM_V + st * V_STAGE, dm = sb + SM_MU + st * MU_STAGE;
+        tma_load_3d(dv, &tmv, q4.x * BLK, 0, h3, b);
+        tma_load_3d(dv + V_HALF, &tmv, q4.y * BLK, 0, h3, b);
+        tma_load_3d(dv + 2 * V_HALF, &tmv, q4.z * BLK, 0, h3, b);
+        tma_load_3d(dv + 3 * V_HALF, &tmv, q4.w * BLK, 0, h3, b);
+        bulk_load(dm, mu + q4.x * (4 * D), MU_HALF, b);
+        bulk_load(dm + MU_HALF, mu + q4.y * (4 * D), MU_HALF, b);
+        bulk_load(dm + 2 * MU_HALF, mu + q4.z * (4 * D), MU_HALF, b);
+        bulk_load(dm + 3 * MU_HALF, mu + q4.w * (4 * D), MU_HALF, b);
+      };
+      int2 pa = pair_after(0, -1), pb = pair_after(1, -1);
+      const uint32_t qb = bar(B_QFULL);
+      mbar_arrive_expect_tx(qb, TILE_BYTES + K_STAGE);
+      tma_load_3d(sb + SM_Q, &tmq, 0, q0, h3, qb);
+      load_k(0, quad(pa, pb), qb);
+      // Test hook: with debug_flags >> 8 = n > 0 the producer stops after n
+      // steps, as if its loads had stalled mid-stream.
+      const int stop_after = p.debug_flags >> 8;
+      int armed[NS];  // the last step that armed each stage (-1: none)
+#pragma unroll
+      for (int u = 0; u < NS; ++u) armed[u] = -1;
+      // Step j brings V(j) and its mean tiles into stage j % NS and K(j+1)
+      // into K stage (j+1) % NS, all on one barrier.  A K stage is free again
+      // once the QK that read it was done, a V stage once the mean terms of
+      // its step were issued.
+      for (int j = 0; j < nst && !*abort && !(stop_after > 0 && j >= stop_after); ++j) {
+        const int st = j % NS, stk = (j + 1) % NS;
+        const int2 na = pa.x >= 0 ? next_pair(0, pa) : pa, nb = pb.x >= 0 ? next_pair(1, pb) : pb;
+        const bool more = j + 1 < nst;
+        if (j >= NS && !mbar_wait(bar(B_VEMPTY + st), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
+          record_timeout(p, abort);
+          break;
+        }
+        if (more && j + 1 >= NS &&
+            !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / NS) - 1) & 1, abort, WAIT_NS)) {
+          record_timeout(p, abort);
+          break;
+        }
+        mbar_arrive_expect_tx(bar(B_FULL + st), V_STAGE - 4 * 1024 + MU_STAGE + (more ? K_STAGE : 0));
+        load_v(st, quad(pa, pb), bar(B_FULL + st));
+        if (more) load_k(stk, quad(na, nb), bar(B_FULL + st));
+        armed[st] = j;
+        pa = na;
+        pb = nb;
+      }
+      // Drain: every copy issued has landed before the CTA can exit, also
+      // when a consumer gave up (time-bounded, ignoring the abort flag).  A
+      // stage is re-armed only after its previous fill was consumed, so
+      // waiting for the parity of its last fill is enough.
+      bool drained = mbar_wait_time(qb, 0, WAIT_NS);
+#pragma unroll
+      for (int u = 0; u < NS; ++u)
+        if (armed[u] >= 0) drained &= mbar_wait_time(bar(B_FULL + u), (armed[u] / NS) & 1, WAIT_NS);
+      if (!drained) record_timeout(p, abort);
+    }
+  } else if (warp == WARP_MMA) {
+    // ----------------------------------------------------------- MMA issue
+    if (lane == 0 && nst > 0) {
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort, WAIT_NS);
+      tc_fence_after();
+      const uint64_t dQ = sdesc_sw128(sb + SM_Q), dK = sdesc_sw128(sb + SM_K);
+      const uint64_t dV = sdesc_sw64(sb + SM_V), dP = sdesc_sw128(sb + SM_P);
+      const uint64_t dL = sdesc_k8_tf32(sb + SM_L);
+      // mean operand of one tile: two 2 KiB parts (its two blocks), K-slots
+      // 0..3 and 4..7, 16-byte rows, one row per channel
+      const uint64_t dMu = sdesc(sb + SM_MU, MU_HALF, 128, 0);
+      const uint32_t dO = tmem + COL_O;
+      auto adv = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+      auto wt = [&](int b, uint32_t par) {
+        if (!ok) return;
+        ok = mbar_wait(bar(b), par, abort, WAIT_NS);
+        tc_fence_after();
+      };
+      auto qk = [&](int j) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8(tmem + COL_S, adv(dQ, 32 * kk), adv(dK, (j % NS) * K_STAGE + 32 * kk), IDESC_QK, kk > 0);
+        mma_commit(bar(B_SFULL));
+        mma_commit(bar(B_KEMPTY + j % NS));
+      };
+      auto mean = [&](int j) {  // both tiles' mean terms of step j
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          mma_tf32(dO, adv(dL, t * L_BYTES), adv(dMu, (j % NS) * MU_STAGE + t * 2 * MU_HALF), IDESC_TF32, 1);
+      };
+      auto pv = [&](int j) {  // mean terms of step j-1, then [O | l] += P(j) [V ; indicators]
+        wt(B_PFULL, j & 1);
+        if (!ok) return;
+        if (j > 0) {
+          mean(j - 1);
+          mma_commit(bar(B_VEMPTY + (j - 1) % NS));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f8(dO, adv(dP, (kk >> 2) * TILE_BYTES + 32 * (kk & 3)),
+                 adv(dV, (j % NS) * V_STAGE + (kk >> 1) * V_HALF + 32 * (kk & 1)), IDESC_PV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_ODONE));
+      };
+      for (int i = 0; ok && i <= nst; ++i) {
+        if (i < nst) {
+          // K(i) came with Q (i = 0) or with V(i-1); S is free once the
+          // softmax holds S(i-1)
+          if (i > 0) {
+            wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);
+            wt(B_STAKEN, (i - 1) & 1);
+          }
+          if (!ok) break;
+          qk(i);
+        }
+        if (i > 0) {
+          if (i == nst) wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);  // V of the last step
+          pv(i - 1);
+        }
+      }
+      // the last step's mean terms (the softmax's extra p_full arrival)
+      wt(B_PFULL, nst & 1);
+      if (ok) {
+        mean(nst - 1);
+        mma_commit(bar(B_MDONE));
+      }
+      if (!ok) record_timeout(p, abort);
+      // Drain: every MMA of this lane has completed before TMEM is released,
+      // also after an abort (the wait ignores the abort flag).
+      mma_commit(bar(B_FIN));
+      if (!mbar_wait_time(bar(B_FIN), 0, WAIT_NS)) record_timeout(p, abort);
+    }
+  } else if (warp >= WARP_SOFTMAX) {
+    // ------------------------------------------------------ softmax warps
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int my_tile = r >> 6;  // 0: A, 1: B (warp-uniform)
+    const int64_t row = static_cast<int64_t>(q0) + r;
+    const bool row_ok = row < p.N;
+    const int qt = static_cast<int>(row >> 6);
+    const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + COL_S + 128 * my_tile;
+    const uint32_t tO = tmem + lane_addr + COL_O;
+    const uint32_t tL = tO + 128 + 2 * my_tile;  // this tile's two row-sum columns
+    uint8_t* Prow = sm + SM_P + my_tile * TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+    uint8_t* Lrow = sm + SM_L + my_tile * L_BYTES + (r >> 3) * 256 + (r & 7) * 16;
+    const float qsc = p.q_scale[bh * p.nbp + (qt < p.nbp ? qt : p.nbp - 1)];
+    const float a_i = p.c0 * qsc;
+    const float* ksc = p.k_scale + bh * p.nbp;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const uint32_t FULL = 0xffffffffu;
+    auto ld_rowsums = [&](float& l0, float& l1) {
+      uint32_t ls0, ls1;
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(ls0), "=r"(ls1) : "r"(tL));
+      tmem_wait_ld();
+      l0 = __uint_as_float(ls0);
+      l1 = __uint_as_float(ls1);
+    };
+    // tf32 A operand row of this tile's mean MMA, [hi0, lo0, hi0, 0 | hi1,
+    // lo1, hi1, 0] against the mean tiles' (hi, hi, lo, 0) of its two blocks
+    auto put_lrow = [&](float v0, float v1) {
+      const float h0 = to_tf32(v0), h1 = to_tf32(v1);
+      const float g0 = to_tf32(v0 - h0), g1 = to_tf32(v1 - h1);
+      *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, 0.0f);
+      *reinterpret_cast<float4*>(Lrow + 128) = make_float4(h1, g1, h1, 0.0f);
+      fence_proxy_async_smem();
+    };
+    float m_run = NEG_INF;
+    float l = 0.0f;
+    bool ok = true;
+    int2 pr = pair_after(my_tile, -1);  // this row's tile's current step (x = -1: none)
+    int i = 0;
+    for (; i < nst; ++i) {
+      const int2 pn = pr.x >= 0 ? next_pair(my_tile, pr) : pr;
+      const bool keep0 = row_ok && pr.x >= 0;
+      const bool keep1 = row_ok && pr.y >= 0;
+      const int n32 = static_cast<int>(p.N);
+      const int lim_lo = pr.x >= 0 ? n32 - pr.x * BLK : BLK;
+      const int lim_hi = pr.y >= 0 ? BLK + n32 - pr.y * BLK : TILE;
+      const float A0 = pr.x >= 0 ? a_i * ksc[pr.x] : 0.0f;
+      const float A1 = pr.y >= 0 ? a_i * ksc[pr.y] : 0.0f;
+      const bool partial = !__all_sync(FULL, lim_lo >= BLK && lim_hi >= TILE);
+
+      if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL), i & 1, abort, WAIT_NS)))) break;
+      tc_fence_after();
+      float x[128];
+      uint32_t w[32];
+      float m_new, alpha;
+      bool resc;
+      {
+        {
+          uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
+          uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
+          uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
+          uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
+          tmem_ld32(tS + 0, c0);
+          tmem_ld32(tS + 32, c1);
+          tmem_ld32(tS + 64, c2);
+          tmem_ld32(tS + 96, c3);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_STAKEN));  // S may be overwritten
+        if (partial) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) x[j] = j < (j < 64 ? lim_lo : lim_hi) ? x[j] : NEG_INF;
+        }
+        float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
+        float mc = fmax3(x[64], x[65], x[66]), md = fmax3(x[96], x[97], x[98]);
+#pragma unroll
+        for (int j = 3; j < 31; j += 2) {
+          ma = fmax3(ma, x[j], x[j + 1]);
+          mb = fmax3(mb, x[32 + j], x[33 + j]);
+          mc = fmax3(mc, x[64 + j], x[65 + j]);
+          md = fmax3(md, x[96 + j], x[97 + j]);
+        }
+        const float mx0 = fmax3(ma, mb, fmaxf(x[31], x[63]));
+        const float mx1 = fmax3(mc, md, fmaxf(x[95], x[127]));
+        const float m_tile = fmaxf(keep0 ? A0 * mx0 : NEG_INF, keep1 ? A1 * mx1 : NEG_INF);
+        const bool need = m_tile > m_run + p.tau8;
+        m_new = need ? m_tile : m_run;
+        const bool live = m_new != NEG_INF;
+        resc = need && m_run != NEG_INF;
+        alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
+        if (partial) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
+        }
+        const bool k0 = live && keep0, k1 = live && keep1;
+        const float Bq = (p.C - m_new) * 0.00390625f;
+        const float A0q = k0 ? A0 * 0.00390625f : 0.0f, B0q = k0 ? Bq : 0.0f;
+        const float A1q = k1 ? A1 * 0.00390625f : 0.0f, B1q = k1 ? Bq : 0.0f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q,
+                          q < 16 ? B0q : B1q);
+        if (partial) {
+          const int lim0 = k0 ? (lim_lo < 64 ? lim_lo : 64) : 0;
+          const int lim1 = k1 ? (lim_hi < 128 ? lim_hi : 128) : 64;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            uint32_t keep = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * q + e < (q < 16 ? lim0 : lim1)) keep |= 0xFFu << (8 * e);
+            w[q] &= keep;
+          }
+        }
+      }
+      m_run = m_new;
+      if (i > 0) {
+        // PV(i-1) done (and with it the mean terms of step i-2): P may be
+        // overwritten and the row sums of step i-1 are final.
+        if (!(ok = __all_sync(FULL, mbar_wait(bar(B_ODONE), (i - 1) & 1, abort, WAIT_NS)))) break;
+        tc_fence_after();
+      }
+      // row r of this tile's P: 128 bytes, 16-byte chunk c at position c ^ (r & 7)
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(Prow + ((c ^ (r & 7)) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      if (i > 0) {
+        // Row sums of step i-1: read and cleared, so that PV(i) accumulates
+        // its own.  If the maximum moved, O and l move to the new maximum,
+        // and the mean operand of step i-1 is written already scaled.
+        float l0, l1;
+        ld_rowsums(l0, l1);
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tL), "r"(0u), "r"(0u)
+                     : "memory");
+        if (__any_sync(FULL, resc)) {
+          uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
+          uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
+          uint32_t (&o2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
+          uint32_t (&o3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
+          tmem_ld32(tO + 0, o0);
+          tmem_ld32(tO + 32, o1);
+          tmem_ld32(tO + 64, o2);
+          tmem_ld32(tO + 96, o3);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 128; ++e) x[e] *= alpha;
+          tmem_st32(tO + 0, o0);
+          tmem_st32(tO + 32, o1);
+          tmem_st32(tO + 64, o2);
+          tmem_st32(tO + 96, o3);
+        }
+        l = (l + (l0 + l1)) * alpha;
+        put_lrow(l0 * alpha, l1 * alpha);
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL));
+      pr = pn;
+    }
+    // the last step's row sums, then its mean terms
+    if (ok && nst > 0) {
+      ok = __all_sync(FULL, mbar_wait(bar(B_ODONE), (nst - 1) & 1, abort, WAIT_NS));
+      if (ok) {
+        tc_fence_after();
+        float l0, l1;
+        ld_rowsums(l0, l1);
+        l += l0 + l1;
+        put_lrow(l0, l1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL));
+        ok = __all_sync(FULL, mbar_wait(bar(B_MDONE), 0, abort, WAIT_NS));
+        tc_fence_after();
+      }
+    }
+    if (!ok) record_timeout(p, abort);
+
+    // ------------------------------------------------------------ epilogue
+    const bool have = ok && nst > 0;
+    if (__all_sync(0xffffffffu, have)) {
+      const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        if (row_ok) {
+          float y[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            y[e] = __uint_as_float(o[e]) * p.v_scale[bh * D + 32 * c + e] * inv_l;
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + p.lo.head(bh) + p.lo.row(row) + 32 * c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const __nv_bfloat162 v2 = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&v2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.O) + p.lo.head(bh) + p.lo.row(row) + 32 * c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+      }
+    } else if (row_ok && nst == 0) {
+      const int nvec = p.out_f32 ? 32 : 16;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.O) +
+                                            (p.lo.head(bh) + p.lo.row(row)) * (p.out_f32 ? 4 : 2));
+      for (int e = 0; e < nvec; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+    }
+    if (row_ok && p.lse2) {
+      p.lse2[bh * p.N + row] = l > 0.0f
+          ? m_run * 0.125f - p.off + log2f(l) + p.qmu[bh * p.N + row] * p.lse_qmu
+          : -__int_as_float(0x7f800000);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == WARP_MMA) tmem_dealloc(tmem, 512);
+}
+}  // namespace sp
+
 // The driver's tensor-map encoder (looked up once; a function-local static is
 // initialised thread-safely).
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -928,14 +1471,18 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_MASKED);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(sp::attn_sparse, cudaFuncAttributeMaxDynamicSharedMemorySize, sp::SMEM_BYTES);
     return e;
   });
   if (ea != cudaSuccess) return ea;
-  const dim3 grid(static_cast<unsigned>(ceil_div(Np, CTA_ROWS)), static_cast<unsigned>(a.BH));
-  if (p.mask)
-    attn_fwd<true><<<grid, NTHREADS, SMEM_BYTES_MASKED, s>>>(mq, mk, mv, p);
-  else
+  if (p.mask) {
+    const dim3 grid(static_cast<unsigned>(Np / TILE), static_cast<unsigned>(a.BH));
+    sp::attn_sparse<<<grid, sp::NTHREADS, sp::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  } else {
+    const dim3 grid(static_cast<unsigned>(ceil_div(Np, CTA_ROWS)), static_cast<unsigned>(a.BH));
     attn_fwd<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+  }
   return cudaGetLastError();
 }
 
