@@ -875,8 +875,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // the next QK as soon as the softmax holds S in registers.
 namespace sp {
 constexpr int NTHREADS = 256;
-constexpr int WARP_MMA = 0, WARP_TMA = 1, WARP_SOFTMAX = 4;
-constexpr int NS = 2;
+constexpr int WARP_MMA = 0, WARP_TMA = 1, WARP_PV = 2, WARP_SOFTMAX = 4;
+constexpr int NS = 2;   // K and V stages
+constexpr int NM = 3;   // mean-tile stages
 constexpr uint32_t COL_S = 0;
 constexpr uint32_t COL_O = 256;
 constexpr uint32_t KBOX = 8192;              // 64 keys x 128 channels, 128B swizzle
@@ -890,16 +891,19 @@ constexpr uint32_t SM_Q = 0;
 constexpr uint32_t SM_K = SM_Q + TILE_BYTES;
 constexpr uint32_t SM_V = SM_K + NS * K_STAGE;
 constexpr uint32_t SM_MU = SM_V + NS * V_STAGE;
-constexpr uint32_t SM_L = SM_MU + NS * MU_STAGE;
+constexpr uint32_t SM_L = SM_MU + NM * MU_STAGE;
 constexpr uint32_t SM_P = SM_L + 2 * L_BYTES;      // P tile 0 (keys of A), P tile 1 (keys of B)
 constexpr uint32_t SM_KEPT = SM_P + 2 * TILE_BYTES;
 constexpr uint32_t SM_BAR = SM_KEPT + 2 * 4 * KEPT_WORDS;
 enum {
   B_QFULL = 0,
-  B_FULL,
-  B_KEMPTY = B_FULL + NS,
-  B_VEMPTY = B_KEMPTY + NS,
-  B_SFULL = B_VEMPTY + NS,
+  B_KFULL,
+  B_KEMPTY = B_KFULL + NS,
+  B_VFULL = B_KEMPTY + NS,
+  B_VEMPTY = B_VFULL + NS,
+  B_MFULL = B_VEMPTY + NS,
+  B_MEMPTY = B_MFULL + NM,
+  B_SFULL = B_MEMPTY + NM,
   B_STAKEN,
   B_PFULL,
   B_ODONE,
@@ -930,16 +934,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < NM; ++s) {
+      mbar_init(bar(B_MFULL + s), 1);
+      mbar_init(bar(B_MEMPTY + s), 1);
     }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_STAKEN), 4);
     mbar_init(bar(B_PFULL), 4);
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_MDONE), 1);
-    mbar_init(bar(B_FIN), 1);
+    mbar_init(bar(B_FIN), 2);  // both issuing lanes
     *abort = 0;
     mbar_fence_init();
   }
@@ -1030,11 +1039,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_3d(dk + 3 * KBOX, &tmk, 0, q4.w * BLK, h3, b);
       };
       auto load_v = [&](int st, int4 q4, uint32_t b) {
-        const uint32_t dv = sb + SM_V + st * V_STAGE, dm = sb + SM_MU + st * MU_STAGE;
+        const uint32_t dv = sb + SM_V + st * V_STAGE;
         tma_load_3d(dv, &tmv, q4.x * BLK, 0, h3, b);
         tma_load_3d(dv + V_HALF, &tmv, q4.y * BLK, 0, h3, b);
         tma_load_3d(dv + 2 * V_HALF, &tmv, q4.z * BLK, 0, h3, b);
         tma_load_3d(dv + 3 * V_HALF, &tmv, q4.w * BLK, 0, h3, b);
+      };
+      auto load_mu = [&](int st, int4 q4, uint32_t b) {
+        const uint32_t dm = sb + SM_MU + st * MU_STAGE;
         bulk_load(dm, mu + q4.x * (4 * D), MU_HALF, b);
         bulk_load(dm + MU_HALF, mu + q4.y * (4 * D), MU_HALF, b);
         bulk_load(dm + 2 * MU_HALF, mu + q4.z * (4 * D), MU_HALF, b);
@@ -1042,38 +1054,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       };
       int2 pa = pair_after(0, -1), pb = pair_after(1, -1);
       const uint32_t qb = bar(B_QFULL);
-      mbar_arrive_expect_tx(qb, TILE_BYTES + K_STAGE);
+      mbar_arrive_expect_tx(qb, TILE_BYTES);
       tma_load_3d(sb + SM_Q, &tmq, 0, q0, h3, qb);
-      load_k(0, quad(pa, pb), qb);
       // Test hook: with debug_flags >> 8 = n > 0 the producer stops after n
       // steps, as if its loads had stalled mid-stream.
       const int stop_after = p.debug_flags >> 8;
-      int armed[NS];  // the last step that armed each stage (-1: none)
+      // the last step that armed each stage (-1: none)
+      int karmed[NS], varmed[NS], marmed[NM];
 #pragma unroll
-      for (int u = 0; u < NS; ++u) armed[u] = -1;
-      // Step j brings V(j) and its mean tiles into stage j % NS and K(j+1)
-      // into K stage (j+1) % NS, all on one barrier.  A K stage is free again
-      // once the QK that read it was done, a V stage once the mean terms of
-      // its step were issued.
+      for (int u = 0; u < NS; ++u) karmed[u] = varmed[u] = -1;
+#pragma unroll
+      for (int u = 0; u < NM; ++u) marmed[u] = -1;
+      // Step j: K(j) once QK(j-2) has read its stage, V(j) once PV(j-2) has,
+      // and the mean tiles of j once the mean terms of j-3 are done, each on
+      // barriers of its own, so that no load waits for another's stage.
       for (int j = 0; j < nst && !*abort && !(stop_after > 0 && j >= stop_after); ++j) {
-        const int st = j % NS, stk = (j + 1) % NS;
-        const int2 na = pa.x >= 0 ? next_pair(0, pa) : pa, nb = pb.x >= 0 ? next_pair(1, pb) : pb;
-        const bool more = j + 1 < nst;
-        if (j >= NS && !mbar_wait(bar(B_VEMPTY + st), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
+        const int sk = j % NS, sm3 = j % NM;
+        const int4 q4 = quad(pa, pb);
+        if (j >= NS && !mbar_wait(bar(B_KEMPTY + sk), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
-        if (more && j + 1 >= NS &&
-            !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / NS) - 1) & 1, abort, WAIT_NS)) {
+        mbar_arrive_expect_tx(bar(B_KFULL + sk), K_STAGE);
+        load_k(sk, q4, bar(B_KFULL + sk));
+        karmed[sk] = j;
+        if (j >= NS && !mbar_wait(bar(B_VEMPTY + sk), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
-        mbar_arrive_expect_tx(bar(B_FULL + st), V_STAGE - 4 * 1024 + MU_STAGE + (more ? K_STAGE : 0));
-        load_v(st, quad(pa, pb), bar(B_FULL + st));
-        if (more) load_k(stk, quad(na, nb), bar(B_FULL + st));
-        armed[st] = j;
-        pa = na;
-        pb = nb;
+        mbar_arrive_expect_tx(bar(B_VFULL + sk), V_STAGE - 4 * 1024);
+        load_v(sk, q4, bar(B_VFULL + sk));
+        varmed[sk] = j;
+        if (j >= NM && !mbar_wait(bar(B_MEMPTY + sm3), ((j / NM) - 1) & 1, abort, WAIT_NS)) {
+          record_timeout(p, abort);
+          break;
+        }
+        mbar_arrive_expect_tx(bar(B_MFULL + sm3), MU_STAGE);
+        load_mu(sm3, q4, bar(B_MFULL + sm3));
+        marmed[sm3] = j;
+        if (pa.x >= 0) pa = next_pair(0, pa);
+        if (pb.x >= 0) pb = next_pair(1, pb);
       }
       // Drain: every copy issued has landed before the CTA can exit, also
       // when a consumer gave up (time-bounded, ignoring the abort flag).  A
@@ -1081,15 +1101,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // waiting for the parity of its last fill is enough.
       bool drained = mbar_wait_time(qb, 0, WAIT_NS);
 #pragma unroll
-      for (int u = 0; u < NS; ++u)
-        if (armed[u] >= 0) drained &= mbar_wait_time(bar(B_FULL + u), (armed[u] / NS) & 1, WAIT_NS);
+      for (int u = 0; u < NS; ++u) {
+        if (karmed[u] >= 0) drained &= mbar_wait_time(bar(B_KFULL + u), (karmed[u] / NS) & 1, WAIT_NS);
+        if (varmed[u] >= 0) drained &= mbar_wait_time(bar(B_VFULL + u), (varmed[u] / NS) & 1, WAIT_NS);
+      }
+#pragma unroll
+      for (int u = 0; u < NM; ++u)
+        if (marmed[u] >= 0) drained &= mbar_wait_time(bar(B_MFULL + u), (marmed[u] / NM) & 1, WAIT_NS);
       if (!drained) record_timeout(p, abort);
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp == WARP_MMA || warp == WARP_PV) {
     // ----------------------------------------------------------- MMA issue
+    // Two issuing lanes: warp 0 issues the QKs, warp 2 the mean terms and
+    // PVs (S and O are disjoint columns; tcgen05.commit tracks each lane's
+    // own MMAs).
     if (lane == 0 && nst > 0) {
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort, WAIT_NS);
-      tc_fence_after();
+      bool ok = true;
       const uint64_t dQ = sdesc_sw128(sb + SM_Q), dK = sdesc_sw128(sb + SM_K);
       const uint64_t dV = sdesc_sw64(sb + SM_V), dP = sdesc_sw128(sb + SM_P);
       const uint64_t dL = sdesc_k8_tf32(sb + SM_L);
@@ -1103,57 +1130,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = mbar_wait(bar(b), par, abort, WAIT_NS);
         tc_fence_after();
       };
-      auto qk = [&](int j) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f8(tmem + COL_S, adv(dQ, 32 * kk), adv(dK, (j % NS) * K_STAGE + 32 * kk), IDESC_QK, kk > 0);
-        mma_commit(bar(B_SFULL));
-        mma_commit(bar(B_KEMPTY + j % NS));
-      };
-      auto mean = [&](int j) {  // both tiles' mean terms of step j
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          mma_tf32(dO, adv(dL, t * L_BYTES), adv(dMu, (j % NS) * MU_STAGE + t * 2 * MU_HALF), IDESC_TF32, 1);
-      };
-      auto pv = [&](int j) {  // mean terms of step j-1, then [O | l] += P(j) [V ; indicators]
-        wt(B_PFULL, j & 1);
-        if (!ok) return;
-        if (j > 0) {
-          mean(j - 1);
-          mma_commit(bar(B_VEMPTY + (j - 1) % NS));
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f8(dO, adv(dP, (kk >> 2) * TILE_BYTES + 32 * (kk & 3)),
-                 adv(dV, (j % NS) * V_STAGE + (kk >> 1) * V_HALF + 32 * (kk & 1)), IDESC_PV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_ODONE));
-      };
-      for (int i = 0; ok && i <= nst; ++i) {
-        if (i < nst) {
-          // K(i) came with Q (i = 0) or with V(i-1); S is free once the
-          // softmax holds S(i-1)
-          if (i > 0) {
-            wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);
-            wt(B_STAKEN, (i - 1) & 1);
-          }
+      if (warp == WARP_MMA) {
+        // QK(i) once K(i) is in and the softmax holds S(i-1)
+        wt(B_QFULL, 0);
+        for (int i = 0; ok && i < nst; ++i) {
+          wt(B_KFULL + i % NS, (i / NS) & 1);
+          if (i > 0) wt(B_STAKEN, (i - 1) & 1);
           if (!ok) break;
-          qk(i);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8(tmem + COL_S, adv(dQ, 32 * kk), adv(dK, (i % NS) * K_STAGE + 32 * kk), IDESC_QK, kk > 0);
+          mma_commit(bar(B_SFULL));
+          mma_commit(bar(B_KEMPTY + i % NS));
         }
-        if (i > 0) {
-          if (i == nst) wt(B_FULL + (i - 1) % NS, ((i - 1) / NS) & 1);  // V of the last step
-          pv(i - 1);
+      } else {
+        auto mean = [&](int j) {  // both tiles' mean terms of step j
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            mma_tf32(dO, adv(dL, t * L_BYTES), adv(dMu, (j % NM) * MU_STAGE + t * 2 * MU_HALF), IDESC_TF32, 1);
+        };
+        // mean terms of step j-1, then [O | l] += P(j) [V ; indicators], once
+        // V(j) is in and the softmax has written P(j) (and the mean operand
+        // of j-1)
+        for (int j = 0; ok && j < nst; ++j) {
+          wt(B_VFULL + j % NS, (j / NS) & 1);
+          wt(B_PFULL, j & 1);
+          if (j > 0) wt(B_MFULL + (j - 1) % NM, ((j - 1) / NM) & 1);
+          if (!ok) break;
+          if (j > 0) {
+            mean(j - 1);
+            mma_commit(bar(B_MEMPTY + (j - 1) % NM));
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f8(dO, adv(dP, (kk >> 2) * TILE_BYTES + 32 * (kk & 3)),
+                   adv(dV, (j % NS) * V_STAGE + (kk >> 1) * V_HALF + 32 * (kk & 1)), IDESC_PV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(B_VEMPTY + j % NS));
+          mma_commit(bar(B_ODONE));
         }
-      }
-      // the last step's mean terms (the softmax's extra p_full arrival)
-      wt(B_PFULL, nst & 1);
-      if (ok) {
-        mean(nst - 1);
-        mma_commit(bar(B_MDONE));
+        // the last step's mean terms (the softmax's extra p_full arrival)
+        wt(B_PFULL, nst & 1);
+        wt(B_MFULL + (nst - 1) % NM, ((nst - 1) / NM) & 1);
+        if (ok) {
+          mean(nst - 1);
+          mma_commit(bar(B_MDONE));
+        }
       }
       if (!ok) record_timeout(p, abort);
-      // Drain: every MMA of this lane has completed before TMEM is released,
-      // also after an abort (the wait ignores the abort flag).
+      // Drain: every MMA of both lanes has completed before TMEM is
+      // released, also after an abort (the wait ignores the abort flag).
       mma_commit(bar(B_FIN));
       if (!mbar_wait_time(bar(B_FIN), 0, WAIT_NS)) record_timeout(p, abort);
     }
