@@ -18,10 +18,10 @@
 //   split into tf32 high and low parts and whose B operand is the prepared
 //   mean tile.
 //
-// CTA = 256 query rows (two 128-row slots) of one (b, h).  Warps 0 and 1
-// issue the MMAs of slot 0 and slot 1 from one lane each (warp 0 also
-// allocates TMEM), warp 2 issues the TMA loads (with a tile mask: those of
-// slot 0, and warp 3 those of slot 1; dense, warp 3 is idle), warps 4-7 run
+// Dense kernel (attn_fwd).  CTA = 256 query rows (two 128-row slots) of one
+// (b, h).  Warps 0 and 1 issue the MMAs of slot 0 and slot 1 from one lane
+// each (warp 0 also allocates TMEM), warp 2 issues the TMA loads (warp 3 is
+// idle), warps 4-7 run
 // the softmax of slot 0 (thread = row = TMEM lane quarter warp & 3) and warps
 // 8-11 that of slot 1.  The issuing warps have the lowest warp numbers so that
 // the warp schedulers favour them over the softmax warps sharing their
@@ -50,18 +50,10 @@
 // tcgen05 operations of one thread complete in issue order, so "PV(t-1)
 // done" implies that MEAN(t-2) is done.
 //
-// A KV tile is two 64-key blocks, one per 64-column half of S and P.  Dense,
-// tile t holds blocks 2t and 2t+1 (one 128-row TMA box of K and of V) for
-// both slots, through one ring of NS stages.  With a tile mask, each query
-// 64-tile has its own KV steps: the blocks it keeps, in ascending order, two
-// per step.  A slot (two query tiles) streams its first tile's step 0, its
-// second tile's step 0, the first tile's step 1, and so on, through two
-// stages of its own; only the rows of the tile whose step it is use it, the
-// other 64 rows treat it as absent (codes 0, no max, no row sum).  K arrives
-// as two 64-row boxes, V as two 64-key boxes in the 64B-swizzled layout
-// (each half of the PV B operand has its own indicator row), and the mean
-// tile as two 2 KiB halves.  The slots then have different tile counts; S is
-// taken in turn while both have tiles, and the slot with more goes on alone.
+// A KV tile is two 64-key blocks, one per 64-column half of S and P: tile t
+// holds blocks 2t and 2t+1 (one 128-row TMA box of K and of V) for both
+// slots, through one ring of NS stages.  With a tile mask the block-sparse
+// kernel (attn_sparse, below) runs instead.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -89,7 +81,6 @@ constexpr uint32_t COL_L = 128;    // row sums inside O_s
 
 constexpr uint32_t TILE_BYTES = 16384;    // 128 x 128 E4M3
 constexpr uint32_t V_STAGE = 18432;       // V tile + 16 indicator rows
-constexpr uint32_t V_HALF = 9216;         // masked: 144 x 64 keys per block (64B swizzle)
 constexpr uint32_t MU_BYTES = 4096;       // 128 x 8 tf32
 constexpr uint32_t SM_Q = 0;
 constexpr uint32_t SM_K = SM_Q + 2 * TILE_BYTES;
@@ -99,8 +90,8 @@ constexpr uint32_t SM_L = SM_MU + NS * MU_BYTES;
 constexpr uint32_t SM_P = SM_L + 2 * MU_BYTES;  // P of each slot, A operand of the PV MMA
 constexpr uint32_t SM_BAR = SM_P + 2 * TILE_BYTES;
 enum {
-  B_QFULL = 0,  // + slot (dense: entry 0 for both Q tiles)
-  B_FULL = 2,   // V(j) and its mean tile in stage j's, plus K(j+1)
+  B_QFULL = 0,  // both Q tiles and K(0)
+  B_FULL = 1,   // V(j) and its mean tile in stage j's, plus K(j+1)
   B_KEMPTY = B_FULL + NS,
   B_VEMPTY = B_KEMPTY + NS,
   B_SFULL = B_VEMPTY + NS,
@@ -115,13 +106,11 @@ constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
 constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
 constexpr uint32_t SM_END = SM_ABORT + 8;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;  // slack for 1024-byte alignment
-// Masked: per query 64-tile of the CTA (four), one bit per 64-key block, set
-// when the tile keeps it (the first 32 * KEPT_WORDS blocks; later ones are
-// looked up in the mask itself).
-constexpr uint32_t SM_KEPT = SM_END;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// Block-sparse kernel: per query 64-tile of the CTA, one bit per 64-key
+// block, set when the tile keeps it (the first 32 * KEPT_WORDS blocks; later
+// ones are looked up in the mask itself).
 constexpr int KEPT_WORDS = 112;  // per query tile
-constexpr uint32_t SMEM_BYTES_MASKED = SMEM_BYTES + 4 * 4 * KEPT_WORDS;
-static_assert(SMEM_BYTES_MASKED <= 232448, "shared memory per CTA");
 
 constexpr uint32_t IDESC_QK = idesc(FMT_E4M3, FMT_E4M3, 128, 128);
 constexpr uint32_t IDESC_PV = idesc(FMT_E4M3, FMT_E4M3, 128, 144);
@@ -163,18 +152,6 @@ __device__ __noinline__ int next_kept_slow(const Params& p, int64_t bh, int qt, 
     if (block_kept(p, bh, qt, u)) return u;
   return -1;
 }
-
-// A slot's walk over its KV tiles.  Dense: tile t = blocks (2t, 2t + 1), for
-// all 128 rows.  Masked: each of the slot's two query tiles (A: rows 0-63, B:
-// rows 64-127) has its own steps, the blocks it keeps taken two by two in
-// ascending order (y = -1 in an odd last step); the slot's tiles are A's
-// step 0, B's step 0, A's step 1, ..., and once one tile has no steps left
-// the other goes on alone.  Only the owner's rows use a tile; the others
-// treat it as absent.  x = -1 past the last tile.
-struct Walk {
-  int2 pa, pb;  // the current steps of A and B (masked; dense: pa only)
-  int onB;      // masked: the current tile is B's step
-};
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort) {
   *abort = 1;
@@ -253,10 +230,6 @@ __global__ void expcast_probe(const float4* __restrict__ x, const float* __restr
   out[g] = expcast4(f[0], f[1], f[2], f[3], A[g] * 0.00390625f, B[g] * 0.00390625f) & keep;
 }
 
-// kMasked: the block-sparse instantiation (a tile mask is given: the per-tile
-// bitmask, the block-pair walk, 64-key boxes); the dense one compiles
-// without them.
-template <bool kMasked>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ Params p) {
@@ -270,16 +243,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bh = blockIdx.y;
   const int q0 = blockIdx.x * CTA_ROWS;
-  const int qt0 = q0 / BLK;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_QFULL + 0), 1);
-    mbar_init(bar(B_QFULL + 1), 1);
+    mbar_init(bar(B_QFULL), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(B_FULL + s), 1);
-      // dense: both slots' MMA lanes release a stage; masked: its own slot's
-      mbar_init(bar(B_KEMPTY + s), kMasked ? 1 : 2);
-      mbar_init(bar(B_VEMPTY + s), kMasked ? 1 : 2);
+      // both slots' MMA lanes release a stage
+      mbar_init(bar(B_KEMPTY + s), 2);
+      mbar_init(bar(B_VEMPTY + s), 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
@@ -294,38 +265,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_fence_init();
   }
   // Indicator rows 128..143 of every V stage (B operand rows of the PV MMA,
-  // K-major): row 128 = 1.0 on keys 0..63, row 129 = 1.0 on keys 64..127,
-  // rows 130..143 = 0.  TMA writes only rows 0..127.  Dense: one
-  // 128B-swizzled tile; masked: one 64B-swizzled tile per 64-key half (the
-  // rows are uniform, so the swizzle does not move them).
+  // K-major, 128B-swizzled): row 128 = 1.0 on keys 0..63, row 129 = 1.0 on
+  // keys 64..127, rows 130..143 = 0.  TMA writes only rows 0..127.
   const uint32_t one4 = 0x38383838u;  // four E4M3 1.0 bytes
-  if constexpr (kMasked) {
-    for (int c = threadIdx.x; c < NS * 2 * 16 * 4; c += NTHREADS) {
-      const int st = c >> 7, h = (c >> 6) & 1, n = (c >> 2) & 15, k = c & 3;  // stage, half, row, chunk
-      const uint32_t v = n == h ? one4 : 0u;
-      *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + h * V_HALF + 8192 + n * 64 + k * 16) =
-          make_uint4(v, v, v, v);
-    }
-  } else {
-    for (int c = threadIdx.x; c < NS * 16 * 8; c += NTHREADS) {
-      const int st = c >> 7, n = (c >> 3) & 15, k = c & 7;  // stage, row, 16-key chunk
-      const uint32_t v = ((n == 0 && k < 4) || (n == 1 && k >= 4)) ? one4 : 0u;
-      *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + TILE_BYTES + n * 128 + ((k ^ (n & 7)) * 16)) =
-          make_uint4(v, v, v, v);
-    }
-  }
-  // Masked: per query tile of the CTA, the bitmask of the blocks it keeps.
-  uint32_t* kept_w = reinterpret_cast<uint32_t*>(sm + SM_KEPT);
-  const int nkw = (p.nbp + 31) >> 5;
-  if (kMasked) {
-    for (int w = warp; w < nkw && w < KEPT_WORDS; w += NTHREADS / 32) {
-      const int b = 32 * w + lane;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t m = __ballot_sync(0xffffffffu, b < p.nbp && block_kept(p, bh, qt0 + q, b));
-        if (lane == 0) kept_w[q * KEPT_WORDS + w] = m;
-      }
-    }
+  for (int c = threadIdx.x; c < NS * 16 * 8; c += NTHREADS) {
+    const int st = c >> 7, n = (c >> 3) & 15, k = c & 7;  // stage, row, 16-key chunk
+    const uint32_t v = ((n == 0 && k < 4) || (n == 1 && k >= 4)) ? one4 : 0u;
+    *reinterpret_cast<uint4*>(sm + SM_V + st * V_STAGE + TILE_BYTES + n * 128 + ((k ^ (n & 7)) * 16)) =
+        make_uint4(v, v, v, v);
   }
   fence_proxy_async_smem();
   if (warp == WARP_MMA) tmem_alloc(sb + SM_TSLOT, 512);
@@ -334,143 +281,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TSLOT);
 
-  // Every role of a slot walks the same sequence of tiles (see Walk).
-  const int kept_lim = p.nbp < 32 * KEPT_WORDS ? p.nbp : 32 * KEPT_WORDS;
-  auto next_kept = [&](int q, int b) {  // the next block after b that query tile qt0 + q keeps
-    const uint32_t* kw = kept_w + q * KEPT_WORDS;
-    int u = b + 1;
-    for (; u < kept_lim; u = (u | 31) + 1) {  // bits past nbp are 0
-      const uint32_t m = kw[u >> 5] >> (u & 31);
-      if (m) return u + __ffs(static_cast<int>(m)) - 1;
-    }
-    return u < p.nbp ? next_kept_slow(p, bh, qt0 + q, u) : -1;
-  };
-  auto pair_after = [&](int q, int b) -> int2 {  // the step of query tile q that starts after block b
-    if constexpr (kMasked) {
-      const int x = next_kept(q, b);
-      return make_int2(x, x >= 0 ? next_kept(q, x) : -1);
-    } else {
-      return b + 2 < p.nbp ? make_int2(b + 1, b + 2) : make_int2(-1, -1);
-    }
-  };
-  auto next_pair = [&](int q, int2 pr) { return pr.y < 0 ? make_int2(-1, -1) : pair_after(q, pr.y); };
-  auto w_start = [&](int sl) -> Walk {
-    if constexpr (kMasked) return Walk{pair_after(2 * sl, -1), pair_after(2 * sl + 1, -1), 0};
-    else return Walk{pair_after(0, -1), make_int2(-1, -1), 0};
-  };
-  auto w_tile = [&](const Walk& w) -> int2 {
-    if constexpr (kMasked) return (w.onB || w.pa.x < 0) ? w.pb : w.pa;
-    else return w.pa;
-  };
-  // the tile's owner: 0 = the slot's first query tile, 1 = its second, 2 = both
-  auto w_owner = [&](const Walk& w) -> int {
-    if constexpr (kMasked) return (w.onB || w.pa.x < 0) ? 1 : 0;
-    else return 2;
-  };
-  auto w_next = [&](int sl, Walk w) -> Walk {
-    if constexpr (kMasked) {
-      if (!w.onB && w.pa.x >= 0) {      // A's step was the tile: B's step of the same index next
-        if (w.pb.x >= 0) w.onB = 1;
-        else w.pa = next_pair(2 * sl, w.pa);
-      } else {                          // B's step was the tile: both move on
-        w.onB = 0;
-        w.pa = next_pair(2 * sl, w.pa);
-        w.pb = next_pair(2 * sl + 1, w.pb);
-      }
-    } else {
-      w.pa = next_pair(0, w.pa);
-    }
-    return w;
-  };
+  // KV tile t = blocks (2t, 2t + 1), for both slots and all their rows;
+  // x = -1 past the last tile.
+  const int ntiles = p.ntile;
+  auto tile_of = [&](int t) { return t < ntiles ? make_int2(2 * t, 2 * t + 1) : make_int2(-1, -1); };
 
-  // Number of KV tiles of each slot (the same in every role).
-  int nt0 = p.ntile, nt1 = p.ntile;
-  if constexpr (kMasked) {
-    auto steps = [&](int q) {
-      int nb = 0;
-      for (int w = 0; w < nkw && w < KEPT_WORDS; ++w) nb += __popc(kept_w[q * KEPT_WORDS + w]);
-      for (int u = 32 * KEPT_WORDS; u >= 0 && (u = next_kept_slow(p, bh, qt0 + q, u)) >= 0; ++u) ++nb;
-      return (nb + 1) >> 1;
-    };
-    nt0 = steps(0) + steps(1);
-    nt1 = steps(2) + steps(3);
-  }
-  auto nt = [&](int sl) { return sl ? nt1 : nt0; };
-  // K/V/mean stages: dense, one ring of NS shared by both slots; masked, two
-  // stages of its own per slot.
-  constexpr int SN = kMasked ? 2 : NS;
-
-  if (warp == WARP_TMA || (kMasked && warp == WARP_TMA + 1)) {
+  if (warp == WARP_TMA) {
     // ------------------------------------------------------------ producer
-    // Dense: warp 2 loads both Q tiles and the shared K/V ring.  Masked:
-    // warp 2 + s loads slot s's Q tile and its own two stages.
-    const int ps = kMasked ? warp - WARP_TMA : 0;  // the slot whose sequence is walked
-    const int sbase = kMasked ? 2 * ps : 0;
-    if (lane == 0 && !(p.debug_flags & 1) && nt(ps) > 0) {
+    // Warp 2 loads both Q tiles and the K/V ring that both slots share.
+    if (lane == 0 && !(p.debug_flags & 1) && ntiles > 0) {
       const int h3 = static_cast<int>(bh);
       const float* mu = p.vmu_op + bh * p.nbp * (4 * D);  // 2 KiB per block
-      // K of a tile: one 128-row box, or (masked) a 64-row box per block
-      auto load_k = [&](uint32_t dst, int2 pr, uint32_t b) {
-        tma_load_3d(dst, &tmk, 0, pr.x * BLK, h3, b);
-        if constexpr (kMasked) tma_load_3d(dst + TILE_BYTES / 2, &tmk, 0, (pr.y >= 0 ? pr.y : pr.x) * BLK, h3, b);
-      };
-      // V and the mean tile of a tile.  An empty second half is filled with
-      // the first block again (finite bytes; its P bytes and row sums are 0).
+      // K of a tile: one 128-row box
+      auto load_k = [&](uint32_t dst, int2 pr, uint32_t b) { tma_load_3d(dst, &tmk, 0, pr.x * BLK, h3, b); };
+      // V and the mean tile (blocks 2t and 2t+1 are adjacent) of a tile
       auto load_v = [&](int st, int2 pr, uint32_t b) {
         const uint32_t dv = sb + SM_V + st * V_STAGE, dm = sb + SM_MU + st * MU_BYTES;
         tma_load_3d(dv, &tmv, pr.x * BLK, 0, h3, b);
-        if constexpr (kMasked) {
-          const int y = pr.y >= 0 ? pr.y : pr.x;
-          tma_load_3d(dv + V_HALF, &tmv, y * BLK, 0, h3, b);
-          bulk_load(dm, mu + pr.x * (4 * D), MU_BYTES / 2, b);
-          bulk_load(dm + MU_BYTES / 2, mu + y * (4 * D), MU_BYTES / 2, b);
-        } else {
-          bulk_load(dm, mu + pr.x * (4 * D), MU_BYTES, b);
-        }
+        bulk_load(dm, mu + pr.x * (4 * D), MU_BYTES, b);
       };
       // Q and the first K tile
-      Walk wk = w_start(ps);
-      int2 pr = w_tile(wk);
-      const uint32_t qb = bar(B_QFULL + ps);
-      if constexpr (kMasked) {
-        mbar_arrive_expect_tx(qb, 2 * TILE_BYTES);
-        tma_load_3d(sb + SM_Q + ps * TILE_BYTES, &tmq, 0, q0 + 128 * ps, h3, qb);
-      } else {
-        mbar_arrive_expect_tx(qb, 3 * TILE_BYTES);
-        tma_load_3d(sb + SM_Q, &tmq, 0, q0, h3, qb);
-        tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, h3, qb);
-      }
-      load_k(sb + SM_K + sbase * TILE_BYTES, pr, qb);
+      int2 pr = tile_of(0);
+      const uint32_t qb = bar(B_QFULL);
+      mbar_arrive_expect_tx(qb, 3 * TILE_BYTES);
+      tma_load_3d(sb + SM_Q, &tmq, 0, q0, h3, qb);
+      tma_load_3d(sb + SM_Q + TILE_BYTES, &tmq, 0, q0 + 128, h3, qb);
+      load_k(sb + SM_K, pr, qb);
       // Test hook: with debug_flags >> 8 = n > 0 the producer stops after n
       // steps, as if its loads had stalled mid-stream.
       const int stop_after = p.debug_flags >> 8;
-      // the last step that armed each of this producer's stages (-1: none)
-      int armed[SN];
+      // the last step that armed each stage (-1: none)
+      int armed[NS];
 #pragma unroll
-      for (int u = 0; u < SN; ++u) armed[u] = -1;
-      // Step j brings V(j) and its mean tile into stage sbase + j % SN and
-      // K(j+1) into K stage sbase + (j+1) % SN, all on one barrier.  A K
-      // stage is free again once the QKs that read it were done, a V stage
-      // once the mean terms of its tile were issued (dense: both slots').
+      for (int u = 0; u < NS; ++u) armed[u] = -1;
+      // Step j brings V(j) and its mean tile into stage j % NS and K(j+1)
+      // into K stage (j+1) % NS, all on one barrier.  A K stage is free again
+      // once both slots' QKs that read it were done, a V stage once both
+      // slots' mean terms of its tile were issued.
       for (int j = 0; pr.x >= 0 && !*abort && !(stop_after > 0 && j >= stop_after); ++j) {
-        const int st = sbase + j % SN, stk = sbase + (j + 1) % SN;
-        const Walk wn = w_next(ps, wk);
-        const int2 pn = w_tile(wn);
-        if (j >= SN && !mbar_wait(bar(B_VEMPTY + st), ((j / SN) - 1) & 1, abort, WAIT_NS)) {
+        const int st = j % NS, stk = (j + 1) % NS;
+        const int2 pn = tile_of(j + 1);
+        if (j >= NS && !mbar_wait(bar(B_VEMPTY + st), ((j / NS) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
-        if (pn.x >= 0 && j + 1 >= SN &&
-            !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / SN) - 1) & 1, abort, WAIT_NS)) {
+        if (pn.x >= 0 && j + 1 >= NS &&
+            !mbar_wait(bar(B_KEMPTY + stk), (((j + 1) / NS) - 1) & 1, abort, WAIT_NS)) {
           record_timeout(p, abort);
           break;
         }
         mbar_arrive_expect_tx(bar(B_FULL + st), TILE_BYTES + MU_BYTES + (pn.x >= 0 ? TILE_BYTES : 0));
         load_v(st, pr, bar(B_FULL + st));
         if (pn.x >= 0) load_k(sb + SM_K + stk * TILE_BYTES, pn, bar(B_FULL + st));
-        armed[j % SN] = j;
+        armed[j % NS] = j;
         pr = pn;
-        wk = wn;
       }
       // Drain: every copy this producer issued has landed before the CTA can
       // exit, also when a consumer gave up and never waited for it.  A stage
@@ -479,9 +343,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // the abort flag).
       bool drained = mbar_wait_time(qb, 0, WAIT_NS);
 #pragma unroll
-      for (int u = 0; u < SN; ++u)
-        if (armed[u] >= 0)
-          drained &= mbar_wait_time(bar(B_FULL + sbase + u), (armed[u] / SN) & 1, WAIT_NS);
+      for (int u = 0; u < NS; ++u)
+        if (armed[u] >= 0) drained &= mbar_wait_time(bar(B_FULL + u), (armed[u] / NS) & 1, WAIT_NS);
       if (!drained) record_timeout(p, abort);
     }
   } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
@@ -489,15 +352,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // One issuing lane per slot, so that one slot's waits never hold back
     // the other slot's MMAs; tcgen05.commit tracks each lane's own MMAs.
     const int s = warp - WARP_MMA;
-    const int ntiles = nt(s), nother = nt(1 - s);
-    const int sbase = kMasked ? 2 * s : 0;  // this slot's stages: sbase + j % SN
     if (lane == 0 && ntiles > 0) {
-      bool ok = mbar_wait(bar(B_QFULL + (kMasked ? s : 0)), 0, abort, WAIT_NS);
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort, WAIT_NS);
       tc_fence_after();
       // Descriptors are built once; a byte offset o advances them by o >> 4
       // in the start-address field (all of shared memory is below 256 KiB).
       const uint64_t dQ = sdesc_sw128(sb + SM_Q + s * TILE_BYTES), dK = sdesc_sw128(sb + SM_K);
-      const uint64_t dV = kMasked ? sdesc_sw64(sb + SM_V) : sdesc_sw128(sb + SM_V);
+      const uint64_t dV = sdesc_sw128(sb + SM_V);
       const uint64_t dL = sdesc_k8_tf32(sb + SM_L + s * MU_BYTES);
       // mean tile: K-slots 0..3 (block of the first half) and 4..7 (second
       // half) are two 2 KiB parts of 16-byte rows, one row per channel
@@ -510,7 +371,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = mbar_wait(bar(b), par, abort, WAIT_NS);
         tc_fence_after();
       };
-      auto stg = [&](int j) { return sbase + j % SN; };
+      auto stg = [](int j) { return j % NS; };
       // S of this slot for its j-th tile
       auto qk = [&](int j) {
 #pragma unroll
@@ -520,12 +381,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_commit(bar(B_KEMPTY + stg(j)));  // this slot has read K(j)
       };
       // The single S buffer is taken in turn: S0(0) S1(0) S0(1) S1(1) ...
-      // while both slots have tiles, then the slot with more goes on alone.
-      // QK of slot 0 for tile i waits until slot 1 holds S(i-1) (or, once
-      // slot 1 is done, until slot 0 holds its own S(i-1)); QK of slot 1
-      // until slot 0 holds S(i) (once slot 0 is done: its own S(i-1)).
-      // Dense, both slots have the same count.  Each QK goes ahead of the PV
-      // that the same slot's softmax releases later.
+      // QK of slot 0 for tile i waits until slot 1 holds S(i-1); QK of slot 1
+      // until slot 0 holds S(i).  Each QK goes ahead of the PV that the same
+      // slot's softmax releases later.
       auto pv = [&](int j) {  // mean term of tile j-1, then [O | l] += P(j) [V ; 1_b0 ; 1_b1]
         wt(B_PFULL + s, j & 1);  // P(j), and for j > 0 the mean operand of j-1
         if (!ok) return;
@@ -534,30 +392,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma_commit(bar(B_VEMPTY + stg(j - 1)));  // this slot is done with V(j-1)
         }
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t vo = kMasked ? (kk >> 1) * V_HALF + 32 * (kk & 1) : 32 * kk;
-          mma_f8(dO, adv(dP, 32 * kk), adv(dV, stg(j) * V_STAGE + vo), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8(dO, adv(dP, 32 * kk), adv(dV, stg(j) * V_STAGE + 32 * kk), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_ODONE + s));
       };
       for (int i = 0; ok && i <= ntiles; ++i) {
         if (i < ntiles) {
           // K(i) came with Q (i = 0) or with V(i-1)
-          if (i > 0) wt(B_FULL + stg(i - 1), ((i - 1) / SN) & 1);
+          if (i > 0) wt(B_FULL + stg(i - 1), ((i - 1) / NS) & 1);
           if (s == 0) {
-            if (i > 0) wt(B_STAKEN + (i - 1 < nother ? 1 : 0), (i - 1) & 1);
+            if (i > 0) wt(B_STAKEN + 1, (i - 1) & 1);
           } else {
-            if (i < nother) {
-              wt(B_STAKEN + 0, i & 1);
-            } else if (i > 0) {
-              wt(B_STAKEN + 1, (i - 1) & 1);
-            }
+            wt(B_STAKEN + 0, i & 1);
           }
           if (!ok) break;
           qk(i);
         }
         if (i > 0) {
-          if (i == ntiles) wt(B_FULL + stg(i - 1), ((i - 1) / SN) & 1);  // V of the last tile
+          if (i == ntiles) wt(B_FULL + stg(i - 1), ((i - 1) / NS) & 1);  // V of the last tile
           pv(i - 1);
         }
       }
@@ -618,28 +470,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int i = 0;
     // block scales of a tile
     auto pair_scales = [&](int2 pr) -> float2 {
-      if (pr.x < 0) return make_float2(0.0f, 0.0f);
-      if constexpr (kMasked) return make_float2(ksc[pr.x], pr.y >= 0 ? ksc[pr.y] : 0.0f);
-      else return *reinterpret_cast<const float2*>(ksc + pr.x);
+      return pr.x < 0 ? make_float2(0.0f, 0.0f) : *reinterpret_cast<const float2*>(ksc + pr.x);
     };
-    const int ntiles = nt(slot);
-    const int my_tile = r >> 6;  // masked: the row's query tile within the slot (0 = A, 1 = B)
-    Walk wk = w_start(slot);
-    int2 pr = w_tile(wk);
-    int owner = w_owner(wk);
+    int2 pr = tile_of(0);
     // loaded one tile ahead
     float2 ks = pair_scales(pr);
     for (; pr.x >= 0; ++i) {
-      const Walk wn = w_next(slot, wk);
-      const int2 pn = w_tile(wn);
-      const int owner_n = w_owner(wn);
+      const int2 pn = tile_of(i + 1);
       const float2 ks_n = pair_scales(pn);
-      // a tile that another query tile owns is absent for this row
-      const bool mine = !kMasked || owner == my_tile;
-      const bool keep0 = row_ok && mine;
-      const bool keep1 = row_ok && mine && pr.y >= 0;
+      const bool keep0 = row_ok;
+      const bool keep1 = row_ok;
       // Score column j of the tile is a valid key iff j < lim_lo (first
-      // half) or j < lim_hi (second half); dense, both are N - 128 t.
+      // half) or j < lim_hi (second half); both are N - 128 t.
       const int n32 = static_cast<int>(p.N);
       const int lim_lo = n32 - pr.x * BLK;
       const int lim_hi = pr.y >= 0 ? BLK + n32 - pr.y * BLK : BLK;
@@ -776,8 +618,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
       pr = pn;
-      wk = wn;
-      owner = owner_n;
       ks = ks_n;
     }
     // the last tile's row sums, then its mean term
@@ -1494,9 +1334,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   static PerDevice attr;
   int dev = 0;
   const cudaError_t ea = per_device_setup(attr, &dev, [](int, int*) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_MASKED);
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(sp::attn_sparse, cudaFuncAttributeMaxDynamicSharedMemorySize, sp::SMEM_BYTES);
     return e;
@@ -1507,7 +1345,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     sp::attn_sparse<<<grid, sp::NTHREADS, sp::SMEM_BYTES, s>>>(mq, mk, mv, p);
   } else {
     const dim3 grid(static_cast<unsigned>(ceil_div(Np, CTA_ROWS)), static_cast<unsigned>(a.BH));
-    attn_fwd<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+    attn_fwd<<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
   }
   return cudaGetLastError();
 }
