@@ -292,7 +292,8 @@ def run_ours(args):
         "prep_hbm_frac": round(prep_gbs / pk["hbm"], 4),
         "kmeans_tflops": round(kmeans_flop / (t_group * 1e-3) / 1e12, 2),
         "group_pct_of_attn": round(100 * t_group / t_attn, 2),
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd", "achieved": round(attn_tflops, 2),
+        "roofline": {"bound": "tensor", "kernel": "attn_sparse" if w.sparse else "attn_fwd",
+                     "achieved": round(attn_tflops, 2),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(attn_tflops / fp8_peak, 4),
                      "peak_source": "%s bf16 burst x %.0f (nominal FP8/bf16 ratio)" % (pk["src"], FP8_OVER_BF16),

@@ -708,9 +708,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // query tile's steps, as in the two-slot kernel; the tensor cores do no work
 // for another tile's rows beyond the zero quadrants of P.
 //
-// Warp 0 issues the MMAs from one lane and allocates TMEM (512 columns: S
-// [0,256), O [256,400)); warp 1 issues the TMA loads through two stages
-// (stage j: V(j), its mean tiles and K(j+1), on one barrier); warps 4-7 run
+// Warp 0 issues the QKs from one lane and allocates TMEM (512 columns: S
+// [0,256), O [256,400)), warp 2 issues the mean and PV MMAs from one lane,
+// warp 1 issues the TMA loads through three rings (K and V of two stages,
+// the mean tiles of three, each with barriers of its own), and warps 4-7 run
 // the softmax, thread = row = TMEM lane.  The single S buffer is taken by
 // the next QK as soon as the softmax holds S in registers.
 namespace sp {
