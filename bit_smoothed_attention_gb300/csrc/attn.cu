@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // the softmax, thread = row = TMEM lane.  The single S buffer is taken by
 // the next QK as soon as the softmax holds S in registers.
 namespace sp {
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 384;
 constexpr int WARP_MMA = 0, WARP_TMA = 1, WARP_PV = 2, WARP_SOFTMAX = 4;
 constexpr int NS = 2;   // K and V stages
 constexpr int NM = 3;   // mean-tile stages
@@ -735,7 +735,8 @@ constexpr uint32_t SM_MU = SM_V + NS * V_STAGE;
 constexpr uint32_t SM_L = SM_MU + NM * MU_STAGE;
 constexpr uint32_t SM_P = SM_L + 2 * L_BYTES;      // P tile 0 (keys of A), P tile 1 (keys of B)
 constexpr uint32_t SM_KEPT = SM_P + 2 * TILE_BYTES;
-constexpr uint32_t SM_BAR = SM_KEPT + 2 * 4 * KEPT_WORDS;
+constexpr uint32_t SM_XCH = SM_KEPT + 2 * 4 * KEPT_WORDS;  // softmax exchange, [2][2][128] floats
+constexpr uint32_t SM_BAR = SM_XCH + 2 * 2 * 128 * 4;
 enum {
   B_QFULL = 0,
   B_KFULL,
@@ -750,7 +751,8 @@ enum {
   B_ODONE,
   B_MDONE,
   B_FIN,
-  NBAR
+  B_XCH,  // + 2 * quarter + step parity
+  NBAR = B_XCH + 8
 };
 constexpr uint32_t SM_TSLOT = SM_BAR + NBAR * 8;
 constexpr uint32_t SM_ABORT = SM_TSLOT + 8;
@@ -785,11 +787,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_MEMPTY + s), 1);
     }
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_STAKEN), 4);
-    mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_STAKEN), 8);
+    mbar_init(bar(B_PFULL), 8);
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_MDONE), 1);
     mbar_init(bar(B_FIN), 2);  // both issuing lanes
+    for (int q = 0; q < 8; ++q) mbar_init(bar(B_XCH + q), 2);  // the two warps of a row quarter
     *abort = 0;
     mbar_fence_init();
   }
@@ -1026,120 +1029,116 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp >= WARP_SOFTMAX) {
     // ------------------------------------------------------ softmax warps
+    // Two threads per row: warps 4-7 take each row's first block (S columns
+    // 0-63 of its tile), warps 8-11 its second (64-127).  The two exchange
+    // their block maxima through shared memory (a barrier per quarter and
+    // step parity, waited with a time limit), so both take the same running
+    // maximum; each casts, writes and sums its own block.
     const int wq = warp & 3;
+    const int hf = (warp - WARP_SOFTMAX) >> 2;  // 0: first block of the step, 1: second
     const int r = wq * 32 + lane;
     const int my_tile = r >> 6;  // 0: A, 1: B (warp-uniform)
     const int64_t row = static_cast<int64_t>(q0) + r;
     const bool row_ok = row < p.N;
     const int qt = static_cast<int>(row >> 6);
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + COL_S + 128 * my_tile;
+    const uint32_t tS = tmem + lane_addr + COL_S + 128 * my_tile + 64 * hf;
     const uint32_t tO = tmem + lane_addr + COL_O;
-    const uint32_t tL = tO + 128 + 2 * my_tile;  // this tile's two row-sum columns
+    const uint32_t tL = tO + 128 + 2 * my_tile + hf;  // this block's row-sum column
     uint8_t* Prow = sm + SM_P + my_tile * TILE_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
-    uint8_t* Lrow = sm + SM_L + my_tile * L_BYTES + (r >> 3) * 256 + (r & 7) * 16;
+    uint8_t* Lrow = sm + SM_L + my_tile * L_BYTES + (r >> 3) * 256 + (r & 7) * 16 + 128 * hf;
+    float* xch = reinterpret_cast<float*>(sm + SM_XCH);  // [step parity][half][row]
     const float qsc = p.q_scale[bh * p.nbp + (qt < p.nbp ? qt : p.nbp - 1)];
     const float a_i = p.c0 * qsc;
     const float* ksc = p.k_scale + bh * p.nbp;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const uint32_t FULL = 0xffffffffu;
-    auto ld_rowsums = [&](float& l0, float& l1) {
-      uint32_t ls0, ls1;
-      asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(ls0), "=r"(ls1) : "r"(tL));
-      tmem_wait_ld();
-      l0 = __uint_as_float(ls0);
-      l1 = __uint_as_float(ls1);
+    // the partner thread's value for exchange round k (a step, or nst for l)
+    auto exchange = [&](int k, float v, float& other) -> bool {
+      xch[((k & 1) * 2 + hf) * 128 + r] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_XCH + 2 * wq + (k & 1)));
+      if (!__all_sync(FULL, mbar_wait(bar(B_XCH + 2 * wq + (k & 1)), (k >> 1) & 1, abort, WAIT_NS))) return false;
+      other = xch[((k & 1) * 2 + (1 - hf)) * 128 + r];
+      return true;
     };
-    // tf32 A operand row of this tile's mean MMA, [hi0, lo0, hi0, 0 | hi1,
-    // lo1, hi1, 0] against the mean tiles' (hi, hi, lo, 0) of its two blocks
-    auto put_lrow = [&](float v0, float v1) {
-      const float h0 = to_tf32(v0), h1 = to_tf32(v1);
-      const float g0 = to_tf32(v0 - h0), g1 = to_tf32(v1 - h1);
-      *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, 0.0f);
-      *reinterpret_cast<float4*>(Lrow + 128) = make_float4(h1, g1, h1, 0.0f);
-      fence_proxy_async_smem();
+    auto ld_rowsum = [&]() {
+      uint32_t ls;
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(ls) : "r"(tL));
+      tmem_wait_ld();
+      return __uint_as_float(ls);
+    };
+    // this block's tf32 part of the row of the tile's mean MMA, [hi, lo, hi,
+    // 0] against the mean tile's (hi, hi, lo, 0)
+    auto put_lrow = [&](float v) {
+      const float h = to_tf32(v);
+      const float g = to_tf32(v - h);
+      *reinterpret_cast<float4*>(Lrow) = make_float4(h, g, h, 0.0f);
     };
     float m_run = NEG_INF;
-    float l = 0.0f;
+    float lh = 0.0f;  // this block's share of the row sum
     bool ok = true;
     int2 pr = pair_after(my_tile, -1);  // this row's tile's current step (x = -1: none)
     int i = 0;
     for (; i < nst; ++i) {
       const int2 pn = pr.x >= 0 ? next_pair(my_tile, pr) : pr;
-      const bool keep0 = row_ok && pr.x >= 0;
-      const bool keep1 = row_ok && pr.y >= 0;
+      const int blk = hf ? pr.y : pr.x;
+      const bool keep = row_ok && blk >= 0;
       const int n32 = static_cast<int>(p.N);
-      const int lim_lo = pr.x >= 0 ? n32 - pr.x * BLK : BLK;
-      const int lim_hi = pr.y >= 0 ? BLK + n32 - pr.y * BLK : TILE;
-      const float A0 = pr.x >= 0 ? a_i * ksc[pr.x] : 0.0f;
-      const float A1 = pr.y >= 0 ? a_i * ksc[pr.y] : 0.0f;
-      const bool partial = !__all_sync(FULL, lim_lo >= BLK && lim_hi >= TILE);
+      const int lim = blk >= 0 ? n32 - blk * BLK : BLK;  // keys of the block before N
+      const float A = blk >= 0 ? a_i * ksc[blk] : 0.0f;
+      const bool partial = !__all_sync(FULL, lim >= BLK);
 
       if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL), i & 1, abort, WAIT_NS)))) break;
       tc_fence_after();
-      float x[128];
-      uint32_t w[32];
-      float m_new, alpha;
-      bool resc;
+      float x[64];
+      uint32_t w[16];
       {
-        {
-          uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
-          uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
-          uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
-          uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
-          tmem_ld32(tS + 0, c0);
-          tmem_ld32(tS + 32, c1);
-          tmem_ld32(tS + 64, c2);
-          tmem_ld32(tS + 96, c3);
-          tmem_wait_ld();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_STAKEN));  // S may be overwritten
-        if (partial) {
+        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
+        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
+        tmem_ld32(tS + 0, c0);
+        tmem_ld32(tS + 32, c1);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_STAKEN));  // S may be overwritten
+      if (partial) {
 #pragma unroll
-          for (int j = 0; j < 128; ++j) x[j] = j < (j < 64 ? lim_lo : lim_hi) ? x[j] : NEG_INF;
-        }
-        float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
-        float mc = fmax3(x[64], x[65], x[66]), md = fmax3(x[96], x[97], x[98]);
+        for (int j = 0; j < 64; ++j) x[j] = j < lim ? x[j] : NEG_INF;
+      }
+      float ma = fmax3(x[0], x[1], x[2]), mb = fmax3(x[32], x[33], x[34]);
 #pragma unroll
-        for (int j = 3; j < 31; j += 2) {
-          ma = fmax3(ma, x[j], x[j + 1]);
-          mb = fmax3(mb, x[32 + j], x[33 + j]);
-          mc = fmax3(mc, x[64 + j], x[65 + j]);
-          md = fmax3(md, x[96 + j], x[97 + j]);
-        }
-        const float mx0 = fmax3(ma, mb, fmaxf(x[31], x[63]));
-        const float mx1 = fmax3(mc, md, fmaxf(x[95], x[127]));
-        const float m_tile = fmaxf(keep0 ? A0 * mx0 : NEG_INF, keep1 ? A1 * mx1 : NEG_INF);
-        const bool need = m_tile > m_run + p.tau8;
-        m_new = need ? m_tile : m_run;
-        const bool live = m_new != NEG_INF;
-        resc = need && m_run != NEG_INF;
-        alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
-        if (partial) {
+      for (int j = 3; j < 31; j += 2) {
+        ma = fmax3(ma, x[j], x[j + 1]);
+        mb = fmax3(mb, x[32 + j], x[33 + j]);
+      }
+      const float mine = keep ? A * fmax3(ma, mb, fmaxf(x[31], x[63])) : NEG_INF;
+      float other;
+      if (!(ok = exchange(i, mine, other))) break;
+      const float m_tile = hf ? fmaxf(other, mine) : fmaxf(mine, other);
+      const bool need = m_tile > m_run + p.tau8;
+      const float m_new = need ? m_tile : m_run;
+      const bool live = m_new != NEG_INF;
+      const bool resc = need && m_run != NEG_INF;
+      const float alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
+      if (partial) {
 #pragma unroll
-          for (int j = 0; j < 128; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
-        }
-        const bool k0 = live && keep0, k1 = live && keep1;
-        const float Bq = (p.C - m_new) * 0.00390625f;
-        const float A0q = k0 ? A0 * 0.00390625f : 0.0f, B0q = k0 ? Bq : 0.0f;
-        const float A1q = k1 ? A1 * 0.00390625f : 0.0f, B1q = k1 ? Bq : 0.0f;
+        for (int j = 0; j < 64; ++j) x[j] = x[j] == NEG_INF ? 0.0f : x[j];
+      }
+      const bool k = live && keep;
+      const float Aq = k ? A * 0.00390625f : 0.0f, Bq = k ? (p.C - m_new) * 0.00390625f : 0.0f;
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], q < 16 ? A0q : A1q,
-                          q < 16 ? B0q : B1q);
-        if (partial) {
-          const int lim0 = k0 ? (lim_lo < 64 ? lim_lo : 64) : 0;
-          const int lim1 = k1 ? (lim_hi < 128 ? lim_hi : 128) : 64;
+      for (int q = 0; q < 16; ++q) w[q] = expcast4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3], Aq, Bq);
+      if (partial) {
+        const int lim_k = k ? (lim < 64 ? lim : 64) : 0;
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            uint32_t keep = 0;
+        for (int q = 0; q < 16; ++q) {
+          uint32_t keepb = 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (4 * q + e < (q < 16 ? lim0 : lim1)) keep |= 0xFFu << (8 * e);
-            w[q] &= keep;
-          }
+          for (int e = 0; e < 4; ++e)
+            if (4 * q + e < lim_k) keepb |= 0xFFu << (8 * e);
+          w[q] &= keepb;
         }
       }
       m_run = m_new;
@@ -1149,38 +1148,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!(ok = __all_sync(FULL, mbar_wait(bar(B_ODONE), (i - 1) & 1, abort, WAIT_NS)))) break;
         tc_fence_after();
       }
-      // row r of this tile's P: 128 bytes, 16-byte chunk c at position c ^ (r & 7)
+      // this block's 64 bytes of row r of the tile's P: 16-byte chunk c at
+      // position c ^ (r & 7)
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(Prow + ((c ^ (r & 7)) << 4)) =
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(Prow + (((4 * hf + c) ^ (r & 7)) << 4)) =
             make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       if (i > 0) {
-        // Row sums of step i-1: read and cleared, so that PV(i) accumulates
-        // its own.  If the maximum moved, O and l move to the new maximum,
-        // and the mean operand of step i-1 is written already scaled.
-        float l0, l1;
-        ld_rowsums(l0, l1);
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(tL), "r"(0u), "r"(0u)
-                     : "memory");
+        // The block's row sum of step i-1: read and cleared, so that PV(i)
+        // accumulates its own.  If the maximum moved, this thread's half of
+        // O and its share of l move to the new maximum, and its part of the
+        // mean operand of step i-1 is written already scaled.
+        const float ls = ld_rowsum();
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tL), "r"(0u) : "memory");
         if (__any_sync(FULL, resc)) {
           uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
           uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
-          uint32_t (&o2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
-          uint32_t (&o3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
-          tmem_ld32(tO + 0, o0);
-          tmem_ld32(tO + 32, o1);
-          tmem_ld32(tO + 64, o2);
-          tmem_ld32(tO + 96, o3);
+          tmem_ld32(tO + 64 * hf, o0);
+          tmem_ld32(tO + 64 * hf + 32, o1);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 128; ++e) x[e] *= alpha;
-          tmem_st32(tO + 0, o0);
-          tmem_st32(tO + 32, o1);
-          tmem_st32(tO + 64, o2);
-          tmem_st32(tO + 96, o3);
+          for (int e = 0; e < 64; ++e) x[e] *= alpha;
+          tmem_st32(tO + 64 * hf, o0);
+          tmem_st32(tO + 64 * hf + 32, o1);
         }
-        l = (l + (l0 + l1)) * alpha;
-        put_lrow(l0 * alpha, l1 * alpha);
+        lh = (lh + ls) * alpha;
+        put_lrow(ls * alpha);
       }
       fence_proxy_async_smem();
       tmem_wait_st();
@@ -1189,30 +1182,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(bar(B_PFULL));
       pr = pn;
     }
-    // the last step's row sums, then its mean terms
+    // the last step's row sums, then its mean terms, then the row sum of
+    // both blocks
+    float l = 0.0f;
     if (ok && nst > 0) {
       ok = __all_sync(FULL, mbar_wait(bar(B_ODONE), (nst - 1) & 1, abort, WAIT_NS));
       if (ok) {
         tc_fence_after();
-        float l0, l1;
-        ld_rowsums(l0, l1);
-        l += l0 + l1;
-        put_lrow(l0, l1);
+        const float ls = ld_rowsum();
+        lh += ls;
+        put_lrow(ls);
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_PFULL));
         ok = __all_sync(FULL, mbar_wait(bar(B_MDONE), 0, abort, WAIT_NS));
         tc_fence_after();
       }
+      float lo_ = 0.0f;
+      if (ok && (ok = exchange(nst, lh, lo_))) l = hf ? lo_ + lh : lh + lo_;
     }
     if (!ok) record_timeout(p, abort);
 
     // ------------------------------------------------------------ epilogue
+    // this thread's 64 output channels, 64 hf .. 64 hf + 63
     const bool have = ok && nst > 0;
     if (__all_sync(0xffffffffu, have)) {
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
         uint32_t o[32];
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
@@ -1239,12 +1238,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     } else if (row_ok && nst == 0) {
-      const int nvec = p.out_f32 ? 32 : 16;
+      // this thread's half of the row: 64 channels
+      const int nvec = p.out_f32 ? 16 : 8;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.O) +
-                                            (p.lo.head(bh) + p.lo.row(row)) * (p.out_f32 ? 4 : 2));
+                                            (p.lo.head(bh) + p.lo.row(row) + 64 * hf) * (p.out_f32 ? 4 : 2));
       for (int e = 0; e < nvec; ++e) dst[e] = make_uint4(0, 0, 0, 0);
     }
-    if (row_ok && p.lse2) {
+    if (row_ok && p.lse2 && hf == 0) {
       p.lse2[bh * p.N + row] = l > 0.0f
           ? m_run * 0.125f - p.off + log2f(l) + p.qmu[bh * p.N + row] * p.lse_qmu
           : -__int_as_float(0x7f800000);
