@@ -233,3 +233,40 @@ def test_sparse_full_size(vc, orc):
             assert np.array_equal(views[key][h].cpu().numpy(), opp[key][0]), key
         _check_head(orc, O32[0, h].cpu().numpy(), L[0, h].cpu().numpy(), Qb, Kb, Vb, opp, sm, qidx,
                     mask_h=m[0, h], perm_h=op[0])
+
+
+def test_sparse_beyond_kept_bitmask(vc, orc):
+    """A sequence longer than the kernel's shared-memory bitmask of kept
+    blocks (112 words per query tile, 3584 blocks): blocks past it are read
+    from the mask itself.  One query tile keeps only blocks past the bitmask
+    (among them the partial last block of the sequence), one only blocks
+    before it, one straddles it; the sampled rows of every kind match both
+    oracles."""
+    N, H, k = 245000, 1, 64
+    w = W.WORKLOADS["sparse"]
+    sm = float(np.float32(w.sm_scale))
+    Q, K, V = W.make_qkv(1, H, N, k, 1450, device="cuda")
+    nq, nbp = (N + 63) // 64, vc.npad(N) // 64
+    assert nbp > 32 * 112
+    mask = W.make_tile_mask(1, H, N, 1451)
+    m = mask.numpy()
+    m[0, 0, 1, :] = 0
+    m[0, 0, 1, [3600, 3650, 3700, (N - 1) // 64]] = 1   # only past the bitmask; the last block is partial
+    m[0, 0, 2, :] = 0
+    m[0, 0, 2, [5, 700, 3583]] = 1                       # only before it
+    m[0, 0, 3, :] = 0
+    m[0, 0, 3, [3000, 3583, 3584, 3800]] = 1             # across it
+    mask = torch.from_numpy(m)
+    labels, perm = vc.group(V, k, 5)
+    pp = vc.prep(Q, K, V, perm)
+    O32, L = vc.attn(pp, sm, mask=mask.cuda(), out_f32=True)
+    torch.cuda.synchronize()
+    assert vc.last_device_error() == 0
+    qidx = np.unique(np.concatenate([W.evenly_spaced_queries(N), [64, 100, 127, 128, 191, 192, 255]]))
+    Qb, Kb, Vb = (_head_bits(t, 0) for t in (Q, K, V))
+    ol, _ = orc.kmeans(Vb, k, 5)
+    op = orc.stable_sort(ol, k)
+    assert np.array_equal(perm[0, 0].cpu().numpy(), op[0])
+    opp = orc.prep(Qb, Kb, Vb, op)
+    _check_head(orc, O32[0, 0].cpu().numpy(), L[0, 0].cpu().numpy(), Qb, Kb, Vb, opp, sm, qidx,
+                mask_h=m[0, 0], perm_h=op[0])
