@@ -43,6 +43,7 @@ def _L():
         lib.orc_stable_sort.argtypes = [P, i64, i64, i32, P]
         lib.orc_prep.argtypes = [P, P, P, P, i64, i64] + [P] * 9
         lib.orc_prep_ex.argtypes = [P, P, P, P, i64, i64, i32] + [P] * 9
+        lib.orc_prep_ties.argtypes = [P, P, P, P, i64, i64, i32] + [P] * 10
         lib.orc_hadamard128.argtypes = [P, P, i64]
         lib.orc_attn_emul.argtypes = [P] * 8 + [i64, f32, i32, f32, P, P, i64, i32, P, P]
         lib.orc_attn_dense.argtypes = [P, P, P, i64, f32, P, P, P, i64, P, P]
@@ -164,12 +165,13 @@ def hadamard128(x):
     return y
 
 
-def prep(Q, K, V, perm=None, flags=0):
+def prep(Q, K, V, perm=None, flags=0, count_ties=False):
     """Preprocessing of all heads.  Returns a dict of numpy arrays:
     q8, k8 [BH, Npad, 128] u8; r8t [BH, 128, Npad] u8; q_scale, k_scale
     [BH, Npad/64]; v_scale, k_mean [BH, 128]; v_mean [BH, Npad/64, 128]; qmu [BH, N].
     flags & PREP_QK_HADAMARD: Q and centred K rotated by the Hadamard transform
-    before their quantisers."""
+    before their quantisers.  count_ties: also "ties" [BH, 3] int64, the E4M3
+    rounding ties among the quantiser inputs of Q, K and the V residual."""
     Q, K, V = (_c(t, np.uint16) for t in (Q, K, V))
     BH, N, _ = Q.shape
     Np = npad(N)
@@ -182,10 +184,15 @@ def prep(Q, K, V, perm=None, flags=0):
         v_mean=np.empty((BH, nbp, D), np.float32), qmu=np.empty((BH, N), np.float32))
     if perm is not None:
         perm = _c(perm, np.int32)
-    rc = _L().orc_prep_ex(_p(Q), _p(K), _p(V), _p(perm), BH, N, int(flags),
-                       _p(out["q8"]), _p(out["k8"]), _p(out["r8t"]),
-                       _p(out["q_scale"]), _p(out["k_scale"]), _p(out["v_scale"]),
-                       _p(out["k_mean"]), _p(out["v_mean"]), _p(out["qmu"]))
+    args = (_p(Q), _p(K), _p(V), _p(perm), BH, N, int(flags),
+            _p(out["q8"]), _p(out["k8"]), _p(out["r8t"]),
+            _p(out["q_scale"]), _p(out["k_scale"]), _p(out["v_scale"]),
+            _p(out["k_mean"]), _p(out["v_mean"]), _p(out["qmu"]))
+    if count_ties:
+        out["ties"] = np.zeros((BH, 3), np.int64)
+        rc = _L().orc_prep_ties(*args, _p(out["ties"]))
+    else:
+        rc = _L().orc_prep_ex(*args)
     if rc:
         raise ValueError("orc_prep: bad arguments")
     return out

@@ -315,7 +315,7 @@ int orc_stable_sort(const int32_t* labels, int64_t BH, int64_t N, int k, int32_t
 #define AMAX_FLOOR 7.888609052210118e-31f /* 2^-100 */
 
 static void quant_block(const float* x, int64_t rows, int64_t stride, int64_t cols,
-                        uint8_t* out, int64_t ostride, float* scale) {
+                        uint8_t* out, int64_t ostride, float* scale, int64_t* ties) {
   float amax = 0.0f;
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < cols; ++c) {
@@ -329,7 +329,11 @@ static void quant_block(const float* x, int64_t rows, int64_t stride, int64_t co
   }
   float inv = 448.0f / amax;
   for (int64_t r = 0; r < rows; ++r)
-    for (int64_t c = 0; c < cols; ++c) out[r * ostride + c] = orc_e4m3_encode(x[r * stride + c] * inv);
+    for (int64_t c = 0; c < cols; ++c) {
+      const float y = x[r * stride + c] * inv;
+      out[r * ostride + c] = orc_e4m3_encode(y);
+      if (ties) *ties += orc_e4m3_is_tie(y);
+    }
   *scale = amax / 448.0f;
 }
 
@@ -361,11 +365,13 @@ void orc_hadamard128(const float* x, float* y, int64_t rows) {
 
 #define ORC_PREP_QK_HADAMARD 1
 
-int orc_prep_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
-                int64_t BH, int64_t N, int flags,
-                uint8_t* q8, uint8_t* k8, uint8_t* r8t,
-                float* q_scale, float* k_scale, float* v_scale,
-                float* k_mean, float* v_mean, float* qmu) {
+/* ties (nullable): [BH][3] counts of E4M3 rounding ties (R15) among the
+ * quantiser inputs fl(x * inv) of Q, K and the V residual of each head. */
+static int prep_impl(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+                     int64_t BH, int64_t N, int flags,
+                     uint8_t* q8, uint8_t* k8, uint8_t* r8t,
+                     float* q_scale, float* k_scale, float* v_scale,
+                     float* k_mean, float* v_mean, float* qmu, int64_t* ties) {
   const int rot = (flags & ORC_PREP_QK_HADAMARD) != 0;
   if (N < 1) return 1;
   const int64_t Npad = ((N + ORC_TILE - 1) / ORC_TILE) * ORC_TILE;
@@ -388,6 +394,8 @@ int orc_prep_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const i
     float* vs = v_scale + bh * ORC_D;
     float* km = k_mean + bh * ORC_D;
     float* vm = v_mean + bh * nbp * ORC_D;
+    int64_t* tq = ties ? ties + 3 * bh : NULL;
+    if (tq) tq[0] = tq[1] = tq[2] = 0;
     memset(Q8, 0, (size_t)Npad * ORC_D);
     memset(K8, 0, (size_t)Npad * ORC_D);
     memset(R8t, 0, (size_t)Npad * ORC_D);
@@ -426,7 +434,7 @@ int orc_prep_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const i
       }
     for (int64_t b = 0; b < nb; ++b) {
       int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
-      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, Q8 + r0 * ORC_D, ORC_D, &qs[b]);
+      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, Q8 + r0 * ORC_D, ORC_D, &qs[b], tq ? tq + 0 : NULL);
     }
 
     /* K: gathered by perm, centred, (rotated,) per-block scale. */
@@ -440,7 +448,7 @@ int orc_prep_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const i
     }
     for (int64_t b = 0; b < nb; ++b) {
       int64_t r0 = b * ORC_BLK, rows = (N - r0) < ORC_BLK ? (N - r0) : ORC_BLK;
-      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, K8 + r0 * ORC_D, ORC_D, &ks[b]);
+      quant_block(xf + r0 * ORC_D, rows, ORC_D, ORC_D, K8 + r0 * ORC_D, ORC_D, &ks[b], tq ? tq + 1 : NULL);
     }
 
     /* V: gathered by perm; block means; residual; per-channel scale. */
@@ -465,13 +473,37 @@ int orc_prep_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const i
       }
       if (!(amax >= AMAX_FLOOR)) { vs[d] = 1.0f; continue; }  /* bytes stay 0 */
       float inv = 448.0f / amax;
-      for (int64_t j = 0; j < N; ++j) R8t[d * Npad + j] = orc_e4m3_encode(xf[j * ORC_D + d] * inv);
+      for (int64_t j = 0; j < N; ++j) {
+        const float y = xf[j * ORC_D + d] * inv;
+        R8t[d * Npad + j] = orc_e4m3_encode(y);
+        if (tq) tq[2] += orc_e4m3_is_tie(y);
+      }
       vs[d] = amax / 448.0f;
     }
     free(tmp);
     free(xf);
   }
   return 0;
+}
+
+int orc_prep_ex(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+                int64_t BH, int64_t N, int flags,
+                uint8_t* q8, uint8_t* k8, uint8_t* r8t,
+                float* q_scale, float* k_scale, float* v_scale,
+                float* k_mean, float* v_mean, float* qmu) {
+  return prep_impl(Q, K, V, perm, BH, N, flags, q8, k8, r8t, q_scale, k_scale, v_scale, k_mean, v_mean,
+                   qmu, NULL);
+}
+
+/* As orc_prep_ex, also counting the E4M3 rounding ties of each head's
+ * quantisers into ties[BH][3] (Q, K, V residual). */
+int orc_prep_ties(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,
+                  int64_t BH, int64_t N, int flags,
+                  uint8_t* q8, uint8_t* k8, uint8_t* r8t,
+                  float* q_scale, float* k_scale, float* v_scale,
+                  float* k_mean, float* v_mean, float* qmu, int64_t* ties) {
+  return prep_impl(Q, K, V, perm, BH, N, flags, q8, k8, r8t, q_scale, k_scale, v_scale, k_mean, v_mean,
+                   qmu, ties);
 }
 
 int orc_prep(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* perm,

@@ -85,6 +85,26 @@ def test_e4m3_tie_detector(orc):
     assert not orc.e4m3_is_tie(np.nextafter(mids, np.float32(0))).any()
 
 
+def test_prep_counts_quantiser_ties(orc):
+    """The preprocessing's tie count (R15): a Q block whose largest |q| is 448
+    quantises with inv = 1, so q = 1.0625 (halfway between the E4M3 values 1
+    and 1.125) is a tie and 448, 1.0 and 0 are not; a constant K centres to
+    zero and a constant V leaves a zero residual (no quantiser input at all)."""
+    N = 64
+    q = np.zeros((1, N, 128), np.float32)
+    q[0, 0, 0] = 448.0
+    q[0, 1:11, 3] = 1.0625
+    q[0, 11:20, 5] = 1.0
+    k = np.full((1, N, 128), 0.75, np.float32)
+    v = np.full((1, N, 128), -2.5, np.float32)
+    bits = [W.bf16_bits(torch.from_numpy(t).to(torch.bfloat16)) for t in (q, k, v)]
+    out = orc.prep(*bits, count_ties=True)
+    assert out["ties"].tolist() == [[10, 0, 0]]
+    plain = orc.prep(*bits)
+    for key in plain:
+        assert np.array_equal(plain[key], out[key]), key
+
+
 # ------------------------------------------------------------------- ExpCast
 @pytest.mark.parametrize("off", [0, 8])
 def test_expcast_round_trip_identity(orc, off):
