@@ -528,7 +528,11 @@ def test_live_workload_all_heads(vc, orc):
     """The 32,626-token workload in the launch configuration the benchmark
     times (all 56 heads in one call): labels, permutation and every prepped
     tensor (bytes, scales, means, k_mean, qmu) bit-exact on every head; 64
-    evenly spaced queries of every head against both oracles."""
+    evenly spaced queries of every head against both oracles.  The rounding
+    ties are counted and reported: E4M3 quantiser inputs exactly halfway
+    between two codes (where the bytes still agree, both sides rounding half
+    to even), and tokens whose last k-means assignment has two equal best
+    scores (where the labels still agree, the lower cluster winning)."""
     w = W.WORKLOADS["live"]
     sm = float(np.float32(w.sm_scale))
     Q, K, V = W.make_workload(w, device="cuda")
@@ -544,12 +548,26 @@ def test_live_workload_all_heads(vc, orc):
     op = orc.stable_sort(ol, w.k)
     assert np.array_equal(labels[0].cpu().numpy(), ol)
     assert np.array_equal(perm[0].cpu().numpy(), op)
-    opp = orc.prep(Qa, Ka, Va, op)
+    opp = orc.prep(Qa, Ka, Va, op, count_ties=True)
     for key in PREP_KEYS:
         g, r = views[key], opp[key]
         if g.dtype == np.float32:
             g, r = g.view(np.uint32), r.view(np.uint32)
         assert np.array_equal(g, r), key
+    ties = opp["ties"].sum(axis=0)
+    # the last assignment scores each token against the centroids of the
+    # iteration before it
+    _, cprev = orc.kmeans(Va, w.k, w.iters - 1)
+    score_ties = 0
+    for h in range(w.H):
+        sc = orc.kmeans_scores(Va[h], cprev[h])
+        best = sc.max(axis=1, keepdims=True)
+        tied = (sc == best).sum(axis=1) > 1
+        score_ties += int(tied.sum())
+        # a tied token goes to the lowest tied cluster
+        assert np.array_equal(ol[h][tied], np.argmax(sc[tied] == best[tied], axis=1))
+    print("live, all 56 heads: E4M3 rounding ties Q %d, K %d, V residual %d (bytes equal at all); "
+          "k-means score ties %d (labels equal at all)" % (ties[0], ties[1], ties[2], score_ties))
     O32h, Lh = O32[0].cpu().numpy(), L[0].cpu().numpy()
     worst = 0.0
     for h in range(w.H):
