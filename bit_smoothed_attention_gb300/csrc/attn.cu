@@ -500,17 +500,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float m_new, alpha;
       bool resc;
       {
-        {
-          uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
-          uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
-          uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[64]);
-          uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[96]);
-          tmem_ld32(tS + 0, c0);
-          tmem_ld32(tS + 32, c1);
-          tmem_ld32(tS + 64, c2);
-          tmem_ld32(tS + 96, c3);
-          tmem_wait_ld();
-        }
+        tmem_ld128(tS, *reinterpret_cast<uint32_t(*)[128]>(&x[0]));
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_STAKEN + slot));  // S may be overwritten
@@ -1093,13 +1084,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       float x[64];
       uint32_t w[16];
-      {
-        uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
-        uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
-        tmem_ld32(tS + 0, c0);
-        tmem_ld32(tS + 32, c1);
-        tmem_wait_ld();
-      }
+      tmem_ld64(tS, *reinterpret_cast<uint32_t(*)[64]>(&x[0]));
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_STAKEN));  // S may be overwritten
@@ -1162,15 +1148,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float ls = ld_rowsum();
         asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tL), "r"(0u) : "memory");
         if (__any_sync(FULL, resc)) {
-          uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[0]);
-          uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[32]);
-          tmem_ld32(tO + 64 * hf, o0);
-          tmem_ld32(tO + 64 * hf + 32, o1);
+          uint32_t (&o)[64] = *reinterpret_cast<uint32_t(*)[64]>(&x[0]);
+          tmem_ld64(tO + 64 * hf, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 64; ++e) x[e] *= alpha;
-          tmem_st32(tO + 64 * hf, o0);
-          tmem_st32(tO + 64 * hf + 32, o1);
+          tmem_st64(tO + 64 * hf, o);
         }
         lh = (lh + ls) * alpha;
         put_lrow(ls * alpha);
