@@ -302,13 +302,8 @@ __global__ void __launch_bounds__(KT_THREADS, 2)
       }
       tc_fence_after();
       float T[64];
-      {
-        uint32_t (&u0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&T[0]);
-        uint32_t (&u1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&T[32]);
-        tmem_ld32(tmem + lane_addr + 64 * b, u0);
-        tmem_ld32(tmem + lane_addr + 64 * b + 32, u1);
-        tmem_wait_ld();
-      }
+      tmem_ld64(tmem + lane_addr + 64 * b, *reinterpret_cast<uint32_t(*)[64]>(&T[0]));
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(KB_DEMPTY + b));
