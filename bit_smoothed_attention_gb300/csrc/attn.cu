@@ -462,7 +462,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float g0 = to_tf32(v0 - h0), g1 = to_tf32(v1 - h1);
       *reinterpret_cast<float4*>(Lrow) = make_float4(h0, g0, h0, 0.0f);
       *reinterpret_cast<float4*>(Lrow + 128) = make_float4(h1, g1, h1, 0.0f);
-      fence_proxy_async_smem();
     };
     float m_run = NEG_INF;
     float l = 0.0f;
@@ -620,6 +619,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ld_rowsums(l0, l1);
         l += l0 + l1;
         put_lrow(l0, l1);
+        fence_proxy_async_smem();  // the mean operand to the tensor core
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
