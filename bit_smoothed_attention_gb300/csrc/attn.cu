@@ -695,16 +695,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // Once one tile has no steps left, the other goes on alone: the finished
 // tile's blocks are replaced by a block of the step that is present (finite
 // bytes) and its rows cast nothing.  An odd last step has an empty second
-// block, filled the same way.  The arithmetic of each row is that of its own
-// query tile's steps, as in the two-slot kernel; the tensor cores do no work
-// for another tile's rows beyond the zero quadrants of P.
+// block, filled the same way.  Each row's arithmetic is that of its own
+// query tile's steps, done as in the dense kernel; the tensor cores do no
+// work for another tile's rows beyond the zero quadrants of P.
 //
 // Warp 0 issues the QKs from one lane and allocates TMEM (512 columns: S
 // [0,256), O [256,400)), warp 2 issues the mean and PV MMAs from one lane,
 // warp 1 issues the TMA loads through three rings (K and V of two stages,
-// the mean tiles of three, each with barriers of its own), and warps 4-7 run
-// the softmax, thread = row = TMEM lane.  The single S buffer is taken by
-// the next QK as soon as the softmax holds S in registers.
+// the mean tiles of three, each with barriers of its own), and warps 4-11
+// run the softmax, two threads per row (TMEM lane): warps 4-7 take the first
+// block of each row's step, warps 8-11 the second.  The single S buffer is
+// taken by the next QK as soon as the softmax holds S in registers.
 namespace sp {
 constexpr int NTHREADS = 384;
 constexpr int WARP_MMA = 0, WARP_TMA = 1, WARP_PV = 2, WARP_SOFTMAX = 4;
