@@ -41,7 +41,7 @@
 // is computed while the softmax of the current one runs, and the softmax of
 // slot s does
 //   wait S(t), load it, release S -> max -> ExpCast -> wait PV(t-1) ->
-//   P(t) to TMEM, read and clear the row sums of t-1, (rare) rescale O,
+//   P(t) to shared memory, read and clear the row sums of t-1, (rare) rescale O,
 //   write the mean operand of t-1 -> release P(t) and the mean operand.
 // The row sums of tile t-1 are read one tile late, so no softmax waits for
 // its own PV; when the running maximum moves at tile t, O (which then holds
