@@ -35,7 +35,7 @@
 // stage only after both mean terms of its tile.
 //
 // S is a single TMEM buffer that the two slots take in turn (S0(t), S1(t),
-// S0(t+1), ...).  Per KV tile t the MMA lane issues
+// S0(t+1), ...).  Per KV tile t the two MMA lanes (slot 0's, slot 1's) issue
 //   QK_0(t+1) | MEAN_0(t-1) PV_0(t) | QK_1(t+1) | MEAN_1(t-1) PV_1(t)
 // each QK as soon as the other slot holds its S in registers, so the next S
 // is computed while the softmax of the current one runs, and the softmax of
