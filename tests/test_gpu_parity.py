@@ -373,6 +373,17 @@ def test_attn_mask_parity(vc, orc):
     assert np.all(g32[192:256] == 0) and np.all(np.isneginf(res[0][2][192:256]))
 
 
+@pytest.mark.parametrize("tau8", [0.0, 4.0])
+def test_attn_mask_rescale_threshold_parity(vc, orc, tau8):
+    """The block-sparse kernel with the exact running maximum (tau8 = 0,
+    every rising maximum rescales O and l) and a lower lazy threshold: its
+    rescale path (each of a row's two threads rescales its half of O) against
+    the oracle replaying the same rule."""
+    N, H = 1500, 2
+    mask = np.asarray(W.make_tile_mask(1, H, N, 557, keep_frac=0.4), np.uint8).copy()
+    _check_attn(_attn_case(vc, orc, N, H, 8, 406, mask=mask, tau8=tau8))
+
+
 def test_attn_mask_empty_slot(vc, orc):
     """Both query tiles of one 128-row slot keep no block (that slot has no
     KV tile at all) while the other slot of the same CTA, and other CTAs,
