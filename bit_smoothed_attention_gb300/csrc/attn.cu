@@ -68,7 +68,7 @@ namespace vc {
 namespace {
 
 constexpr int NS = 4;          // K/V/mean pipeline stages
-constexpr int NTHREADS = 384;  // one MMA warp per slot, two TMA warps, 8 softmax warps
+constexpr int NTHREADS = 384;  // one MMA warp per slot, one TMA warp, one idle, 8 softmax warps
 constexpr int WARP_MMA = 0;    // + slot
 constexpr int WARP_TMA = 2;
 constexpr int WARP_SOFTMAX = 4;
@@ -488,8 +488,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float A1 = a_i * ks.y;
       // Warp-uniform: does the tile hold keys past N (the last block of the
       // sequence, or an empty second half)?  Only then are keys masked one
-      // by one; a 64-key block that a row does not keep is dropped as a
-      // whole (no max contribution, bytes cleared).
+      // by one; a row past N keeps no block (no max contribution, code 0).
       const bool partial = !__all_sync(FULL, lim_lo >= BLK && lim_hi >= TILE);
 
       if (!(ok = __all_sync(FULL, mbar_wait(bar(B_SFULL + slot), i & 1, abort, WAIT_NS)))) break;
@@ -528,7 +527,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         resc = need && m_run != NEG_INF;
         alpha = resc ? exp2f((m_run - m_new) * 0.125f) : 1.0f;
 
-        // ExpCast -> 32 words of E4M3 bytes.  A dropped block, and a row with
+        // ExpCast -> 32 words of E4M3 bytes.  A row past N, and a row with
         // no key kept so far, cast with A = B = 0: t = 0, every code 0 (the
         // scores are finite).  In the partial tile the -inf scores are
         // replaced by 0 and the bytes of keys past N are cleared after the
