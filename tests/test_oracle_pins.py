@@ -152,6 +152,18 @@ def test_expcast_underflow_and_clip(orc):
     assert out[4] == 126 and out[5] == 126
 
 
+def test_expcast_half_integers_round_to_even(orc):
+    """The integer conversion of ExpCast rounds half to even (the default
+    rounding of a float-to-integer conversion): every half-integer t in
+    [7.5, 126.5] gives numpy's round-half-even of t, then the flush below 8
+    and the clip at 126."""
+    t = np.arange(7, 127, dtype=np.float32) + np.float32(0.5)   # exact in FP32
+    out = orc.expcast(t, 1.0, 0.0)                                # fmaf(t, 1, 0) = t
+    k = np.rint(t.astype(np.float64))                             # half to even
+    want = np.where(k < 8, 0, np.minimum(k, 126)).astype(np.uint8)
+    assert np.array_equal(out, want)
+
+
 def _row_tv(orc, logits2, off=8):
     """Exact vs ExpCast distributions for one row of log2-domain scores."""
     C = orc.expcast_C(off)
