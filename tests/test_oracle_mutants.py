@@ -82,15 +82,28 @@ MUTANTS = [
     ("dense without the softmax scale", "s[j] = dot * (double)sm_scale;", "s[j] = dot;"),
     ("dense mask transposed", "mask[(i / ORC_BLK) * nbp + p / ORC_BLK]", "mask[(p / ORC_BLK) * nbp + i / ORC_BLK]"),
     ("dense LSE in natural log", "lse2[qi] = (mx + log(l)) * 1.4426950408889634;", "lse2[qi] = (mx + log(l));"),
+    ("emulated ExpCast constant", "const float C = (float)(56.0 + 8.0 * off - 8.0 * orc_expcast_cstar());",
+     "const float C = (float)(56.0 + 8.0 * off + 8.0 * orc_expcast_cstar());"),
+    ("score coefficient without the softmax scale",
+     "const float c0 = (float)(8.0 * 1.4426950408889634 * (double)sm_scale);",
+     "const float c0 = (float)(8.0 * 1.4426950408889634);"),
+    ("keys past N kept", "valid[jj] = kept[h] && (j < N);", "valid[jj] = kept[h];"),
+    ("empty row LSE", "lse2[qi] = -INFINITY;\n    }\n  }\n  return 0;", "lse2[qi] = 0.0;\n    }\n  }\n  return 0;"),
+    # tree sums, k-means partials, zero-block rule
+    ("tree sum reads the first half twice", "float b = tree_sum_f32(x + h, h);", "float b = tree_sum_f32(x, h);"),
+    ("chunk partials not reset", "memset(part, 0, (size_t)k * ORC_D * sizeof(float));", ";"),
+    ("zero-block rule dropped", "if (!(amax >= AMAX_FLOOR)) {\n    for (int64_t r",
+     "if (!(amax >= 0.0f)) {\n    for (int64_t r"),
     # QK Hadamard
     ("butterfly sign", "x[i + h] = a - b;", "x[i + h] = b - a;"),
+    ("K rotation scale", "xf[j * ORC_D + d] *= 0.125f;", "xf[j * ORC_D + d] *= 0.0625f;"),
     ("Q rotation scale", "for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] *= 0.0625f;",
      "for (int d = 0; d < ORC_D; ++d) xf[j * ORC_D + d] *= 0.125f;"),
 ]
 
 
 def _run_pins(lib):
-    env = dict(os.environ, OMP_NUM_THREADS="2")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OMP_WAIT_POLICY="passive")
     env[ob.ENV_LIB] = lib
     r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider", "-k", FAST],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
@@ -127,7 +140,7 @@ def test_unmodified_oracle_passes_the_fast_pins(libs):
 
 def test_every_planted_mistake_fails_a_pin(libs):
     names = [m[0] for m in MUTANTS]
-    with cf.ThreadPoolExecutor(4) as ex:
+    with cf.ThreadPoolExecutor(max(2, min(8, os.cpu_count() or 2))) as ex:
         results = dict(zip(names, ex.map(lambda n: _run_pins(libs[n]), names)))
     # exit status 1: tests ran and at least one failed (not a crash or an
     # error in collecting them)
