@@ -51,6 +51,32 @@ __global__ void km_init(const uint16_t* __restrict__ V, RowLayout lv, int64_t N,
 // +0 partial, 16-byte loads straight from global memory, several in flight
 // (the 16 threads of a cluster group read a whole 256-byte row).  grid
 // (nchunk, BH), block 256.
+// L2 eviction priorities: the chunk sums stream V through once (evict
+// first), and their partials are read back by km_finalize right after
+// (evict last).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_l2hint(const void* ptr, uint64_t pol) {
+  uint4 r;
+  asm("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(ptr), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ void st_l2hint(void* ptr, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V, RowLayout lv,
                                                   const int32_t* __restrict__ labels, int64_t N,
                                                   int k, int nchunk, float* __restrict__ part,
@@ -113,6 +139,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
   const uint16_t* vb = V + lv.head(bh) + lv.row(j0) + 8 * q;
   // partials [BH, k, nchunk, D]: a cluster's chunks side by side
   float* pg = part + (bh * k * static_cast<int64_t>(nchunk) + g) * D;
+  const uint64_t pol_v = l2_evict_first(), pol_p = l2_evict_last();
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
     const int c = 4 * cg + cc;
@@ -125,7 +152,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
     for (; i + 8 <= i1; i += 8) {
       uint4 u[8];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) u[x] = *reinterpret_cast<const uint4*>(vb + lv.row(order[i + x]));
+      for (int x = 0; x < 8; ++x) u[x] = ld_l2hint(vb + lv.row(order[i + x]), pol_v);
 #pragma unroll
       for (int x = 0; x < 8; ++x) {
         const uint32_t w4[4] = {u[x].x, u[x].y, u[x].z, u[x].w};
@@ -137,7 +164,7 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
       }
     }
     for (; i < i1; ++i) {
-      const uint4 u = *reinterpret_cast<const uint4*>(vb + lv.row(order[i]));
+      const uint4 u = ld_l2hint(vb + lv.row(order[i]), pol_v);
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -146,8 +173,8 @@ __global__ void __launch_bounds__(256) km_partial(const uint16_t* __restrict__ V
       }
     }
     float* dst = pg + static_cast<int64_t>(c) * nchunk * D + 8 * q;
-    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    st_l2hint(dst, make_float4(acc[0], acc[1], acc[2], acc[3]), pol_p);
+    st_l2hint(dst + 4, make_float4(acc[4], acc[5], acc[6], acc[7]), pol_p);
     if (q == 0) cnt[(bh * nchunk + g) * k + c] = i1 - cstart[c];
   }
 }
