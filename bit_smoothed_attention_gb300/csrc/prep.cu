@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(D * KM_SEG) prep_kmean(const float* __restrict
   }
 }
 
-// Quantisers, one tensor per CTA (blockIdx.z: 0 = Q, 1 = K, 2 = V).  Each CTA
+// Quantisers, one tensor per CTA (blockIdx.y: 0 = Q, 1 = K, 2 = V).  Each CTA
 // handles QUANT_BPC consecutive 64-token blocks of one (b, h) through a ring
 // of QUANT_NST staged tiles (16 KiB each, all rows of a tile in flight at
 // once), so QUANT_NST - 1 blocks load while one is quantised.  One tensor per
@@ -376,8 +376,11 @@ __global__ void __launch_bounds__(D * KM_SEG) prep_kmean(const float* __restrict
 // The FP32 operations and their order are those of the per-element
 // definition (packed f32x2 instructions round each lane as the scalar ones
 // do).  With the QK Hadamard flag the Q and K paths rotate first (four lanes
-// per row, as in hadamard_row32).  grid (ceil(nbp / QUANT_BPC), BH, 3),
-// block 256, dynamic shared memory QUANT_SMEM.
+// per row, as in hadamard_row32).  grid (ceil(nbp / QUANT_BPC), 3, BH),
+// block 256, dynamic shared memory QUANT_SMEM: the heads in reverse order
+// with the three tensors of a head together, so that the first heads
+// quantised are the last ones prep_stats read, whose K and V are still in
+// L2.
 constexpr int QUANT_BPC = 8;
 constexpr int QUANT_NST = 3;
 constexpr int QUANT_SMEM = QUANT_NST * TILE_SMEM + D * (BLK + 16) + D * 4 + 64;
@@ -414,11 +417,11 @@ __global__ void __launch_bounds__(256, 3) prep_quant(
   uint8_t (*tb)[BLK + 16] = reinterpret_cast<uint8_t (*)[BLK + 16]>(qsm + QUANT_NST * TILE_SMEM);
   float* kmu = reinterpret_cast<float*>(qsm + QUANT_NST * TILE_SMEM + D * (BLK + 16));
   float* red = kmu + D;
-  const int z = blockIdx.z;  // 0 = Q, 1 = K, 2 = V
+  const int z = blockIdx.y;  // 0 = Q, 1 = K, 2 = V
   // V keeps the token-group lanes (its transposed bytes go to shared memory
   // without bank conflicts); Q and K take the coalescing mapping
   const Map m = z == 2 ? thread_map() : quant_map();
-  const int64_t bh = blockIdx.y;
+  const int64_t bh = gridDim.z - 1 - blockIdx.z;  // heads in reverse order
   const int64_t nb = ceil_div(N, BLK);
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * QUANT_BPC;
   const int64_t b1 = b0 + QUANT_BPC < nbp ? b0 + QUANT_BPC : nbp;
@@ -674,7 +677,7 @@ cudaError_t launch_prep(const uint16_t* Q, const RowLayout& lq, const uint16_t* 
                STATS_SMEM, s>>>(K, lk, V, lv, perm, N, nb, nbp, ws.kbs, o.v_mean, ws.vamax, err);
   prep_kmean<<<static_cast<unsigned>(BH), dim3(D, KM_SEG), 0, s>>>(ws.kbs, ws.vamax, N, nb, nbp,
                                                                    o.k_mean, o.v_scale);
-  prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), static_cast<unsigned>(BH), 3), 256,
+  prep_quant<<<dim3(static_cast<unsigned>(ceil_div(nbp, QUANT_BPC)), 3, static_cast<unsigned>(BH)), 256,
                QUANT_SMEM, s>>>(
       Q, lq, K, lk, V, lv, perm, N, Np, nbp, ws.vamax, o.k_mean, o.v_scale, o.v_mean, o.q8, o.k8, o.r8t,
       o.q_scale, o.k_scale, o.qmu, o.vmu_op, err, (flags & PREP_QK_HADAMARD) != 0);
