@@ -486,6 +486,26 @@ def test_emul_exact_exp_equals_softmax_of_dequantised(orc, N):
     assert np.allclose(lq, lse2, rtol=0, atol=1e-9)
 
 
+def test_single_block_is_global_v_centring(orc):
+    """With one 64-token block over the whole sequence the block mean is the
+    sequence mean of V, and the restoration reduces to plain V centring: the
+    output equals attention on the centred (residual) values plus the mean,
+    since every softmax row sums to 1."""
+    N = 50
+    Q, K, V = _small_inputs(N=N, H=1, seed=55)
+    pp = orc.prep(Q, K, V, None)
+    mu = pp["v_mean"][0][0].astype(np.float64)
+    v64 = torch.from_numpy(V[0].view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.allclose(mu, v64.mean(0), rtol=1e-6, atol=1e-6)
+    O1, _ = orc.attn_emul(pp, 0, N, SM, flags=1)
+    q, k, _ = _deq(orc, pp, 0, N)
+    resid = orc.e4m3_decode(pp["r8t"][0][:, :N]).T * pp["v_scale"][0].astype(np.float64)
+    o_res, _ = _softmax_attn(q, k, resid, SM)
+    assert np.allclose(O1, o_res + mu[None, :], rtol=1e-10, atol=1e-10)
+    # the centred values carry (almost) no mean: what is left is E4M3 rounding
+    assert np.abs(resid.mean(0)).max() <= 0.02 * np.abs(v64).max()
+
+
 def test_emul_mask_and_empty_rows(orc):
     N = 300
     Q, K, V = _small_inputs(N=N, H=1, seed=40)
